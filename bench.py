@@ -1,0 +1,444 @@
+#!/usr/bin/env python3
+"""Benchmark of one LoGRA optimiser step on GB300: sketch every microbatch of
+every compressed matrix, then apply RowAdam from the sketch.
+
+A step covers, for each layer and each projection matrix (q, k, v, o, gate,
+up, down): zero S, one logra_sketch_accumulate per microbatch, then one
+logra_rowadam_apply_ex (fp32 master W, bf16 working copy, v, norms).  Inputs
+(bf16 X and dY for every microbatch) are resident in HBM before timing; they
+are far larger than L2, so no L2 flush is needed between steps.
+
+Default workload: 4 decoder layers of 27B-class shapes (q/o 5120x5120, k/v
+1024x5120, gate/up 27648x5120, down 5120x27648), r = 256, 16 microbatches x
+8192 tokens, 30% padding rows; the largest workload whose inputs fit in one
+GPU's memory.  The metric is sketch TFLOP/s over the whole step (algorithmic
+sketch FLOPs 2 n r (k + d) per matrix-microbatch, divided by the step time
+including the apply), with the apply's GB/s and both kernels' roofline
+fractions alongside.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank sketches its own microbatches (weak
+scaling), all-reduces each S, then applies; rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sketch TFLOP/s + fused RowAdam-apply GB/s per GB300; % of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=5)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--workload", default="layers27b")
+    p.add_argument("--rank", type=int, default=256)
+    p.add_argument("--layers", type=int, default=None, help="override the workload's layer count")
+    p.add_argument("--e2e-steps", type=int, default=2)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    return p.parse_args(argv)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------- work accounting
+def sketch_work(n, d, k, r):
+    """Algorithmic FLOPs and bytes of one matrix-microbatch sketch (bf16 X, dY; fp32 S RMW)."""
+    return 2.0 * n * r * (k + d), 2.0 * n * (k + d) + 2.0 * d * r * 4
+
+
+def apply_work(d, k, r):
+    """Algorithmic FLOPs and bytes of one apply: W fp32 RMW + bf16 copy + S read + v RMW."""
+    return 2.0 * d * k * r, d * k * (4 + 4 + 2) + d * r * 4 + 2.0 * d * 4
+
+
+# ----------------------------------------------------------------------------- clocks
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+def time_oracle(w, r, seconds, host_seed=0):
+    """Time the fp64 oracle on a bounded sample of the workload: microbatches of
+    the q matrix (d = k = hidden) until ``seconds`` pass, plus one apply of that
+    matrix; extrapolate to the step's ratio of microbatches to applies."""
+    import numpy as np
+    from oracle import logra_oracle as O
+    from rank_gradient_sketching_02_gb300 import synth
+    name, d, k = w.matrices[0]
+    n = w.tokens
+    X, dY, _ = synth.host_microbatch(n, d, k, dy_kind=w.dy_kind, dy_std=w.dy_std, mask_frac=w.mask_frac,
+                                     key=(host_seed, 0, 0, 0))
+    X64 = synth.to_bf16_bits(X).double().numpy()
+    dY64 = synth.to_bf16_bits(dY).double().numpy()
+    S = np.zeros((d, r))
+    t0 = time.perf_counter()
+    mbs = 0
+    while True:
+        S = O.sketch_accumulate(S, X64, dY64, 1, 0, r)
+        mbs += 1
+        if time.perf_counter() - t0 >= seconds * 0.75:
+            break
+    t_mb = (time.perf_counter() - t0) / mbs
+    W = np.zeros((d, k))
+    t1 = time.perf_counter()
+    O.rowadam_apply(W, S, np.zeros(d), 1, 0, 0.999, 1e-8, 1e-6, 1.0)
+    t_apply = time.perf_counter() - t1
+    f_mb, _ = sketch_work(n, d, k, r)
+    _, b_apply = apply_work(d, k, r)
+    t_unit = w.microbatches * t_mb + t_apply        # one matrix, one step
+    value = w.microbatches * f_mb / t_unit / 1e12
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": (f"fp64 numpy oracle on the {name} matrix ({d}x{k}, r={r}): {mbs} microbatch sketches of "
+                       f"{n} tokens ({t_mb:.2f} s each) and one apply ({t_apply:.2f} s, "
+                       f"{b_apply / t_apply / 1e9:.2f} GB/s); value = {w.microbatches} microbatches' sketch "
+                       f"FLOPs / ({w.microbatches} sketches + 1 apply)")}
+
+
+def run_reference(args):
+    """Reference arm: the fp64 CPU oracle, as it stands, on the machine's host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from rank_gradient_sketching_02_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    r = args.rank
+    per_step = max(2.0, args.cpu_seconds / 2)
+    for _ in range(args.warmup):
+        time_oracle(w, r, 0.5)
+    vals = []
+    t0 = time.perf_counter()
+    res = None
+    for _ in range(args.steps):
+        res = time_oracle(w, r, per_step)
+        vals.append(res["value"])
+    wall = time.perf_counter() - t0
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": w.name, "r": r, "tokens": w.tokens, "microbatches": w.microbatches},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": res["cores"], "kind": "oracle",
+                             "sample": res["sample"]},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import rank_gradient_sketching_02_gb300 as L
+    from rank_gradient_sketching_02_gb300 import dp, synth
+
+    w = synth.WORKLOADS[args.workload]
+    r = args.rank
+    layers = args.layers or w.layers
+    n, nmb = w.tokens, w.microbatches
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    dev = torch.device("cuda", local)
+    beta2, eps, lr, c = synth.BETA2, synth.EPS, synth.LR, synth.C
+
+    # ---- resident state and inputs
+    mats = []
+    for layer in range(layers):
+        for mi, (name, d, k) in enumerate(w.matrices):
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(1000 + 16 * layer + mi)
+            W = torch.empty((d, k), dtype=torch.float32, device=dev).normal_(0.0, 0.02, generator=gen)
+            m = {"name": name, "layer": layer, "d": d, "k": k, "seed": synth.matrix_seed(2026, layer, mi), "W": W,
+                 "Wb": W.to(torch.bfloat16), "v": torch.zeros(d, dtype=torch.float32, device=dev),
+                 "S": torch.zeros((d, r), dtype=torch.float32, device=dev),
+                 "norms": torch.zeros(2, dtype=torch.float64, device=dev),
+                 "X": torch.empty((nmb, n, k), dtype=dt, device=dev),
+                 "dY": torch.empty((nmb, n, d), dtype=dt, device=dev)}
+            for mb in range(nmb):
+                synth.device_microbatch(n, d, k, dy_kind=w.dy_kind, dy_std=w.dy_std, mask_frac=w.mask_frac,
+                                        key=(2026, rank, layer, mi, mb), dtype=dt, device=dev,
+                                        out_X=m["X"][mb], out_dY=m["dY"][mb])
+            mats.append(m)
+    torch.cuda.synchronize()
+    input_bytes = sum(m["X"].numel() * m["X"].element_size() + m["dY"].numel() * m["dY"].element_size() for m in mats)
+
+    stream = torch.cuda.current_stream()
+    # pre-size the per-stream workspace so no allocation happens while timing
+    ws = max(max(L.lib().logra_sketch_workspace_bytes(n, m["d"], m["k"], r, 1 if dt == torch.bfloat16 else 0),
+                 L.lib().logra_apply_workspace_bytes(m["d"], m["k"], r)) for m in mats)
+    L.logra_reserve_workspace(ws)
+
+    def one_step(step_idx, ev=None):
+        for m in mats:
+            m["S"].zero_()
+            for mb in range(nmb):
+                if ev is not None:
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                L.logra_sketch_accumulate(m["X"][mb], m["dY"][mb], m["S"], m["seed"], step_idx)
+                if ev is not None:
+                    b.record(stream)
+                    ev["sketch"].append((a, b, m["d"], m["k"]))
+            dp.allreduce_sketch(m["S"])
+            if ev is not None:
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+            L.logra_rowadam_apply_ex(m["W"], m["S"], m["v"], m["seed"], step_idx, beta2, eps, lr, c, m["norms"],
+                                     m["Wb"], None)
+            if ev is not None:
+                b.record(stream)
+                ev["apply"].append((a, b, m["d"], m["k"]))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for s in range(args.warmup):
+        one_step(s)
+    torch.cuda.synchronize()
+    if L.logra_get_status() != 0:
+        raise RuntimeError("device status word set during warm-up")
+    barrier()
+    torch.cuda.synchronize()
+
+    ev = {"sketch": [], "apply": []}
+    clocks = Clocks(local)
+    launches0 = L.logra_launch_count()
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        one_step(args.warmup + s, ev)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    launches = L.logra_launch_count() - launches0
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_step = elapsed_ms / args.steps
+    status = L.logra_get_status()
+
+    # ---- accounting
+    sk_f = sk_b = ap_f = ap_b = 0.0
+    for m in mats:
+        f, b = sketch_work(n, m["d"], m["k"], r)
+        sk_f += nmb * f
+        sk_b += nmb * b
+        f, b = apply_work(m["d"], m["k"], r)
+        ap_f += f
+        ap_b += b
+    sk_ms = sum(a.elapsed_time(b) for a, b, _, _ in ev["sketch"]) / args.steps
+    ap_ms = sum(a.elapsed_time(b) for a, b, _, _ in ev["apply"]) / args.steps
+    peaks, peak_kind = load_peaks()
+    hbm, tc = float(peaks["hbm_gbs"]), float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    value = world * sk_f / (ms_step * 1e-3) / 1e12
+
+    sk_tflops = sk_f / (sk_ms * 1e-3) / 1e12
+    sk_gbs = sk_b / (sk_ms * 1e-3) / 1e9
+    ap_gbs = ap_b / (ap_ms * 1e-3) / 1e9
+    sk_bound = "tensor" if sk_f / (tc * 1e12) > sk_b / (hbm * 1e9) else "hbm"
+    sk_roof_ms = 1e3 * max(sk_f / (tc * 1e12), sk_b / (hbm * 1e9))
+    ap_roof_ms = 1e3 * max(ap_f / (tc * 1e12), ap_b / (hbm * 1e9))
+    if sk_bound == "hbm":
+        roof = {"bound": "hbm", "achieved": sk_gbs, "peak": hbm, "unit": "GB/s", "frac": sk_gbs / hbm}
+    else:
+        roof = {"bound": "tensor", "achieved": sk_tflops, "peak": tc, "unit": "TFLOP/s", "frac": sk_tflops / tc}
+    roof.update({"traffic": None, "kernel": "logra_sketch_accumulate (project + accumulate launches)",
+                 "peak_source": f"{peak_kind} ({'MEASURED_PEAKS.json' if peak_kind == 'measured' else 'fallback'})"})
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; torch Philox on device)",
+        "config": {"workload": w.name, "layers": layers, "matrices": [list(x) for x in w.matrices],
+                   "microbatches": nmb, "tokens": n, "r": r, "mask_frac": w.mask_frac,
+                   "input_bytes_resident": input_bytes, "l2": "inputs larger than L2, no flush",
+                   "parallelism": f"dp{world}"},
+        "components": {
+            "sketch": {"ms_per_step": sk_ms, "tflops": sk_tflops, "gbs": sk_gbs,
+                       "frac_of_roofline": sk_roof_ms / sk_ms, "roofline_ms": sk_roof_ms},
+            "apply": {"ms_per_step": ap_ms, "gbs": ap_gbs, "frac_hbm": ap_gbs / hbm,
+                      "frac_of_roofline": ap_roof_ms / ap_ms, "roofline_ms": ap_roof_ms},
+        },
+        "roofline": roof,
+        "gpu_launches": launches,
+        "clocks": clk,
+        "device_status": status,
+    }
+
+    # ---- end to end through the public API from pinned host memory
+    if not args.no_e2e:
+        line["e2e"] = run_e2e(args, L, dp, mats, w, r, dt, dev, stream, sk_f, world)
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = time_oracle(w, r, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, L, dp, mats, w, r, dt, dev, stream, sk_f, world):
+    """Same step, but every microbatch's X and dY come from pinned host memory
+    (copied on a side stream, double-buffered) and the norms go back to the host."""
+    import torch
+    from rank_gradient_sketching_02_gb300 import synth
+    beta2, eps, lr, c = synth.BETA2, synth.EPS, synth.LR, synth.C
+    n, nmb = w.tokens, w.microbatches
+    host = {}
+    for m in mats:
+        key = (m["d"], m["k"])
+        if key not in host:
+            host[key] = (m["X"][0].cpu().pin_memory(), m["dY"][0].cpu().pin_memory())
+    maxk = max(m["k"] for m in mats)
+    maxd = max(m["d"] for m in mats)
+    bufX = [torch.empty(n * maxk, dtype=dt, device=dev) for _ in range(2)]
+    bufY = [torch.empty(n * maxd, dtype=dt, device=dev) for _ in range(2)]
+    copy = torch.cuda.Stream(device=dev)
+    norms_h = torch.empty((len(mats), 2), dtype=torch.float64).pin_memory()
+    h2d = d2h = 0
+
+    def e2e_step(step_idx):
+        nonlocal h2d, d2h
+        done = [None, None]
+        i = 0
+        for mi, m in enumerate(mats):
+            Xh, Yh = host[(m["d"], m["k"])]
+            m["S"].zero_()
+            for mb in range(nmb):
+                slot = i % 2
+                with torch.cuda.stream(copy):
+                    if done[slot] is not None:
+                        copy.wait_event(done[slot])
+                    Xd = bufX[slot][: n * m["k"]].view(n, m["k"])
+                    Yd = bufY[slot][: n * m["d"]].view(n, m["d"])
+                    Xd.copy_(Xh, non_blocking=True)
+                    Yd.copy_(Yh, non_blocking=True)
+                    ready = torch.cuda.Event()
+                    ready.record(copy)
+                h2d += Xh.numel() * Xh.element_size() + Yh.numel() * Yh.element_size()
+                stream.wait_event(ready)
+                L.logra_sketch_accumulate(Xd, Yd, m["S"], m["seed"], step_idx)
+                ev = torch.cuda.Event()
+                ev.record(stream)
+                done[slot] = ev
+                i += 1
+            dp.allreduce_sketch(m["S"])
+            L.logra_rowadam_apply_ex(m["W"], m["S"], m["v"], m["seed"], step_idx, beta2, eps, lr, c,
+                                     m["norms"], m["Wb"], None)
+            norms_h[mi].copy_(m["norms"], non_blocking=True)
+            d2h += 16
+        return norms_h
+
+    e2e_step(10_000)
+    torch.cuda.synchronize()
+    h2d = d2h = 0
+    steps = max(1, args.e2e_steps)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s in range(steps):
+        e2e_step(10_001 + s)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    return {"value": world * sk_f / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d // steps, "d2h_bytes_per_step": d2h // steps,
+            "host_inputs": "pinned host copy of one microbatch per matrix shape, re-sent for every microbatch"}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

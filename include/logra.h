@@ -1,0 +1,210 @@
+/*
+ * logra.h -- C ABI of the LoGRA gradient-sketch / RowAdam library (liblogra.so).
+ *
+ * Method: "LoGRA: Scaling LLM Reinforcement Learning with Low-Rank Gradient
+ * Sketches".  A d x k projection weight W is trained without its d x k
+ * gradient G = dY^T X.  During the backward pass every microbatch adds its
+ * contribution to a d x r sketch S += dY^T (X A^T) (theclarity.today write-up,
+ * "Why it matters": S = G * A^T, G d x k, A r x k, r << d, k), where A is a
+ * random-sign matrix redrawn each step and held fixed over that step's
+ * microbatches (academy.dair.ai summary, "Gradient sketches").  At update time
+ * Ghat = S A is rebuilt tile by tile and consumed by RowAdam, which keeps one
+ * running mean-square statistic per row and no first moment (theclarity.today
+ * write-up, "What happened").
+ *
+ * Conventions shared by every call
+ *   - Matrices are dense, row-major, with no padding between rows:
+ *       X  n x k    activations of one microbatch (one row per token)
+ *       dY n x d    output gradients of that microbatch
+ *       W  d x k    fp32 master weight (nn.Linear layout: out x in)
+ *       S  d x r    fp32 sketch
+ *       v  d        fp32 RowAdam second moment, one value per row of W
+ *   - Every pointer is a DEVICE pointer (cudaMalloc / torch CUDA memory) on the
+ *     current device, owned by the caller, except where a comment says "host".
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream) and do
+ *     not synchronise it.  The library keeps no per-matrix state.
+ *   - A = Sigma * fl32(1/sqrt(r)); Sigma[i][j] = +1 or -1, from bit (j mod 64)
+ *     of a 64-bit word hashed from (seed, step, i, j div 64) with SplitMix64
+ *     (set bit -> -1).  A is regenerated inside the kernels and never stored,
+ *     except by logra_sign_matrix.
+ *   - Shape rules: n >= 0; d, k >= 1 and multiples of 8 (16-byte rows for
+ *     bf16 TMA tiles); r a multiple of 32 in [32, 512].  Other shapes return
+ *     LOGRA_ERR_UNSUPPORTED and launch nothing.  n == 0 is a no-op.
+ *   - Pointers must be 16-byte aligned (LOGRA_ERR_UNSUPPORTED otherwise).
+ *   - Return value: a logra_status.  A non-OK status means nothing was
+ *     launched, except LOGRA_ERR_CUDA, which reports a CUDA runtime error
+ *     from the launch itself.  Device-side failures (a bounded wait that gave
+ *     up) are recorded in a per-device status word read by logra_get_status.
+ *   - The library allocates device memory only for an internal scratch
+ *     workspace per (device, stream), grown on demand (on first use of a
+ *     larger shape) and kept for the life of the process;
+ *     logra_reserve_workspace pre-sizes it so that no allocation happens
+ *     later (e.g. inside a stream capture).
+ */
+#ifndef LOGRA_H
+#define LOGRA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* logra_stream_t; /* identical to cudaStream_t */
+
+enum logra_status {
+  LOGRA_OK = 0,
+  LOGRA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad dtype     */
+  LOGRA_ERR_UNSUPPORTED = 2,   /* shape or alignment outside the rules above */
+  LOGRA_ERR_CUDA = 3,          /* CUDA runtime error (see logra_last_cuda_error) */
+  LOGRA_ERR_TIMEOUT = 4,       /* a device-side wait gave up (logra_get_status) */
+  LOGRA_ERR_NO_DEVICE = 5      /* no usable sm_103 device                    */
+};
+
+enum logra_dtype {
+  LOGRA_F32 = 0,   /* IEEE binary32                 */
+  LOGRA_BF16 = 1   /* bfloat16 (raw 16-bit storage) */
+};
+
+/* Text for a status code; never NULL. */
+const char* logra_status_string(int status);
+
+/* cudaError_t of the most recent LOGRA_ERR_CUDA on this thread (0 if none). */
+int logra_last_cuda_error(void);
+
+/* ABI version: (major << 16) | minor. */
+int logra_version(void);
+
+/*
+ * Number of kernels this process has launched through the library so far
+ * (all devices, all streams).  Host-side counter; lets a caller count the
+ * device work behind a sequence of calls.
+ */
+uint64_t logra_launch_count(void);
+
+/*
+ * logra_sign_matrix -- write A = Sigma * fl32(1/sqrt(r)) as an r x k fp32
+ * matrix (A_out, device, r*k floats, row-major).  The random-sign projection
+ * of the academy.dair.ai summary ("Gradient sketches"); used by tests and by
+ * callers that want the explicit matrix.  Bit-exact with any other
+ * implementation of the same hash.  Any k >= 1 is accepted here.
+ */
+int logra_sign_matrix(uint64_t seed, uint64_t step, int r, int64_t k,
+                      float* A_out, logra_stream_t stream);
+
+/*
+ * logra_sketch_accumulate -- S += dY^T (X A^T) for one microbatch.
+ * (theclarity.today write-up, "Why it matters": S = G A^T accumulated during
+ * backpropagation; aitop.news post: the full gradient is never built.)
+ *   X        n x k, dtype in_dtype (LOGRA_BF16 or LOGRA_F32)
+ *   dY       n x d, same dtype
+ *   S        d x r fp32, read and written in place (the caller zeroes it at
+ *            the first microbatch of a step)
+ *   seed     per-matrix seed; step  the optimiser step (A is redrawn per step)
+ * Padding tokens are zero rows of X and dY.  bf16 inputs are multiplied
+ * exactly and accumulated in fp32; the X A^T intermediate is kept as a
+ * two-term bf16 expansion (relative error about 2^-16), fp32 inputs run in fp32.
+ * Uses the internal workspace (r * n * 4 bytes for bf16 inputs).
+ */
+int logra_sketch_accumulate(const void* X, const void* dY, int in_dtype,
+                            int64_t n, int64_t d, int64_t k, int r,
+                            uint64_t seed, uint64_t step, float* S,
+                            logra_stream_t stream);
+
+/*
+ * logra_rowadam_apply -- RowAdam update rebuilt from the sketch:
+ *   Ghat = S A;  v_i <- beta2 v_i + (1-beta2) * mean_j Ghat_ij^2;
+ *   W_ij <- W_ij - lr * c * Ghat_ij / sqrt(v_i + eps).
+ * (theclarity.today write-up, "What happened": per-row squared magnitudes, no
+ * first moment; c is the step scale of the predicted-KL controller, which the
+ * pages do not define, so the caller supplies it.)
+ *   W          d x k fp32 master weight, updated in place
+ *   S          d x r fp32 sketch (read only)
+ *   v          d fp32, updated in place
+ *   norms_out  device, 2 doubles, overwritten: {||S||_F^2, ||dW||_F^2} where
+ *              dW is the fp32 update added to W -- the controller's inputs.
+ *              May be NULL.
+ * Uses the internal workspace (d * 4 + small bytes).
+ */
+int logra_rowadam_apply(float* W, const float* S, float* v, int64_t d,
+                        int64_t k, int r, uint64_t seed, uint64_t step,
+                        float beta2, float eps, float lr, float c,
+                        double* norms_out, logra_stream_t stream);
+
+/*
+ * logra_rowadam_apply_ex -- logra_rowadam_apply plus two optional outputs
+ * (either may be NULL):
+ *   W_bf16_out      d x k bf16 copy of the updated master weight
+ *                   (round to nearest even), the model's working weights.
+ *   sync_sketch_out d x r fp32, S'_i = -lr * c * S_i / sqrt(v_i + eps) with the
+ *                   updated v: logra_reconstruct(S', accumulate=1) on a rollout
+ *                   worker adds the same update to its weights (academy.dair.ai
+ *                   summary: the update is a product of two small matrices,
+ *                   which makes policy synchronisation cheaper).
+ */
+int logra_rowadam_apply_ex(float* W, const float* S, float* v, int64_t d,
+                           int64_t k, int r, uint64_t seed, uint64_t step,
+                           float beta2, float eps, float lr, float c,
+                           double* norms_out, uint16_t* W_bf16_out,
+                           float* sync_sketch_out, logra_stream_t stream);
+
+/*
+ * logra_rowadam_predict -- the norms logra_rowadam_apply would report with
+ * c = 1, writing nothing else (W and v untouched).  Because dW is linear in c,
+ * ||dW(c)||^2 = c^2 * norms_out[1]; a controller can pick c from this before
+ * applying (academy.dair.ai summary, "Step control": the KL change is
+ * predicted before the update is applied).
+ *   norms_out  device, 2 doubles, overwritten.
+ */
+int logra_rowadam_predict(const float* S, const float* v, int64_t d, int64_t k,
+                          int r, uint64_t seed, uint64_t step, float beta2,
+                          float eps, float lr, double* norms_out,
+                          logra_stream_t stream);
+
+/*
+ * logra_reconstruct -- dW_out (+)= S A, the d x k matrix rebuilt from a d x r
+ * sketch (policy synchronisation to rollout workers; academy.dair.ai summary).
+ *   out_dtype  LOGRA_F32 or LOGRA_BF16 (bf16: round to nearest even)
+ *   accumulate 0: overwrite dW_out; 1: dW_out += S A (bf16: computed in fp32,
+ *              rounded once).
+ */
+int logra_reconstruct(const float* S, int64_t d, int64_t k, int r,
+                      uint64_t seed, uint64_t step, void* dW_out,
+                      int out_dtype, int accumulate, logra_stream_t stream);
+
+/*
+ * logra_get_status -- synchronise `stream`, then return and clear the device
+ * status word of the current device: LOGRA_OK, or LOGRA_ERR_TIMEOUT if a
+ * kernel's bounded wait gave up since the last call.
+ */
+int logra_get_status(logra_stream_t stream);
+
+/*
+ * logra_reserve_workspace -- grow the scratch workspace that calls on
+ * (current device, `stream`) use to at least `bytes` now (synchronous
+ * cudaMalloc), so later calls on that stream allocate nothing.  Each
+ * (device, stream) pair has its own workspace, so calls on different streams
+ * may overlap; calls on one stream are ordered by the stream.  Returns
+ * LOGRA_ERR_CUDA if the allocation fails.
+ */
+int logra_reserve_workspace(size_t bytes, logra_stream_t stream);
+
+/* Workspace bytes a sketch / apply call of this shape needs. */
+size_t logra_sketch_workspace_bytes(int64_t n, int64_t d, int64_t k, int r, int in_dtype);
+size_t logra_apply_workspace_bytes(int64_t d, int64_t k, int r);
+
+/*
+ * logra_debug_inject -- TEST ONLY.  fault = 1 makes the next pipelined kernel
+ * launch drop one producer arrival, so that its consumer's bounded wait runs
+ * out and the kernel records LOGRA_ERR_TIMEOUT and exits cleanly (no trap, no
+ * hang); fault = 0 clears it.  The wait limit is `timeout_cycles` clock ticks
+ * (0 keeps the current limit).
+ */
+int logra_debug_inject(int fault, uint64_t timeout_cycles);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LOGRA_H */

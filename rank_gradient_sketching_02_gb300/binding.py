@@ -1,0 +1,192 @@
+"""ctypes binding of liblogra.so: the C entry points under the same names.
+
+Argument marshalling only: tensors are checked (device, dtype, contiguity)
+and passed as raw device pointers with torch's current CUDA stream; every
+step of the computation runs in the library's kernels.  There is no fallback:
+if the library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblogra.so")
+
+LOGRA_OK, LOGRA_ERR_INVALID_ARG, LOGRA_ERR_UNSUPPORTED, LOGRA_ERR_CUDA, LOGRA_ERR_TIMEOUT, LOGRA_ERR_NO_DEVICE = range(6)
+LOGRA_F32, LOGRA_BF16 = 0, 1
+
+# name -> (restype, argtypes) for every entry point of include/logra.h
+_VP, _I, _I64, _U64, _F, _SZ = C.c_void_p, C.c_int, C.c_int64, C.c_uint64, C.c_float, C.c_size_t
+SIGNATURES = {
+    "logra_status_string": (C.c_char_p, [_I]),
+    "logra_last_cuda_error": (_I, []),
+    "logra_version": (_I, []),
+    "logra_launch_count": (_U64, []),
+    "logra_sign_matrix": (_I, [_U64, _U64, _I, _I64, _VP, _VP]),
+    "logra_sketch_accumulate": (_I, [_VP, _VP, _I, _I64, _I64, _I64, _I, _U64, _U64, _VP, _VP]),
+    "logra_rowadam_apply": (_I, [_VP, _VP, _VP, _I64, _I64, _I, _U64, _U64, _F, _F, _F, _F, _VP, _VP]),
+    "logra_rowadam_apply_ex": (_I, [_VP, _VP, _VP, _I64, _I64, _I, _U64, _U64, _F, _F, _F, _F, _VP, _VP, _VP,
+                                    _VP]),
+    "logra_rowadam_predict": (_I, [_VP, _VP, _I64, _I64, _I, _U64, _U64, _F, _F, _F, _VP, _VP]),
+    "logra_reconstruct": (_I, [_VP, _I64, _I64, _I, _U64, _U64, _VP, _I, _I, _VP]),
+    "logra_get_status": (_I, [_VP]),
+    "logra_reserve_workspace": (_I, [_SZ, _VP]),
+    "logra_sketch_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I, _I]),
+    "logra_apply_workspace_bytes": (_SZ, [_I64, _I64, _I]),
+    "logra_debug_inject": (_I, [_I, _U64]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class LograError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = lib().logra_status_string(status).decode()
+        if status == LOGRA_ERR_CUDA:
+            msg += f" (cudaError {lib().logra_last_cuda_error()})"
+        super().__init__(f"{where}: {msg} [status {status}]")
+
+
+def lib():
+    """Load liblogra.so (built in-tree by build.py); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(f"liblogra.so not built ({LIB_PATH}); run the package's build.py")
+                h = C.CDLL(LIB_PATH)
+                for name, (res, args) in SIGNATURES.items():
+                    f = getattr(h, name)
+                    f.restype, f.argtypes = res, args
+                _lib = h
+    return _lib
+
+
+def _check(st: int, where: str):
+    if st != LOGRA_OK:
+        raise LograError(st, where)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dev(t, name, dtypes=None, shape=None):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t.data_ptr()
+
+
+def _in_dtype(t):
+    import torch
+    return {torch.float32: LOGRA_F32, torch.bfloat16: LOGRA_BF16}[t.dtype]
+
+
+def logra_sign_matrix(seed: int, step: int, r: int, k: int, A_out=None, stream=None):
+    import torch
+    if A_out is None:
+        A_out = torch.empty((r, k), dtype=torch.float32, device="cuda")
+    p = _dev(A_out, "A_out", (torch.float32,), (r, k))
+    _check(lib().logra_sign_matrix(seed, step, r, k, p, _stream(stream)), "logra_sign_matrix")
+    return A_out
+
+
+def logra_sketch_accumulate(X, dY, S, seed: int, step: int, stream=None):
+    """S (d x r fp32) += dY^T (X A^T) for one microbatch; X n x k, dY n x d."""
+    import torch
+    n, k = X.shape
+    d, r = S.shape
+    dt = (torch.float32, torch.bfloat16)
+    px = _dev(X, "X", dt)
+    py = _dev(dY, "dY", (X.dtype,), (n, d))
+    ps = _dev(S, "S", (torch.float32,))
+    _check(lib().logra_sketch_accumulate(px, py, _in_dtype(X), n, d, k, r, seed, step, ps, _stream(stream)),
+           "logra_sketch_accumulate")
+    return S
+
+
+def logra_rowadam_apply(W, S, v, seed: int, step: int, beta2: float, eps: float, lr: float, c: float,
+                        norms_out=None, stream=None):
+    import torch
+    d, k = W.shape
+    r = S.shape[1]
+    f32 = (torch.float32,)
+    pw = _dev(W, "W", f32)
+    ps = _dev(S, "S", f32, (d, r))
+    pv = _dev(v, "v", f32, (d,))
+    pn = _dev(norms_out, "norms_out", (torch.float64,), (2,)) if norms_out is not None else None
+    _check(lib().logra_rowadam_apply(pw, ps, pv, d, k, r, seed, step, beta2, eps, lr, c, pn, _stream(stream)),
+           "logra_rowadam_apply")
+    return W
+
+
+def logra_rowadam_apply_ex(W, S, v, seed: int, step: int, beta2: float, eps: float, lr: float, c: float,
+                           norms_out=None, W_bf16_out=None, sync_sketch_out=None, stream=None):
+    import torch
+    d, k = W.shape
+    r = S.shape[1]
+    f32 = (torch.float32,)
+    pw = _dev(W, "W", f32)
+    ps = _dev(S, "S", f32, (d, r))
+    pv = _dev(v, "v", f32, (d,))
+    pn = _dev(norms_out, "norms_out", (torch.float64,), (2,)) if norms_out is not None else None
+    pb = _dev(W_bf16_out, "W_bf16_out", (torch.bfloat16,), (d, k)) if W_bf16_out is not None else None
+    pq = _dev(sync_sketch_out, "sync_sketch_out", f32, (d, r)) if sync_sketch_out is not None else None
+    _check(lib().logra_rowadam_apply_ex(pw, ps, pv, d, k, r, seed, step, beta2, eps, lr, c, pn, pb, pq,
+                                        _stream(stream)), "logra_rowadam_apply_ex")
+    return W
+
+
+def logra_rowadam_predict(S, v, k: int, seed: int, step: int, beta2: float, eps: float, lr: float,
+                          norms_out, stream=None):
+    import torch
+    d, r = S.shape
+    f32 = (torch.float32,)
+    ps = _dev(S, "S", f32)
+    pv = _dev(v, "v", f32, (d,))
+    pn = _dev(norms_out, "norms_out", (torch.float64,), (2,))
+    _check(lib().logra_rowadam_predict(ps, pv, d, k, r, seed, step, beta2, eps, lr, pn, _stream(stream)),
+           "logra_rowadam_predict")
+    return norms_out
+
+
+def logra_reconstruct(S, k: int, seed: int, step: int, out, accumulate: bool = False, stream=None):
+    import torch
+    d, r = S.shape
+    ps = _dev(S, "S", (torch.float32,))
+    po = _dev(out, "out", (torch.float32, torch.bfloat16), (d, k))
+    _check(lib().logra_reconstruct(ps, d, k, r, seed, step, po, _in_dtype(out), int(bool(accumulate)),
+                                   _stream(stream)), "logra_reconstruct")
+    return out
+
+
+def logra_get_status(stream=None) -> int:
+    return lib().logra_get_status(_stream(stream))
+
+
+def logra_reserve_workspace(nbytes: int, stream=None):
+    _check(lib().logra_reserve_workspace(nbytes, _stream(stream)), "logra_reserve_workspace")
+
+
+def logra_launch_count() -> int:
+    return int(lib().logra_launch_count())
+
+
+def logra_debug_inject(fault: int, timeout_cycles: int = 0):
+    _check(lib().logra_debug_inject(fault, timeout_cycles), "logra_debug_inject")

@@ -1,0 +1,297 @@
+// C ABI of liblogra: argument checks, per-(device, stream) workspace, the
+// per-device control block, and the launches behind each logra_* entry point.
+#include <cstdio>
+#include <atomic>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace logra {
+
+// Control block of each device that loads this library (status word and the
+// bounded-wait settings).  Host code reaches it only through the address
+// cudaGetSymbolAddress returns for the current device.
+static __device__ Control g_control = {0, 0, 2000000000ull};
+
+static thread_local int t_last_cuda_error = 0;
+static std::atomic<unsigned long long> g_launches{0};
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = int(e);
+  return LOGRA_ERR_CUDA;
+}
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+Control* g_ctl_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+
+struct Buffer {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, Buffer> g_ws;
+
+int current_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (*dev < 0 || *dev >= kMaxDevices) return LOGRA_ERR_NO_DEVICE;
+  return LOGRA_OK;
+}
+}  // namespace
+
+Control* control_block(int* status) {
+  int dev;
+  if ((*status = current_device(&dev))) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_ctl_ptr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_control);
+    if (e != cudaSuccess) {
+      *status = cuda_fail(e);
+      return nullptr;
+    }
+    g_ctl_ptr[dev] = static_cast<Control*>(p);
+  }
+  return g_ctl_ptr[dev];
+}
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  if (!g_sm_count[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_sm_count[dev] = n > 0 ? n : 148;
+  }
+  return g_sm_count[dev];
+}
+
+void* workspace(cudaStream_t stream, size_t bytes, int* status) {
+  *status = LOGRA_OK;
+  int dev;
+  if ((*status = current_device(&dev))) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  Buffer& b = g_ws[std::make_pair(dev, stream)];
+  if (b.bytes < bytes) {
+    if (b.ptr) {
+      // Work already queued on this stream may still read the old buffer.
+      cudaError_t e = cudaStreamSynchronize(stream);
+      if (e == cudaSuccess) e = cudaFree(b.ptr);
+      b.ptr = nullptr;
+      b.bytes = 0;
+      if (e != cudaSuccess) {
+        *status = cuda_fail(e);
+        return nullptr;
+      }
+    }
+    size_t want = bytes < (size_t(1) << 20) ? (size_t(1) << 20) : bytes;
+    cudaError_t e = cudaMalloc(&b.ptr, want);
+    if (e != cudaSuccess) {
+      b.ptr = nullptr;
+      *status = cuda_fail(e);
+      return nullptr;
+    }
+    b.bytes = want;
+  }
+  return b.ptr;
+}
+
+int make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, uint32_t elem_bytes, uint64_t inner,
+                 uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                 CUtensorMapSwizzle swizzle) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+      cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess) return cuda_fail(e);
+      if (q != cudaDriverEntryPointSuccess || !fn) return cuda_fail(cudaErrorNotSupported);
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  (void)elem_bytes;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? LOGRA_OK : LOGRA_ERR_UNSUPPORTED;
+}
+
+}  // namespace logra
+
+using namespace logra;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_rank(int r) { return (r >= 32 && r <= 512 && r % 32 == 0) ? LOGRA_OK : LOGRA_ERR_UNSUPPORTED; }
+
+int check_mat(int64_t d, int64_t k) {
+  if (d < 1 || k < 1) return LOGRA_ERR_INVALID_ARG;
+  if (d % 8 || k % 8) return LOGRA_ERR_UNSUPPORTED;
+  if (d > (int64_t(1) << 31) || k > (int64_t(1) << 24)) return LOGRA_ERR_UNSUPPORTED;
+  return LOGRA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* logra_status_string(int status) {
+  switch (status) {
+    case LOGRA_OK: return "ok";
+    case LOGRA_ERR_INVALID_ARG: return "invalid argument (null pointer, negative size or unknown dtype)";
+    case LOGRA_ERR_UNSUPPORTED: return "unsupported shape or alignment";
+    case LOGRA_ERR_CUDA: return "CUDA runtime error";
+    case LOGRA_ERR_TIMEOUT: return "a device-side wait gave up";
+    case LOGRA_ERR_NO_DEVICE: return "no usable CUDA device";
+    default: return "unknown status";
+  }
+}
+
+int logra_last_cuda_error(void) { return t_last_cuda_error; }
+
+int logra_version(void) { return (1 << 16) | 0; }
+
+uint64_t logra_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int logra_sign_matrix(uint64_t seed, uint64_t step, int r, int64_t k, float* A_out, logra_stream_t stream) {
+  if (!A_out || k < 1) return LOGRA_ERR_INVALID_ARG;
+  if (check_rank(r) || k > (int64_t(1) << 31)) return LOGRA_ERR_UNSUPPORTED;
+  return launch_sign_matrix(step_key(seed, step), r, k, inv_sqrt_r(r), A_out, stream);
+}
+
+size_t logra_sketch_workspace_bytes(int64_t n, int64_t d, int64_t k, int r, int in_dtype) {
+  if (n <= 0 || r <= 0 || d <= 0 || k <= 0) return 0;
+  if (in_dtype == LOGRA_BF16) return sketch_tc_workspace_bytes(n, d, k, r, sm_count());
+  return size_t(n) * size_t(r) * 4;
+}
+
+size_t logra_apply_workspace_bytes(int64_t d, int64_t k, int r) {
+  if (d <= 0 || k <= 0 || r <= 0) return 0;
+  return apply_workspace_layout(d, k, r).bytes;
+}
+
+int logra_reserve_workspace(size_t bytes, logra_stream_t stream) {
+  int st;
+  workspace(stream, bytes, &st);
+  return st;
+}
+
+int logra_sketch_accumulate(const void* X, const void* dY, int in_dtype, int64_t n, int64_t d, int64_t k, int r,
+                            uint64_t seed, uint64_t step, float* S, logra_stream_t stream) {
+  if (!S || n < 0) return LOGRA_ERR_INVALID_ARG;
+  if (in_dtype != LOGRA_F32 && in_dtype != LOGRA_BF16) return LOGRA_ERR_INVALID_ARG;
+  if (int st = check_mat(d, k)) return st;
+  if (check_rank(r)) return LOGRA_ERR_UNSUPPORTED;
+  if (n == 0) return LOGRA_OK;
+  if (!X || !dY) return LOGRA_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(dY) || !aligned16(S)) return LOGRA_ERR_UNSUPPORTED;
+  int st;
+  void* ws = workspace(stream, logra_sketch_workspace_bytes(n, d, k, r, in_dtype), &st);
+  if (st) return st;
+  if (in_dtype == LOGRA_BF16) {
+    Control* ctl = control_block(&st);
+    if (!ctl) return st;
+    return launch_sketch_tc(X, dY, n, d, k, r, step_key(seed, step), inv_sqrt_r(r), S, ws, ctl, stream);
+  }
+  return launch_sketch_simt(X, dY, in_dtype, n, d, k, r, step_key(seed, step), inv_sqrt_r(r), S,
+                            static_cast<float*>(ws), stream);
+}
+
+static int rowadam_common(int mode, float* W, const float* S, float* v, int64_t d, int64_t k, int r, uint64_t seed,
+                          uint64_t step, float beta2, float eps, float lr, float c, double* norms_out,
+                          uint16_t* W_bf16_out, float* sync_out, logra_stream_t stream) {
+  if (!S || !v) return LOGRA_ERR_INVALID_ARG;
+  if (mode == 0 && !W) return LOGRA_ERR_INVALID_ARG;
+  if (int st = check_mat(d, k)) return st;
+  if (check_rank(r)) return LOGRA_ERR_UNSUPPORTED;
+  if (!aligned16(S) || !aligned16(v) || (W && !aligned16(W)) || (W_bf16_out && !aligned16(W_bf16_out)) ||
+      (sync_out && !aligned16(sync_out)) || (norms_out && !aligned16(norms_out)))
+    return LOGRA_ERR_UNSUPPORTED;
+  int st;
+  char* ws = static_cast<char*>(workspace(stream, logra_apply_workspace_bytes(d, k, r), &st));
+  if (st) return st;
+  return launch_rowadam_simt(mode, W, reinterpret_cast<__nv_bfloat16*>(W_bf16_out), nullptr, 0, S, v,
+                             mode == 0 ? v : nullptr, mode == 0 ? sync_out : nullptr, d, k, r, step_key(seed, step),
+                             beta2, eps, lr * c, norms_out, ws, stream);
+}
+
+int logra_rowadam_apply(float* W, const float* S, float* v, int64_t d, int64_t k, int r, uint64_t seed,
+                        uint64_t step, float beta2, float eps, float lr, float c, double* norms_out,
+                        logra_stream_t stream) {
+  return rowadam_common(0, W, S, v, d, k, r, seed, step, beta2, eps, lr, c, norms_out, nullptr, nullptr, stream);
+}
+
+int logra_rowadam_apply_ex(float* W, const float* S, float* v, int64_t d, int64_t k, int r, uint64_t seed,
+                           uint64_t step, float beta2, float eps, float lr, float c, double* norms_out,
+                           uint16_t* W_bf16_out, float* sync_sketch_out, logra_stream_t stream) {
+  return rowadam_common(0, W, S, v, d, k, r, seed, step, beta2, eps, lr, c, norms_out, W_bf16_out, sync_sketch_out,
+                        stream);
+}
+
+int logra_rowadam_predict(const float* S, const float* v, int64_t d, int64_t k, int r, uint64_t seed,
+                          uint64_t step, float beta2, float eps, float lr, double* norms_out,
+                          logra_stream_t stream) {
+  if (!norms_out) return LOGRA_ERR_INVALID_ARG;
+  return rowadam_common(1, nullptr, S, const_cast<float*>(v), d, k, r, seed, step, beta2, eps, lr, 1.0f, norms_out,
+                        nullptr, nullptr, stream);
+}
+
+int logra_reconstruct(const float* S, int64_t d, int64_t k, int r, uint64_t seed, uint64_t step, void* dW_out,
+                      int out_dtype, int accumulate, logra_stream_t stream) {
+  if (!S || !dW_out) return LOGRA_ERR_INVALID_ARG;
+  if (out_dtype != LOGRA_F32 && out_dtype != LOGRA_BF16) return LOGRA_ERR_INVALID_ARG;
+  if (accumulate != 0 && accumulate != 1) return LOGRA_ERR_INVALID_ARG;
+  if (int st = check_mat(d, k)) return st;
+  if (check_rank(r)) return LOGRA_ERR_UNSUPPORTED;
+  if (!aligned16(S) || !aligned16(dW_out)) return LOGRA_ERR_UNSUPPORTED;
+  int st;
+  char* ws = static_cast<char*>(workspace(stream, logra_apply_workspace_bytes(d, k, r), &st));
+  if (st) return st;
+  return launch_rowadam_simt(out_dtype == LOGRA_F32 ? 2 : 3, nullptr, nullptr, dW_out, accumulate, S, nullptr,
+                             nullptr, nullptr, d, k, r, step_key(seed, step), 0.f, 0.f, 0.f, nullptr, ws, stream);
+}
+
+int logra_get_status(logra_stream_t stream) {
+  int st;
+  Control* ctl = control_block(&st);
+  if (!ctl) return st;
+  LOGRA_CUDA_TRY(cudaStreamSynchronize(stream));
+  int code = 0;
+  LOGRA_CUDA_TRY(cudaMemcpy(&code, &ctl->status, sizeof(int), cudaMemcpyDeviceToHost));
+  const int zero = 0;
+  LOGRA_CUDA_TRY(cudaMemcpy(&ctl->status, &zero, sizeof(int), cudaMemcpyHostToDevice));
+  return code;
+}
+
+int logra_debug_inject(int fault, uint64_t timeout_cycles) {
+  int st;
+  Control* ctl = control_block(&st);
+  if (!ctl) return st;
+  const int f = fault ? 1 : 0;
+  LOGRA_CUDA_TRY(cudaMemcpy(&ctl->inject_fault, &f, sizeof(int), cudaMemcpyHostToDevice));
+  if (timeout_cycles) {
+    const unsigned long long t = timeout_cycles;
+    LOGRA_CUDA_TRY(cudaMemcpy(&ctl->wait_limit, &t, sizeof(t), cudaMemcpyHostToDevice));
+  }
+  return LOGRA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,74 @@
+// Shared device helpers of liblogra: the sign hash, status word, launch checks.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "../../include/logra.h"
+
+namespace logra {
+
+// ---------------------------------------------------------------------------
+// Sign generator.  SplitMix64 (Steele, Lea & Flood, OOPSLA 2014): the key of
+// (seed, step) is the generator's output number step+1 for seed `seed`; word w
+// of row i of Sigma is the finaliser applied to key ^ (i << 32 | w).  Bit b of
+// that word is the sign of Sigma[i][64 w + b] (set -> -1).  A new key per step
+// is the per-step redraw of the projection (academy.dair.ai summary, "Gradient
+// sketches"); all microbatches of a step share it.
+// ---------------------------------------------------------------------------
+constexpr uint64_t kGolden = 0x9E3779B97F4A7C15ull;
+
+__host__ __device__ __forceinline__ uint64_t mix64(uint64_t z) {
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+__host__ __device__ __forceinline__ uint64_t step_key(uint64_t seed, uint64_t step) {
+  return mix64(seed + kGolden * (step + 1));
+}
+
+__host__ __device__ __forceinline__ uint64_t sign_word(uint64_t key, uint32_t row, uint32_t word) {
+  return mix64(key ^ ((uint64_t(row) << 32) | uint64_t(word)));
+}
+
+// fl32(1/sqrt(r)), computed in double and rounded once.
+inline float inv_sqrt_r(int r) { return float(1.0 / __builtin_sqrt(double(r))); }
+
+// ---------------------------------------------------------------------------
+// Per-device control block: status word and the bounded-wait settings.  It is
+// a file-scope __device__ object of the API translation unit; kernels receive
+// its device address (taken once per device with cudaGetSymbolAddress).
+// ---------------------------------------------------------------------------
+struct Control {
+  int status;                    // first device-side failure since last read
+  int inject_fault;              // test hook: drop one producer arrival
+  unsigned long long wait_limit; // clock64 ticks a bounded wait may spin
+};
+
+__device__ __forceinline__ void record_status(Control* ctl, int code) {
+  atomicCAS(&ctl->status, 0, code);
+}
+
+Control* control_block(int* status);                     // current device
+void* workspace(cudaStream_t stream, size_t bytes, int* status);
+int sm_count();
+int cuda_fail(cudaError_t e);
+void count_launch();
+
+}  // namespace logra
+
+// After every kernel launch: count it and surface a launch error.
+#define LOGRA_LAUNCHED()                                       \
+  do {                                                         \
+    ::logra::count_launch();                                   \
+    cudaError_t _e = cudaGetLastError();                       \
+    if (_e != cudaSuccess) return ::logra::cuda_fail(_e);      \
+  } while (0)
+
+#define LOGRA_CUDA_TRY(expr)                                   \
+  do {                                                         \
+    cudaError_t _e = (expr);                                   \
+    if (_e != cudaSuccess) return ::logra::cuda_fail(_e);      \
+  } while (0)

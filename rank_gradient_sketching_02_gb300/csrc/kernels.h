@@ -1,0 +1,35 @@
+// Internal launchers of liblogra (not part of the C ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace logra {
+
+struct Control;
+
+struct ApplyWorkspace {
+  size_t words_off, gram_off, inv_off, ssq_off, dw2_off, bytes;
+  int n_ssq, n_dw2;
+};
+
+ApplyWorkspace apply_workspace_layout(int64_t d, int64_t k, int r);
+
+int launch_sign_matrix(uint64_t key, int r, int64_t k, float scale, float* A, cudaStream_t s);
+int launch_gram(uint64_t key, int r, int64_t k, uint64_t* words, float* M, cudaStream_t s);
+
+int launch_sketch_simt(const void* X, const void* dY, int dtype, int64_t n, int64_t d, int64_t k, int r,
+                       uint64_t key, float scale, float* S, float* P, cudaStream_t s);
+
+size_t sketch_tc_workspace_bytes(int64_t n, int64_t d, int64_t k, int r, int sms);
+int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_t k, int r, uint64_t key,
+                     float scale, float* S, void* ws, Control* ctl, cudaStream_t s);
+
+// mode 0 apply, 1 predict, 2 reconstruct fp32, 3 reconstruct bf16.
+int launch_rowadam_simt(int mode, float* W, __nv_bfloat16* Wb, void* out, int accumulate, const float* S,
+                        const float* v_in, float* v_out, float* sync_out, int64_t d, int64_t k, int r, uint64_t key,
+                        float beta2, float eps, float lrc, double* norms, char* ws, cudaStream_t s);
+
+}  // namespace logra

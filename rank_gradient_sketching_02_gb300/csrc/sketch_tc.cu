@@ -1,0 +1,526 @@
+// Tensor-core sketch for bf16 inputs (tcgen05 + TMEM + TMA), three launches:
+//
+//   project   P_s^T = Sigma X_s^T for a k-range s  (D[128 tokens x r] in TMEM;
+//             A = X tile by TMA, B = Sigma tile generated in shared memory
+//             from the sign hash; k split over s for occupancy)
+//   split     P^T = sum_s P_s^T, stored as a two-term bf16 expansion
+//             P^T = hi + lo, written pre-swizzled in 32-token chunks so the
+//             next kernel loads one chunk with a single bulk copy
+//   accumulate S += (P^T dY)^T / sqrt(r): D[r x N d-columns] in TMEM with
+//             A = P^T chunk (hi and lo, two MMAs into one accumulator),
+//             B = dY tile (MN-major, TMA), tokens split over units; each unit
+//             adds its tile into S with coalesced fp32 reductions.
+//
+// (theclarity.today write-up, "Why it matters": S = G A^T is accumulated during
+// backpropagation and G is never formed; academy.dair.ai summary: the random-
+// sign projection is redrawn per step and shared by the step's microbatches.)
+//
+// Roles per CTA: warp 0 = TMA producer, warp 1 = TMEM owner + MMA issuer,
+// warps 2..5 = epilogue (TMEM lane quadrant = warp % 4), warps 6..9 (project
+// only) = sign-tile generators.  Every wait is bounded; a wait that runs out
+// records LOGRA_ERR_TIMEOUT in the control block and the CTA drains and exits.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace logra {
+
+using namespace tc;
+
+namespace {
+
+constexpr int kTok = 128;      // tokens per project tile (MMA M)
+constexpr int kKc = 64;        // k per project stage (one sign word per row)
+constexpr int kChunk = 32;     // tokens per accumulate stage / image chunk
+constexpr int kMaxStages = 8;
+
+struct SketchShape {
+  int64_t n, d, k;
+  int r, r_pad;                // r_pad: r rounded up to 128 (accumulate M blocks)
+  int n_pad;                   // n rounded up to kChunk
+  int tiles, splits, chunks_per_split, nchunks;      // project
+  int ntile_n, dtiles, tsplits, tchunks_per_split;   // accumulate
+  int proj_stages, acc_stages;
+};
+
+struct Shared {
+  uint64_t full[kMaxStages];     // project: TMA bytes; accumulate: TMA bytes
+  uint64_t gen[kMaxStages];      // project: 4 generator warps
+  uint64_t empty[kMaxStages];    // MMA commit
+  uint64_t tmem_full, tmem_empty, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ bool wait_or_abort(Shared* sh, uint64_t* bar, uint32_t parity, unsigned long long limit,
+                                              Control* ctl) {
+  while (!mbar_wait(bar, parity, limit / 8 + 1)) {
+    if (*reinterpret_cast<volatile int*>(&sh->abort)) return false;
+    limit -= limit / 8 + 1;
+    if (limit < 16) {
+      record_status(ctl, LOGRA_ERR_TIMEOUT);
+      *reinterpret_cast<volatile int*>(&sh->abort) = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+}  // namespace
+
+// ============================================================================ project
+// Sigma tile for k-chunk c: rows b < r of 128 bytes (64 bf16 +-1), K-major,
+// 128-byte swizzle (16-byte chunk q of row b stored at chunk q ^ (b & 7)).
+__device__ __forceinline__ void gen_sigma_kmajor(uint8_t* tile, uint64_t key, int r, int c, int tid, int nthr) {
+  for (int b = tid; b < r; b += nthr) {
+    const uint64_t w = sign_word(key, uint32_t(b), uint32_t(c));
+    uint8_t* row = tile + size_t(b) * 128;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const uint4 v = signs8_to_bf16(uint32_t(w >> (8 * q)) & 0xFFu);
+      *reinterpret_cast<uint4*>(row + ((q ^ (b & 7)) << 4)) = v;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(320, 1)
+    project_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, SketchShape sh_, uint64_t key,
+                      float* __restrict__ ppart, Control* ctl) {
+  extern __shared__ uint8_t smem_raw[];
+  const SketchShape& P = sh_;
+  uint8_t* base = align1024(smem_raw);
+  const int S = P.proj_stages;
+  const uint32_t a_bytes = kTok * 128;
+  const uint32_t b_bytes = uint32_t(P.r) * 128;
+  uint8_t* a_tiles = base;
+  uint8_t* b_tiles = base + size_t(S) * a_bytes;
+  Shared* sh = reinterpret_cast<Shared*>(b_tiles + size_t(S) * b_bytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned long long limit = ctl->wait_limit;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&sh->full[s], 1);
+      mbar_init(&sh->gen[s], 4);
+      mbar_init(&sh->empty[s], 1);
+    }
+    mbar_init(&sh->tmem_full, 1);
+    mbar_init(&sh->tmem_empty, 4);
+    mbar_init(&sh->drain, 1);
+    sh->abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmap_x);
+  }
+  uint32_t tmem_cols = 32;
+  while (tmem_cols < uint32_t(P.r)) tmem_cols <<= 1;
+  if (warp == 1) {
+    tmem_alloc(&sh->tmem_base, tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh->tmem_base;
+  const int units = P.tiles * P.splits;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer (X tiles)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int inject = ctl->inject_fault && blockIdx.x == 0;
+      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const int tile = u % P.tiles, split = u / P.tiles;
+        const int c0 = split * P.chunks_per_split;
+        const int c1 = min(P.nchunks, c0 + P.chunks_per_split);
+        for (int c = c0; c < c1; ++c) {
+          if (!wait_or_abort(sh, &sh->empty[stage], phase ^ 1u, limit, ctl)) goto producer_done;
+          if (inject && c == c0 + 1) {
+            inject = 0;                      // test hook: this stage never fills
+          } else {
+            mbar_arrive_expect_tx(&sh->full[stage], a_bytes);
+            tma_load_2d(a_tiles + size_t(stage) * a_bytes, &tmap_x, &sh->full[stage], c * kKc, tile * kTok);
+          }
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+      }
+    producer_done:
+      // Copies still in flight land before the CTA exits: wait for the last
+      // phase issued on every stage (bounded; phases already consumed pass).
+      for (int s = 0; s < S; ++s) {
+        const uint32_t ph = (s < stage) ? phase : (phase ^ 1u);
+        mbar_wait(&sh->full[s], ph, limit);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, tphase = 0;
+      const int nparts = P.r > 256 ? 2 : 1;
+      const int npart = P.r / nparts;
+      const uint32_t idesc = idesc_bf16(128, uint32_t(npart), 0, 0);
+      for (int u = blockIdx.x; u < units && !sh->abort; u += gridDim.x) {
+        const int split = u / P.tiles;
+        const int c0 = split * P.chunks_per_split;
+        const int c1 = min(P.nchunks, c0 + P.chunks_per_split);
+        if (!wait_or_abort(sh, &sh->tmem_empty, tphase ^ 1u, limit, ctl)) break;
+        tc_fence_after();
+        bool first = true;
+        for (int c = c0; c < c1; ++c) {
+          if (!wait_or_abort(sh, &sh->full[stage], phase, limit, ctl)) goto mma_done;
+          if (!wait_or_abort(sh, &sh->gen[stage], phase, limit, ctl)) goto mma_done;
+          tc_fence_after();
+          const uint32_t a0 = smem_addr(a_tiles + size_t(stage) * a_bytes);
+          const uint32_t b0 = smem_addr(b_tiles + size_t(stage) * b_bytes);
+#pragma unroll
+          for (int ks = 0; ks < kKc / 16; ++ks) {
+            const uint64_t ad = smem_desc(a0 + ks * 32, 16, 1024, kSw128);
+            for (int p = 0; p < nparts; ++p) {
+              const uint64_t bd = smem_desc(b0 + uint32_t(p * npart) * 128 + ks * 32, 16, 1024, kSw128);
+              mma_bf16(tmem + uint32_t(p * npart), ad, bd, idesc, first ? 0u : 1u);
+            }
+            first = false;
+          }
+          mma_commit(&sh->empty[stage]);
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+        mma_commit(&sh->tmem_full);
+        tphase ^= 1u;
+      }
+    mma_done:
+      mma_commit(&sh->drain);
+      mbar_wait(&sh->drain, 0, limit);
+    }
+  } else if (warp < 6) {
+    // ---------------------------------------------------------------- epilogue: TMEM -> P partials
+    const int quad = warp & 3;
+    uint32_t tphase = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const int tile = u % P.tiles, split = u / P.tiles;
+      if (!wait_or_abort(sh, &sh->tmem_full, tphase, limit, ctl)) break;
+      tphase ^= 1u;
+      tc_fence_after();
+      const int64_t t = int64_t(tile) * kTok + quad * 32 + lane;
+      float* dst = ppart + int64_t(split) * P.r * P.n_pad + t;
+      for (int c = 0; c < P.r; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + uint32_t(c), v);
+        tmem_ld_wait();
+        if (t < P.n) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) dst[int64_t(c + j) * P.n_pad] = __uint_as_float(v[j]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->tmem_empty);
+    }
+  } else {
+    // ---------------------------------------------------------------- sign-tile generators
+    const int gtid = threadIdx.x - 192;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const int split = u / P.tiles;
+      const int c0 = split * P.chunks_per_split;
+      const int c1 = min(P.nchunks, c0 + P.chunks_per_split);
+      for (int c = c0; c < c1; ++c) {
+        if (!wait_or_abort(sh, &sh->empty[stage], phase ^ 1u, limit, ctl)) goto gen_done;
+        gen_sigma_kmajor(b_tiles + size_t(stage) * b_bytes, key, P.r, c, gtid, 128);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->gen[stage]);
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+      }
+    }
+  gen_done:;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tmem_cols);
+  }
+}
+
+// ============================================================================ split
+// image[c][row][128 B]: tokens 32c..32c+31 of P^T row `row`; bytes 0..63 hold
+// the bf16 "hi" terms, 64..127 the "lo" terms, 16-byte chunk q stored at
+// q ^ (row & 7).  Rows >= r and tokens >= n are zero.
+__global__ void __launch_bounds__(256) split_kernel(const float* __restrict__ ppart, SketchShape P,
+                                                    uint8_t* __restrict__ image) {
+  const int64_t total = int64_t(P.n_pad / kChunk) * P.r_pad * 4;
+  for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total; e += int64_t(gridDim.x) * blockDim.x) {
+    const int g = int(e & 3);
+    const int64_t rowc = e >> 2;
+    const int row = int(rowc % P.r_pad);
+    const int64_t c = rowc / P.r_pad;
+    const int64_t t0 = c * kChunk + g * 8;
+    float p[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (row < P.r) {
+      for (int s = 0; s < P.splits; ++s) {
+        const float4* src = reinterpret_cast<const float4*>(ppart + (int64_t(s) * P.r + row) * P.n_pad + t0);
+        const float4 x0 = src[0], x1 = src[1];
+        p[0] += x0.x; p[1] += x0.y; p[2] += x0.z; p[3] += x0.w;
+        p[4] += x1.x; p[5] += x1.y; p[6] += x1.z; p[7] += x1.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (t0 + i >= P.n) p[i] = 0.f;
+    }
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat16 h0 = __float2bfloat16_rn(p[2 * i]), h1 = __float2bfloat16_rn(p[2 * i + 1]);
+      const __nv_bfloat16 l0 = __float2bfloat16_rn(p[2 * i] - __bfloat162float(h0));
+      const __nv_bfloat16 l1 = __float2bfloat16_rn(p[2 * i + 1] - __bfloat162float(h1));
+      hi[i] = uint32_t(__bfloat16_as_ushort(h0)) | (uint32_t(__bfloat16_as_ushort(h1)) << 16);
+      lo[i] = uint32_t(__bfloat16_as_ushort(l0)) | (uint32_t(__bfloat16_as_ushort(l1)) << 16);
+    }
+    uint8_t* rowp = image + (c * P.r_pad + row) * 128;
+    *reinterpret_cast<uint4*>(rowp + ((g ^ (row & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(rowp + (((g + 4) ^ (row & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  }
+}
+
+// ============================================================================ accumulate
+__global__ void __launch_bounds__(192, 1)
+    accumulate_tc_kernel(const __grid_constant__ CUtensorMap tmap_dy, SketchShape sh_, const uint8_t* __restrict__ image,
+                         float scale, float* __restrict__ S, Control* ctl) {
+  extern __shared__ uint8_t smem_raw[];
+  const SketchShape& P = sh_;
+  uint8_t* base = align1024(smem_raw);
+  const int NS = P.acc_stages;
+  const int N = P.ntile_n;
+  const uint32_t a_bytes = uint32_t(P.r_pad) * 128;
+  const uint32_t b_bytes = uint32_t(N) * kChunk * 2;
+  const uint32_t stage_bytes = a_bytes + b_bytes;
+  Shared* sh = reinterpret_cast<Shared*>(base + size_t(NS) * stage_bytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned long long limit = ctl->wait_limit;
+  const int mblocks = P.r_pad / 128;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&sh->full[s], 1);
+      mbar_init(&sh->empty[s], 1);
+    }
+    mbar_init(&sh->tmem_full, 1);
+    mbar_init(&sh->tmem_empty, 4);
+    mbar_init(&sh->drain, 1);
+    sh->abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmap_dy);
+  }
+  uint32_t tmem_cols = 32;
+  while (tmem_cols < uint32_t(mblocks * N)) tmem_cols <<= 1;
+  if (warp == 1) {
+    tmem_alloc(&sh->tmem_base, tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh->tmem_base;
+  const int units = P.dtiles * P.tsplits;
+  const int nchunks = P.n_pad / kChunk;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int inject = ctl->inject_fault && blockIdx.x == 0;
+      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const int dt = u % P.dtiles, ts = u / P.dtiles;
+        const int c0 = ts * P.tchunks_per_split, c1 = min(nchunks, c0 + P.tchunks_per_split);
+        for (int c = c0; c < c1; ++c) {
+          if (!wait_or_abort(sh, &sh->empty[stage], phase ^ 1u, limit, ctl)) goto producer_done;
+          if (inject && c == c0 + 1) {
+            inject = 0;
+          } else {
+            uint8_t* st = base + size_t(stage) * stage_bytes;
+            mbar_arrive_expect_tx(&sh->full[stage], stage_bytes);
+            bulk_load(st, image + size_t(c) * a_bytes, a_bytes, &sh->full[stage]);
+            for (int j = 0; j < N / 64; ++j)
+              tma_load_2d(st + a_bytes + j * (kChunk * 128), &tmap_dy, &sh->full[stage], dt * N + j * 64, c * kChunk);
+          }
+          if (++stage == NS) { stage = 0; phase ^= 1u; }
+        }
+      }
+    producer_done:
+      for (int s = 0; s < NS; ++s) {
+        const uint32_t ph = (s < stage) ? phase : (phase ^ 1u);
+        mbar_wait(&sh->full[s], ph, limit);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, tphase = 0;
+      const uint32_t idesc = idesc_bf16(128, uint32_t(N), 0, 1);
+      for (int u = blockIdx.x; u < units && !sh->abort; u += gridDim.x) {
+        const int ts = u / P.dtiles;
+        const int c0 = ts * P.tchunks_per_split, c1 = min(nchunks, c0 + P.tchunks_per_split);
+        if (!wait_or_abort(sh, &sh->tmem_empty, tphase ^ 1u, limit, ctl)) break;
+        tc_fence_after();
+        bool first = true;
+        for (int c = c0; c < c1; ++c) {
+          if (!wait_or_abort(sh, &sh->full[stage], phase, limit, ctl)) goto mma_done;
+          tc_fence_after();
+          const uint32_t a0 = smem_addr(base + size_t(stage) * stage_bytes);
+          const uint32_t b0 = a0 + a_bytes;
+#pragma unroll
+          for (int ks = 0; ks < kChunk / 16; ++ks) {
+            const uint64_t bd = smem_desc(b0 + ks * 2048, kChunk * 128, 1024, kSw128);
+            for (int m = 0; m < mblocks; ++m) {
+              const uint32_t am = a0 + m * (128 * 128) + ks * 32;
+              mma_bf16(tmem + uint32_t(m * N), smem_desc(am, 16, 1024, kSw128), bd, idesc, first ? 0u : 1u);
+              mma_bf16(tmem + uint32_t(m * N), smem_desc(am + 64, 16, 1024, kSw128), bd, idesc, 1u);
+            }
+            first = false;
+          }
+          mma_commit(&sh->empty[stage]);
+          if (++stage == NS) { stage = 0; phase ^= 1u; }
+        }
+        mma_commit(&sh->tmem_full);
+        tphase ^= 1u;
+      }
+    mma_done:
+      mma_commit(&sh->drain);
+      mbar_wait(&sh->drain, 0, limit);
+    }
+  } else {
+    const int quad = warp & 3;
+    uint32_t tphase = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const int dt = u % P.dtiles;
+      if (!wait_or_abort(sh, &sh->tmem_full, tphase, limit, ctl)) break;
+      tphase ^= 1u;
+      tc_fence_after();
+      for (int m = 0; m < mblocks; ++m) {
+        const int ridx = m * 128 + quad * 32 + lane;
+        for (int c = 0; c < N; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + uint32_t(m * N + c), v);
+          tmem_ld_wait();
+          const int64_t d0 = int64_t(dt) * N + c;
+          if (ridx < P.r) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (d0 + j < P.d) red_add_f32(S + (d0 + j) * P.r + ridx, __uint_as_float(v[j]) * scale);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->tmem_empty);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tmem_cols);
+  }
+}
+
+// ============================================================================ host side
+static int ceil_div(int64_t a, int64_t b) { return int((a + b - 1) / b); }
+
+// Pick the number of token splits for `tiles` tiles over `sms` SMs: the best
+// fraction of busy SMs in the last wave, each split keeping >= min_chunks chunks.
+static int pick_splits(int tiles, int sms, int nchunks, int min_chunks, int max_splits) {
+  int best = 1;
+  double best_eff = -1.0;
+  for (int s = 1; s <= max_splits; ++s) {
+    if (s > 1 && ceil_div(nchunks, s) < min_chunks) break;
+    const int per = ceil_div(nchunks, s);
+    const int real = ceil_div(nchunks, per);
+    const int units = tiles * real;
+    const int waves = ceil_div(units, sms);
+    const double eff = double(units) / double(waves * sms);
+    if (eff > best_eff + 0.02) {
+      best_eff = eff;
+      best = real;
+    }
+  }
+  return best;
+}
+
+static SketchShape plan(int64_t n, int64_t d, int64_t k, int r, int sms) {
+  SketchShape P{};
+  P.n = n; P.d = d; P.k = k; P.r = r;
+  P.r_pad = ceil_div(r, 128) * 128;
+  P.n_pad = ceil_div(n, kChunk) * kChunk;
+  P.tiles = ceil_div(n, kTok);
+  P.nchunks = ceil_div(k, kKc);
+  P.splits = pick_splits(P.tiles, sms, P.nchunks, 8, 4);
+  P.chunks_per_split = ceil_div(P.nchunks, P.splits);
+  P.splits = ceil_div(P.nchunks, P.chunks_per_split);
+  P.ntile_n = (P.r_pad <= 256) ? 256 : 128;
+  P.dtiles = ceil_div(d, P.ntile_n);
+  const int tchunks = P.n_pad / kChunk;
+  P.tsplits = pick_splits(P.dtiles, sms, tchunks, 8, 16);
+  P.tchunks_per_split = ceil_div(tchunks, P.tsplits);
+  P.tsplits = ceil_div(tchunks, P.tchunks_per_split);
+  const int budget = 227 * 1024 - 1024 - int(sizeof(Shared)) - 64;
+  P.proj_stages = budget / (kTok * 128 + r * 128);
+  if (P.proj_stages > kMaxStages) P.proj_stages = kMaxStages;
+  P.acc_stages = budget / (P.r_pad * 128 + P.ntile_n * kChunk * 2);
+  if (P.acc_stages > kMaxStages) P.acc_stages = kMaxStages;
+  return P;
+}
+
+size_t sketch_tc_workspace_bytes(int64_t n, int64_t d, int64_t k, int r, int sms) {
+  const SketchShape P = plan(n, d, k, r, sms);
+  const size_t part = size_t(P.splits) * P.r * P.n_pad * 4;
+  const size_t img = size_t(P.n_pad) * P.r_pad * 4;
+  return ((part + 1023) & ~size_t(1023)) + img;
+}
+
+int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_t k, int r, uint64_t key,
+                     float scale, float* S, void* ws, Control* ctl, cudaStream_t s) {
+  const int sms = sm_count();
+  const SketchShape P = plan(n, d, k, r, sms);
+  float* ppart = static_cast<float*>(ws);
+  const size_t part = size_t(P.splits) * P.r * P.n_pad * 4;
+  uint8_t* image = static_cast<uint8_t*>(ws) + ((part + 1023) & ~size_t(1023));
+
+  CUtensorMap tx, tdy;
+  if (int st = make_tmap_2d(&tx, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, uint64_t(k), uint64_t(n), uint64_t(k) * 2,
+                            kKc, kTok, CU_TENSOR_MAP_SWIZZLE_128B))
+    return st;
+  if (int st = make_tmap_2d(&tdy, dY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, uint64_t(d), uint64_t(n), uint64_t(d) * 2,
+                            64, kChunk, CU_TENSOR_MAP_SWIZZLE_128B))
+    return st;
+
+  const int proj_smem = 1024 + P.proj_stages * (kTok * 128 + r * 128) + int(sizeof(Shared)) + 64;
+  LOGRA_CUDA_TRY(cudaFuncSetAttribute(project_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, proj_smem));
+  const int punits = P.tiles * P.splits;
+  project_tc_kernel<<<punits < sms ? punits : sms, 320, proj_smem, s>>>(tx, P, key, ppart, ctl);
+  LOGRA_LAUNCHED();
+
+  const int64_t stotal = int64_t(P.n_pad / kChunk) * P.r_pad * 4;
+  int sblocks = int((stotal + 255) / 256);
+  if (sblocks > sms * 8) sblocks = sms * 8;
+  split_kernel<<<sblocks, 256, 0, s>>>(ppart, P, image);
+  LOGRA_LAUNCHED();
+
+  const int acc_smem = 1024 + P.acc_stages * (P.r_pad * 128 + P.ntile_n * kChunk * 2) + int(sizeof(Shared)) + 64;
+  LOGRA_CUDA_TRY(cudaFuncSetAttribute(accumulate_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, acc_smem));
+  const int aunits = P.dtiles * P.tsplits;
+  accumulate_tc_kernel<<<aunits < sms ? aunits : sms, 192, acc_smem, s>>>(tdy, P, image, scale, S, ctl);
+  LOGRA_LAUNCHED();
+  return LOGRA_OK;
+}
+
+}  // namespace logra

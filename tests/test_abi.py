@@ -1,0 +1,65 @@
+"""The C ABI library builds, loads without a GPU and exports what the header declares."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "logra.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from rank_gradient_sketching_02_gb300 import build as B
+    B.build()
+    from rank_gradient_sketching_02_gb300 import binding
+    return binding.lib()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(logra_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = header_functions()
+    for must in ("logra_sketch_accumulate", "logra_rowadam_apply", "logra_reconstruct", "logra_sign_matrix"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import ctypes
+    for name in header_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_binding_covers_every_declared_symbol():
+    from rank_gradient_sketching_02_gb300 import binding
+    assert sorted(binding.SIGNATURES) == header_functions()
+
+
+def test_host_only_calls(lib):
+    assert lib.logra_version() >> 16 == 1
+    for st in range(6):
+        assert lib.logra_status_string(st)
+    assert lib.logra_status_string(99) == b"unknown status"
+    assert lib.logra_sketch_workspace_bytes(8192, 1536, 1536, 256, 1) >= 8192 * 256 * 4
+    assert lib.logra_sketch_workspace_bytes(8192, 1536, 1536, 256, 0) == 8192 * 256 * 4
+    assert lib.logra_sketch_workspace_bytes(0, 8, 8, 32, 1) == 0
+    assert lib.logra_apply_workspace_bytes(1536, 1536, 256) > 0
+
+
+def test_bad_arguments_rejected_before_any_cuda_call(lib):
+    from rank_gradient_sketching_02_gb300.binding import LOGRA_ERR_INVALID_ARG, LOGRA_ERR_UNSUPPORTED
+    # null / negative / bad dtype / bad rank / unaligned: no device work is attempted
+    assert lib.logra_sketch_accumulate(None, None, 1, 16, 8, 8, 32, 0, 0, None, None) == LOGRA_ERR_INVALID_ARG
+    assert lib.logra_sketch_accumulate(16, 16, 7, 16, 8, 8, 32, 0, 0, 16, None) == LOGRA_ERR_INVALID_ARG
+    assert lib.logra_sketch_accumulate(16, 16, 1, 16, 12, 8, 32, 0, 0, 16, None) == LOGRA_ERR_UNSUPPORTED
+    assert lib.logra_sketch_accumulate(16, 16, 1, 16, 8, 8, 48, 0, 0, 16, None) == LOGRA_ERR_UNSUPPORTED
+    assert lib.logra_sketch_accumulate(16, 18, 1, 16, 8, 8, 32, 0, 0, 16, None) == LOGRA_ERR_UNSUPPORTED
+    assert lib.logra_sketch_accumulate(16, 16, 1, 0, 8, 8, 32, 0, 0, 16, None) == 0   # n == 0: no-op
+    assert lib.logra_sign_matrix(0, 0, 544, 8, 16, None) == LOGRA_ERR_UNSUPPORTED
+    assert lib.logra_reconstruct(16, 8, 8, 32, 0, 0, 16, 5, 0, None) == LOGRA_ERR_INVALID_ARG
+    assert lib.logra_rowadam_predict(16, 16, 8, 8, 32, 0, 0, 0.9, 1e-8, 1e-3, None, None) == LOGRA_ERR_INVALID_ARG
