@@ -25,6 +25,21 @@ static std::atomic<unsigned long long> g_launches{0};
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+static std::mutex g_attr_mu;
+static std::map<std::pair<int, const void*>, int> g_attr;
+
+cudaError_t ensure_smem(const void* kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  int& have = g_attr[std::make_pair(dev, kernel)];
+  if (have >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) have = bytes;
+  return e;
+}
+
 int cuda_fail(cudaError_t e) {
   t_last_cuda_error = int(e);
   return LOGRA_ERR_CUDA;
@@ -228,9 +243,11 @@ static int rowadam_common(int mode, float* W, const float* S, float* v, int64_t 
   int st;
   char* ws = static_cast<char*>(workspace(stream, logra_apply_workspace_bytes(d, k, r), &st));
   if (st) return st;
-  return launch_rowadam_simt(mode, W, reinterpret_cast<__nv_bfloat16*>(W_bf16_out), nullptr, 0, S, v,
-                             mode == 0 ? v : nullptr, mode == 0 ? sync_out : nullptr, d, k, r, step_key(seed, step),
-                             beta2, eps, lr * c, norms_out, ws, stream);
+  Control* ctl = control_block(&st);
+  if (!ctl) return st;
+  return launch_rowadam(mode, W, reinterpret_cast<__nv_bfloat16*>(W_bf16_out), nullptr, 0, S, v,
+                        mode == 0 ? v : nullptr, mode == 0 ? sync_out : nullptr, d, k, r, step_key(seed, step), beta2,
+                        eps, lr * c, norms_out, ws, ctl, stream);
 }
 
 int logra_rowadam_apply(float* W, const float* S, float* v, int64_t d, int64_t k, int r, uint64_t seed,
@@ -265,8 +282,10 @@ int logra_reconstruct(const float* S, int64_t d, int64_t k, int r, uint64_t seed
   int st;
   char* ws = static_cast<char*>(workspace(stream, logra_apply_workspace_bytes(d, k, r), &st));
   if (st) return st;
-  return launch_rowadam_simt(out_dtype == LOGRA_F32 ? 2 : 3, nullptr, nullptr, dW_out, accumulate, S, nullptr,
-                             nullptr, nullptr, d, k, r, step_key(seed, step), 0.f, 0.f, 0.f, nullptr, ws, stream);
+  Control* ctl = control_block(&st);
+  if (!ctl) return st;
+  return launch_rowadam(out_dtype == LOGRA_F32 ? 2 : 3, nullptr, nullptr, dW_out, accumulate, S, nullptr, nullptr,
+                        nullptr, d, k, r, step_key(seed, step), 0.f, 0.f, 0.f, nullptr, ws, ctl, stream);
 }
 
 int logra_get_status(logra_stream_t stream) {

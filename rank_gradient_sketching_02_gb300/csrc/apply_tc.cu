@@ -1,0 +1,479 @@
+// Tensor-core reconstruct-and-update (tcgen05 + TMEM + TMA):
+//
+//   for each 128-row block of W and each 256-column super-tile:
+//     D[128 x 256] = S_rows (hi + lo bf16, two MMAs) * Sigma[:, cols]   (TMEM)
+//   epilogue, 32 columns at a time, thread = row:
+//     apply    W_ij += f_i D_ij  with f_i = -lr c / (sqrt(r) sqrt(v_i + eps)),
+//              optional bf16 copy of W, sum of (f_i D_ij)^2 per row
+//     predict  only the sum of squares
+//     rebuild  out_ij (+)= D_ij / sqrt(r)   (fp32 or bf16 output)
+//
+// Ghat = S A is formed tile by tile and consumed in the same kernel, so the
+// d x k reconstruction never reaches memory (theclarity.today write-up, "Why
+// it matters": the full-size estimate exists only when the update is
+// applied).  RowAdam's per-row statistic v has been updated beforehand from
+// the exact row norms ||(S A)_i||^2 = S_i Sigma Sigma^T S_i^T / r.
+//
+// Operands: A = the row block of S, pre-split into bf16 hi/lo and pre-swizzled
+// (one bulk copy per 64-wide rank chunk); B = Sigma rows of that chunk for the
+// super-tile's 256 columns, MN-major, generated in shared memory from the sign
+// hash.  W (and its bf16 copy) move by TMA in 128 x 32 sub-tiles.
+//
+// Roles: warp 0 = A producer, warp 1 = TMEM owner + MMA issuer, warps 2..5 =
+// epilogue (TMEM lane quadrant = warp % 4), warps 6..9 = sign-tile generators,
+// warp 10 = W tile producer.  TMEM holds two 256-column accumulators so the
+// epilogue of one super-tile overlaps the MMAs of the next.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace logra {
+
+using namespace tc;
+
+namespace {
+
+constexpr int kRows = 128;        // MMA M: rows of W per block
+constexpr int kCols = 256;        // MMA N: columns per super-tile
+constexpr int kRc = 64;           // ranks per K chunk
+constexpr int kSub = 32;          // epilogue sub-tile width (columns)
+constexpr int kAbStages = 2;
+constexpr int kWStages = 3;
+constexpr uint32_t kABytes = 2 * kRows * 128;   // hi + lo: 32 KB
+constexpr uint32_t kBBytes = kRc * kCols * 2;   // 64 ranks x 256 columns bf16: 32 KB
+constexpr uint32_t kWBytes = kRows * kSub * 4;  // fp32 sub-tile: 16 KB
+constexpr uint32_t kHBytes = kRows * kSub * 2;  // bf16 sub-tile: 8 KB
+
+struct ApplyShared {
+  uint64_t ab_full[kAbStages], gen_full[kAbStages], ab_empty[kAbStages];
+  uint64_t w_full[kWStages], w_empty[kWStages];
+  uint64_t tmem_full[2], tmem_empty[2], drain;
+  uint32_t tmem_base;
+  int abort;
+  int flag;
+  double red[4];
+};
+
+constexpr size_t kApplySmem = 1024 + kAbStages * (kABytes + kBBytes) + kWStages * kWBytes + kHBytes +
+                              sizeof(ApplyShared) + 64;
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Wait taken by the whole 128-thread epilogue group with one verdict: one
+// thread waits (bounded), the group synchronises, every thread then observes
+// the completed phase itself.  Uniform verdicts keep the group's named
+// barriers matched even when a wait gives up.
+__device__ __forceinline__ bool group_wait(ApplyShared* sh, uint64_t* bar, uint32_t parity,
+                                           unsigned long long limit, Control* ctl, int et) {
+  if (et == 0) sh->flag = wait_or_abort(sh, bar, parity, limit, ctl) ? 1 : 0;
+  epi_sync();
+  const int ok = *reinterpret_cast<volatile int*>(&sh->flag);
+  epi_sync();
+  if (ok) (void)mbar_try_wait(bar, parity);
+  return ok != 0;
+}
+
+}  // namespace
+
+struct ApplyArgs {
+  int64_t d, k;
+  int r;
+  int nsuper;                 // column super-tiles per row block
+  int units;                  // row blocks x super-tiles
+  uint64_t key;
+  float neg_lrc_scale;        // -lr c / sqrt(r)   (apply, predict)
+  float scale;                // 1 / sqrt(r)       (rebuild)
+  int accumulate;             // rebuild: add into the output
+  int write_bf16;             // apply: also store the bf16 copy
+  const uint8_t* s_image;     // [row block][rank chunk][hi | lo][128 rows][128 B]
+  const float* inv_den;       // d values 1/sqrt(v_i + eps)
+  double* dw2_part;           // one per CTA
+};
+
+// MODE 0 apply, 1 predict, 2 rebuild fp32, 3 rebuild bf16.
+template <int MODE>
+__global__ void __launch_bounds__(352, 1)
+    apply_tc_kernel(const __grid_constant__ CUtensorMap tmap_f32, const __grid_constant__ CUtensorMap tmap_b16,
+                    ApplyArgs A, Control* ctl) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  uint8_t* ab = base;                                              // [stage][A 32 KB | B 32 KB]
+  uint8_t* wr = ab + kAbStages * (kABytes + kBBytes);              // [stage][16 KB]
+  uint8_t* hb = wr + kWStages * kWBytes;                           // 8 KB bf16 staging
+  ApplyShared* sh = reinterpret_cast<ApplyShared*>(hb + kHBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned long long limit = ctl->wait_limit;
+  const int nchunks = A.r / kRc + ((A.r % kRc) ? 1 : 0);
+  constexpr bool kLoadIn = (MODE == 0);
+  const bool load_in = kLoadIn || ((MODE == 2 || MODE == 3) && A.accumulate);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kAbStages; ++s) {
+      mbar_init(&sh->ab_full[s], 1);
+      mbar_init(&sh->gen_full[s], 4);
+      mbar_init(&sh->ab_empty[s], 1);
+    }
+    for (int s = 0; s < kWStages; ++s) {
+      mbar_init(&sh->w_full[s], 1);
+      mbar_init(&sh->w_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sh->tmem_full[b], 1);
+      mbar_init(&sh->tmem_empty[b], 4);
+    }
+    mbar_init(&sh->drain, 1);
+    sh->abort = 0;
+    fence_mbar_init();
+    if (MODE == 0 || MODE == 2) prefetch_tmap(&tmap_f32);
+    if ((MODE == 0 && A.write_bf16) || MODE == 3) prefetch_tmap(&tmap_b16);
+  }
+  if (warp == 1) {
+    tmem_alloc(&sh->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ A producer (S hi/lo chunks)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int inject = ctl->inject_fault && blockIdx.x == 0;
+      for (int u = blockIdx.x; u < A.units; u += gridDim.x) {
+        const int rb = u / A.nsuper;
+        for (int c = 0; c < nchunks; ++c) {
+          if (!wait_or_abort(sh, &sh->ab_empty[stage], phase ^ 1u, limit, ctl)) goto a_done;
+          if (inject && c == 0) {
+            inject = 0;
+          } else {
+            mbar_arrive_expect_tx(&sh->ab_full[stage], kABytes);
+            bulk_load(ab + stage * (kABytes + kBBytes), A.s_image + (size_t(rb) * nchunks + c) * kABytes, kABytes,
+                      &sh->ab_full[stage]);
+          }
+          if (++stage == kAbStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+    a_done:
+      for (int s = 0; s < kAbStages; ++s) mbar_wait(&sh->ab_full[s], (s < stage) ? phase : (phase ^ 1u), limit);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------------ W tile producer
+    if (lane == 0 && load_in) {
+      int stage = 0;
+      uint32_t phase = 0;
+      const uint32_t bytes = (MODE == 3) ? kHBytes : kWBytes;
+      const CUtensorMap* map = (MODE == 3) ? &tmap_b16 : &tmap_f32;
+      for (int u = blockIdx.x; u < A.units; u += gridDim.x) {
+        const int rb = u / A.nsuper, st = u % A.nsuper;
+        for (int s = 0; s < kCols / kSub; ++s) {
+          const int64_t col0 = int64_t(st) * kCols + s * kSub;
+          if (col0 >= A.k) break;
+          if (!wait_or_abort(sh, &sh->w_empty[stage], phase ^ 1u, limit, ctl)) goto w_done;
+          mbar_arrive_expect_tx(&sh->w_full[stage], bytes);
+          tma_load_2d(wr + stage * kWBytes, map, &sh->w_full[stage], int32_t(col0), rb * kRows);
+          if (++stage == kWStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+    w_done:
+      for (int s = 0; s < kWStages; ++s) mbar_wait(&sh->w_full[s], (s < stage) ? phase : (phase ^ 1u), limit);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t tph[2] = {0, 0};
+      int buf = 0;
+      const uint32_t idesc = idesc_bf16(kRows, kCols, 0, 1);
+      for (int u = blockIdx.x; u < A.units && !sh->abort; u += gridDim.x) {
+        if (!wait_or_abort(sh, &sh->tmem_empty[buf], tph[buf] ^ 1u, limit, ctl)) break;
+        tc_fence_after();
+        const uint32_t dt = tmem + uint32_t(buf * kCols);
+        for (int c = 0; c < nchunks; ++c) {
+          if (!wait_or_abort(sh, &sh->ab_full[stage], phase, limit, ctl)) goto mma_done;
+          if (!wait_or_abort(sh, &sh->gen_full[stage], phase, limit, ctl)) goto mma_done;
+          tc_fence_after();
+          const uint32_t a0 = smem_addr(ab + stage * (kABytes + kBBytes));
+          const uint32_t b0 = a0 + kABytes;
+          const int ksteps = min(kRc, A.r - c * kRc) / 16;
+          for (int ks = 0; ks < ksteps; ++ks) {
+            const uint64_t bd = smem_desc(b0 + ks * 2048, kRc * 128, 1024, kSw128);
+            mma_bf16(dt, smem_desc(a0 + ks * 32, 16, 1024, kSw128), bd, idesc, (c | ks) ? 1u : 0u);
+            mma_bf16(dt, smem_desc(a0 + kRows * 128 + ks * 32, 16, 1024, kSw128), bd, idesc, 1u);
+          }
+          mma_commit(&sh->ab_empty[stage]);
+          if (++stage == kAbStages) { stage = 0; phase ^= 1u; }
+        }
+        mma_commit(&sh->tmem_full[buf]);
+        tph[buf] ^= 1u;
+        buf ^= 1;
+      }
+    mma_done:
+      mma_commit(&sh->drain);
+      mbar_wait(&sh->drain, 0, limit);
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------------ epilogue
+    const int quad = warp & 3;
+    const int row_l = quad * 32 + lane;                  // row within the block = TMEM lane
+    const int et = threadIdx.x - 64;                     // 0..127
+    uint32_t tph[2] = {0, 0};
+    int buf = 0;
+    int wstage = 0;
+    uint32_t wphase = 0;
+    double dw2 = 0.0;
+    for (int u = blockIdx.x; u < A.units; u += gridDim.x) {
+      const int rb = u / A.nsuper, st = u % A.nsuper;
+      if (!group_wait(sh, &sh->tmem_full[buf], tph[buf], limit, ctl, et)) break;
+      tph[buf] ^= 1u;
+      tc_fence_after();
+      const int64_t row = int64_t(rb) * kRows + row_l;
+      const bool row_ok = row < A.d;
+      float f = 0.f;
+      if (MODE == 0 || MODE == 1) f = row_ok ? A.neg_lrc_scale * A.inv_den[row] : 0.f;
+      else f = A.scale;
+      bool aborted = false;
+      for (int s = 0; s < kCols / kSub; ++s) {
+        const int64_t col0 = int64_t(st) * kCols + s * kSub;
+        if (col0 >= A.k) break;
+        uint32_t g[32];
+        tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + uint32_t(buf * kCols + s * kSub), g);
+        tmem_ld_wait();
+        const int ncol = int(A.k - col0 < kSub ? A.k - col0 : kSub);
+        if (MODE == 1) {
+          float acc = 0.f;
+          if (row_ok) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float dw = f * __uint_as_float(g[j]);
+              if (j < ncol) acc = fmaf(dw, dw, acc);
+            }
+          }
+          dw2 += double(acc);
+          continue;
+        }
+        uint8_t* wt = wr + wstage * kWBytes;
+        if (load_in) {
+          if (!group_wait(sh, &sh->w_full[wstage], wphase, limit, ctl, et)) { aborted = true; break; }
+        }
+        if (MODE == 0 || MODE == 2) {
+          // fp32 sub-tile, 128-byte rows, 16-byte chunk q at q ^ (row & 7)
+          float acc = 0.f;
+          uint8_t* rowp = wt + row_l * 128;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            float4* p = reinterpret_cast<float4*>(rowp + ((q ^ (row_l & 7)) << 4));
+            float4 w = load_in ? *p : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float d0 = f * __uint_as_float(g[4 * q + 0]), d1 = f * __uint_as_float(g[4 * q + 1]);
+            const float d2 = f * __uint_as_float(g[4 * q + 2]), d3 = f * __uint_as_float(g[4 * q + 3]);
+            if (MODE == 0) {
+              if (4 * q + 0 < ncol) acc = fmaf(d0, d0, acc);
+              if (4 * q + 1 < ncol) acc = fmaf(d1, d1, acc);
+              if (4 * q + 2 < ncol) acc = fmaf(d2, d2, acc);
+              if (4 * q + 3 < ncol) acc = fmaf(d3, d3, acc);
+            }
+            w.x += d0; w.y += d1; w.z += d2; w.w += d3;
+            *p = w;
+            if (MODE == 0 && A.write_bf16) {
+              // bf16 staging: 64-byte rows, 16-byte chunk h at h ^ ((row >> 1) & 3)
+              const int h = q >> 1;
+              uint2 packed;
+              packed.x = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(w.x))) |
+                         (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(w.y))) << 16);
+              packed.y = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(w.z))) |
+                         (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(w.w))) << 16);
+              *reinterpret_cast<uint2*>(hb + row_l * 64 + ((h ^ ((row_l >> 1) & 3)) << 4) + (q & 1) * 8) = packed;
+            }
+          }
+          if (MODE == 0 && row_ok) dw2 += double(acc);
+        } else {
+          // MODE 3: bf16 output sub-tile (64-byte rows) in the staging buffer
+          const uint8_t* src = wt + row_l * 64;
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const int off = (h ^ ((row_l >> 1) & 3)) << 4;
+            uint4 in = load_in ? *reinterpret_cast<const uint4*>(src + off) : make_uint4(0, 0, 0, 0);
+            const uint32_t iw[4] = {in.x, in.y, in.z, in.w};
+            uint32_t ow[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float lo = __uint_as_float(iw[e] << 16) + f * __uint_as_float(g[8 * h + 2 * e]);
+              const float hi = __uint_as_float(iw[e] & 0xFFFF0000u) + f * __uint_as_float(g[8 * h + 2 * e + 1]);
+              ow[e] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+                      (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+            }
+            *reinterpret_cast<uint4*>(hb + row_l * 64 + off) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+          }
+        }
+        fence_proxy_async_smem();
+        epi_sync();
+        if (et == 0) {
+          if (MODE == 0 || MODE == 2) tma_store_2d(&tmap_f32, wt, int32_t(col0), rb * kRows);
+          if ((MODE == 0 && A.write_bf16) || MODE == 3) tma_store_2d(&tmap_b16, hb, int32_t(col0), rb * kRows);
+          bulk_commit();
+          bulk_wait_read_all();
+          if (load_in) mbar_arrive(&sh->w_empty[wstage]);
+        }
+        epi_sync();
+        if (load_in) {
+          if (++wstage == kWStages) { wstage = 0; wphase ^= 1u; }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->tmem_empty[buf]);
+      buf ^= 1;
+      if (aborted) break;
+    }
+    if (et == 0) bulk_wait_all();
+    if (MODE == 0 || MODE == 1) {
+      // per-CTA sum of dW^2 over this CTA's rows and columns, fixed order
+      for (int o = 16; o; o >>= 1) dw2 += __shfl_xor_sync(0xffffffffu, dw2, o);
+      if (lane == 0) sh->red[quad] = dw2;
+      epi_sync();
+      if (et == 0) A.dw2_part[blockIdx.x] = sh->red[0] + sh->red[1] + sh->red[2] + sh->red[3];
+    }
+  } else if (warp < 10) {
+    // ------------------------------------------------------------------ sign-tile generators (MN-major)
+    const int gtid = threadIdx.x - 192;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int u = blockIdx.x; u < A.units; u += gridDim.x) {
+      const int st = u % A.nsuper;
+      for (int c = 0; c < nchunks; ++c) {
+        if (!warp_wait(sh, &sh->ab_empty[stage], phase ^ 1u, limit, ctl)) goto gen_done;
+        uint8_t* bt = ab + stage * (kABytes + kBBytes) + kABytes;
+        // 4 groups of 64 columns x 64 rank rows; row = one sign word (64 columns)
+        for (int e = gtid; e < 4 * kRc; e += 128) {
+          const int grp = e / kRc, a_l = e % kRc;
+          const int a = c * kRc + a_l;
+          const uint64_t w = a < A.r ? sign_word(A.key, uint32_t(a), uint32_t(st * (kCols / 64) + grp)) : 0ull;
+          uint8_t* rowp = bt + grp * (kRc * 128) + a_l * 128;
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<uint4*>(rowp + ((q ^ (a_l & 7)) << 4)) = signs8_to_bf16(uint32_t(w >> (8 * q)) & 0xFFu);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->gen_full[stage]);
+        if (++stage == kAbStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+  gen_done:;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// S image for the A operand: rows split into bf16 hi + lo, 64-rank chunks of
+// 128-byte rows, 16-byte chunk q of row i stored at q ^ (i & 7).
+__global__ void s_image_kernel(const float* __restrict__ S, int64_t d, int r, uint8_t* __restrict__ img) {
+  const int nchunks = (r + kRc - 1) / kRc;
+  const int64_t rows_pad = ((d + kRows - 1) / kRows) * kRows;
+  const int64_t total = rows_pad * nchunks * 8;   // one thread per (row, chunk, 8-rank group)
+  for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total; e += int64_t(gridDim.x) * blockDim.x) {
+    const int q = int(e & 7);
+    const int c = int((e >> 3) % nchunks);
+    const int64_t row = (e >> 3) / nchunks;
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int a = c * kRc + q * 8 + i;
+      v[i] = (row < d && a < r) ? S[row * r + a] : 0.f;
+    }
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * i]), h1 = __float2bfloat16_rn(v[2 * i + 1]);
+      const __nv_bfloat16 l0 = __float2bfloat16_rn(v[2 * i] - __bfloat162float(h0));
+      const __nv_bfloat16 l1 = __float2bfloat16_rn(v[2 * i + 1] - __bfloat162float(h1));
+      hi[i] = uint32_t(__bfloat16_as_ushort(h0)) | (uint32_t(__bfloat16_as_ushort(h1)) << 16);
+      lo[i] = uint32_t(__bfloat16_as_ushort(l0)) | (uint32_t(__bfloat16_as_ushort(l1)) << 16);
+    }
+    const int64_t rb = row / kRows;
+    const int rl = int(row % kRows);
+    uint8_t* chunk = img + (size_t(rb) * nchunks + c) * kABytes;
+    const int off = rl * 128 + ((q ^ (rl & 7)) << 4);
+    *reinterpret_cast<uint4*>(chunk + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(chunk + kRows * 128 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  }
+}
+
+size_t s_image_bytes(int64_t d, int r) {
+  const int64_t rb = (d + kRows - 1) / kRows;
+  const int nchunks = (r + kRc - 1) / kRc;
+  return size_t(rb) * nchunks * kABytes;
+}
+
+int launch_s_image(const float* S, int64_t d, int r, uint8_t* img, cudaStream_t s) {
+  const int nchunks = (r + kRc - 1) / kRc;
+  const int64_t total = ((d + kRows - 1) / kRows) * kRows * nchunks * 8;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > int64_t(sm_count()) * 8) blocks = int64_t(sm_count()) * 8;
+  s_image_kernel<<<unsigned(blocks), 256, 0, s>>>(S, d, r, img);
+  LOGRA_LAUNCHED();
+  return LOGRA_OK;
+}
+
+int launch_apply_tc(int mode, float* W, __nv_bfloat16* Wb, void* out, int accumulate, int64_t d, int64_t k, int r,
+                    uint64_t key, float neg_lrc, const uint8_t* s_img, const float* inv_den, double* dw2_part,
+                    int* grid_out, Control* ctl, cudaStream_t s) {
+  const int sms = sm_count();
+  ApplyArgs A{};
+  A.d = d; A.k = k; A.r = r;
+  A.nsuper = int((k + kCols - 1) / kCols);
+  const int64_t rbs = (d + kRows - 1) / kRows;
+  A.units = int(rbs * A.nsuper);
+  A.key = key;
+  A.scale = inv_sqrt_r(r);
+  A.neg_lrc_scale = neg_lrc * A.scale;
+  A.accumulate = accumulate;
+  A.write_bf16 = (mode == 0 && Wb) ? 1 : 0;
+  A.s_image = s_img;
+  A.inv_den = inv_den;
+  A.dw2_part = dw2_part;
+  CUtensorMap t32{}, t16{};
+  if (mode == 0 || mode == 2) {
+    const void* p = mode == 0 ? static_cast<const void*>(W) : out;
+    if (int st = make_tmap_2d(&t32, p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(k), uint64_t(d), uint64_t(k) * 4,
+                              kSub, kRows, CU_TENSOR_MAP_SWIZZLE_128B))
+      return st;
+  }
+  if ((mode == 0 && Wb) || mode == 3) {
+    const void* p = mode == 0 ? static_cast<const void*>(Wb) : out;
+    if (int st = make_tmap_2d(&t16, p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, uint64_t(k), uint64_t(d),
+                              uint64_t(k) * 2, kSub, kRows, CU_TENSOR_MAP_SWIZZLE_64B))
+      return st;
+  }
+  const int grid = A.units < sms ? A.units : sms;
+  *grid_out = grid;
+  auto run = [&](auto kern) -> int {
+    LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(kern), int(kApplySmem)));
+    kern<<<grid, 352, kApplySmem, s>>>(t32, t16, A, ctl);
+    LOGRA_LAUNCHED();
+    return LOGRA_OK;
+  };
+  switch (mode) {
+    case 0: return run(apply_tc_kernel<0>);
+    case 1: return run(apply_tc_kernel<1>);
+    case 2: return run(apply_tc_kernel<2>);
+    default: return run(apply_tc_kernel<3>);
+  }
+}
+
+}  // namespace logra

@@ -56,6 +56,9 @@ void* workspace(cudaStream_t stream, size_t bytes, int* status);
 int sm_count();
 int cuda_fail(cudaError_t e);
 void count_launch();
+// Raise a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device; remembered per (device, kernel) so repeated calls are free.
+cudaError_t ensure_smem(const void* kernel, int bytes);
 
 }  // namespace logra
 

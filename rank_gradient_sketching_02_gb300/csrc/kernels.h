@@ -11,8 +11,8 @@ namespace logra {
 struct Control;
 
 struct ApplyWorkspace {
-  size_t words_off, gram_off, inv_off, ssq_off, dw2_off, bytes;
-  int n_ssq, n_dw2;
+  size_t words_off, gram_off, inv_off, ssq_off, dw2_off, img_off, bytes;
+  int n_ssq;
 };
 
 ApplyWorkspace apply_workspace_layout(int64_t d, int64_t k, int r);
@@ -27,9 +27,15 @@ size_t sketch_tc_workspace_bytes(int64_t n, int64_t d, int64_t k, int r, int sms
 int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_t k, int r, uint64_t key,
                      float scale, float* S, void* ws, Control* ctl, cudaStream_t s);
 
+size_t s_image_bytes(int64_t d, int r);
+int launch_s_image(const float* S, int64_t d, int r, uint8_t* img, cudaStream_t s);
+int launch_apply_tc(int mode, float* W, __nv_bfloat16* Wb, void* out, int accumulate, int64_t d, int64_t k, int r,
+                    uint64_t key, float neg_lrc, const uint8_t* s_img, const float* inv_den, double* dw2_part,
+                    int* grid_out, Control* ctl, cudaStream_t s);
+
 // mode 0 apply, 1 predict, 2 reconstruct fp32, 3 reconstruct bf16.
-int launch_rowadam_simt(int mode, float* W, __nv_bfloat16* Wb, void* out, int accumulate, const float* S,
-                        const float* v_in, float* v_out, float* sync_out, int64_t d, int64_t k, int r, uint64_t key,
-                        float beta2, float eps, float lrc, double* norms, char* ws, cudaStream_t s);
+int launch_rowadam(int mode, float* W, __nv_bfloat16* Wb, void* out, int accumulate, const float* S,
+                   const float* v_in, float* v_out, float* sync_out, int64_t d, int64_t k, int r, uint64_t key,
+                   float beta2, float eps, float lrc, double* norms, char* ws, Control* ctl, cudaStream_t s);
 
 }  // namespace logra

@@ -1,8 +1,10 @@
-// RowAdam apply from the sketch (theclarity.today write-up, "What happened":
-// per-row squared magnitudes, no first moment), on CUDA cores:
-//   rownorm:  q_i = ||(S A)_i||^2 = S_i M S_i^T / r with M = Sigma Sigma^T,
-//             v_i <- beta2 v_i + (1 - beta2) q_i / k, inv_i = 1/sqrt(v_i + eps)
-//   apply:    W_ij += -lr c (S A)_ij inv_i, tile by tile, A regenerated
+// RowAdam's per-row statistic and the norms, plus the orchestration of one
+// apply (theclarity.today write-up, "What happened": running estimates of
+// squared row magnitudes, no first moment):
+//   rownorm:  q_i = ||(S A)_i||^2 = S_i M S_i^T / r with M = Sigma Sigma^T
+//             (exact integers from popcounts), v_i <- beta2 v_i + (1-beta2) q_i/k,
+//             inv_i = 1/sqrt(v_i + eps), optional sync sketch, ||S||^2 partials
+//   apply:    the tensor-core reconstruct-and-update kernel (apply_tc.cu)
 //   norms:    {||S||^2, ||dW||^2} reduced in fp64 in a fixed order.
 #include "common.cuh"
 #include "kernels.h"
@@ -84,75 +86,6 @@ __global__ void __launch_bounds__(256) rownorm_kernel(const float* __restrict__ 
   if (threadIdx.x == 0) ssq_part[blockIdx.x] = dred[0];
 }
 
-// Tile of 16 rows x 256 columns; thread = one column, 16 rows.
-// MODE 0: RowAdam apply (optionally the bf16 copy);  MODE 1: predict (norm only);
-// MODE 2: reconstruct to fp32;  MODE 3: reconstruct to bf16.
-constexpr int kApplyRows = 16, kApplyCols = 256;
-
-template <int MODE>
-__global__ void __launch_bounds__(256) apply_simt_kernel(float* __restrict__ W, __nv_bfloat16* __restrict__ Wb,
-                                                         void* __restrict__ out, int accumulate,
-                                                         const float* __restrict__ S,
-                                                         const float* __restrict__ inv_den, int64_t d, int64_t k,
-                                                         int r, uint64_t key, float scale, float neg_lrc,
-                                                         double* __restrict__ dw2_part) {
-  extern __shared__ float smem[];
-  float* ss = smem;                                                  // [16][r]
-  uint64_t* ws = reinterpret_cast<uint64_t*>(smem + kApplyRows * r); // [r][4]
-  const int64_t i0 = int64_t(blockIdx.y) * kApplyRows;
-  const int64_t j0 = int64_t(blockIdx.x) * kApplyCols;
-  const int rows = int(d - i0 < kApplyRows ? d - i0 : kApplyRows);
-  for (int e = threadIdx.x; e < kApplyRows * r; e += blockDim.x) {
-    const int rr = e / r;
-    ss[e] = rr < rows ? S[(i0 + rr) * r + (e - rr * r)] : 0.f;
-  }
-  for (int e = threadIdx.x; e < r * 4; e += blockDim.x)
-    ws[e] = sign_word(key, uint32_t(e >> 2), uint32_t((j0 >> 6) + (e & 3)));
-  __syncthreads();
-  const int jl = threadIdx.x;
-  const int64_t j = j0 + jl;
-  float acc[kApplyRows];
-#pragma unroll
-  for (int q = 0; q < kApplyRows; ++q) acc[q] = 0.f;
-  for (int a = 0; a < r; ++a) {
-    const uint32_t sg = (uint32_t(ws[a * 4 + (jl >> 6)] >> (jl & 63)) & 1u) << 31;
-#pragma unroll
-    for (int q = 0; q < kApplyRows; ++q) acc[q] += __uint_as_float(__float_as_uint(ss[q * r + a]) ^ sg);
-  }
-  float dw2 = 0.f;
-  if (j < k) {
-    for (int q = 0; q < rows; ++q) {
-      const int64_t i = i0 + q;
-      const float g = acc[q] * scale;        // (S A)_ij
-      if (MODE == 0 || MODE == 1) {
-        const float dw = neg_lrc * g * inv_den[i];
-        dw2 = fmaf(dw, dw, dw2);
-        if (MODE == 0) {
-          const float wn = W[i * k + j] + dw;
-          W[i * k + j] = wn;
-          if (Wb) Wb[i * k + j] = __float2bfloat16_rn(wn);
-        }
-      } else if (MODE == 2) {
-        float* o = static_cast<float*>(out) + i * k + j;
-        *o = accumulate ? *o + g : g;
-      } else {
-        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out) + i * k + j;
-        *o = __float2bfloat16_rn(accumulate ? __bfloat162float(*o) + g : g);
-      }
-    }
-  }
-  if (MODE == 0 || MODE == 1) {
-    __shared__ double red[256];
-    red[threadIdx.x] = double(dw2);
-    __syncthreads();
-    for (int o = 128; o; o >>= 1) {
-      if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
-      __syncthreads();
-    }
-    if (threadIdx.x == 0) dw2_part[int64_t(blockIdx.y) * gridDim.x + blockIdx.x] = red[0];
-  }
-}
-
 // norms[0] = sum ssq_part, norms[1] = sum dw2_part (fixed order, one block).
 __global__ void norms_kernel(const double* __restrict__ ssq, int nssq, const double* __restrict__ dw2, int ndw2,
                              double* __restrict__ norms) {
@@ -182,56 +115,43 @@ ApplyWorkspace apply_workspace_layout(int64_t d, int64_t k, int r) {
   ApplyWorkspace w{};
   const int64_t nw = (k + 63) / 64;
   const int64_t nnorm = (d + kRowsPerNormBlock - 1) / kRowsPerNormBlock;
-  const int64_t ntiles = ((k + kApplyCols - 1) / kApplyCols) * ((d + kApplyRows - 1) / kApplyRows);
   size_t off = 0;
   w.words_off = off;   off += align256(size_t(r) * nw * 8);
   w.gram_off = off;    off += align256(size_t(r) * r * 4);
   w.inv_off = off;     off += align256(size_t(d) * 4);
   w.ssq_off = off;     off += align256(size_t(nnorm) * 8);
-  w.dw2_off = off;     off += align256(size_t(ntiles) * 8);
+  w.dw2_off = off;     off += align256(size_t(1024) * 8);
+  w.img_off = off;     off += align256(s_image_bytes(d, r));
   w.n_ssq = int(nnorm);
-  w.n_dw2 = int(ntiles);
   w.bytes = off;
   return w;
 }
 
-int launch_rowadam_simt(int mode, float* W, __nv_bfloat16* Wb, void* out, int accumulate, const float* S,
-                        const float* v_in, float* v_out, float* sync_out, int64_t d, int64_t k, int r, uint64_t key,
-                        float beta2, float eps, float lrc, double* norms, char* ws, cudaStream_t s) {
+// mode 0 apply, 1 predict (norms only), 2 rebuild fp32, 3 rebuild bf16.
+int launch_rowadam(int mode, float* W, __nv_bfloat16* Wb, void* out, int accumulate, const float* S,
+                   const float* v_in, float* v_out, float* sync_out, int64_t d, int64_t k, int r, uint64_t key,
+                   float beta2, float eps, float lrc, double* norms, char* ws, Control* ctl, cudaStream_t s) {
   const ApplyWorkspace L = apply_workspace_layout(d, k, r);
   float* inv = reinterpret_cast<float*>(ws + L.inv_off);
   double* ssq = reinterpret_cast<double*>(ws + L.ssq_off);
   double* dw2 = reinterpret_cast<double*>(ws + L.dw2_off);
-  const float scale = inv_sqrt_r(r);
+  uint8_t* img = reinterpret_cast<uint8_t*>(ws + L.img_off);
   if (mode == 0 || mode == 1) {
     uint64_t* words = reinterpret_cast<uint64_t*>(ws + L.words_off);
     float* M = reinterpret_cast<float*>(ws + L.gram_off);
-    int st = launch_gram(key, r, k, words, M, s);
-    if (st) return st;
+    if (int st = launch_gram(key, r, k, words, M, s)) return st;
     const size_t sm = size_t(kRowsPerNormBlock) * r * 4;
-    LOGRA_CUDA_TRY(cudaFuncSetAttribute(rownorm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm)));
+    LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(rownorm_kernel), int(sm)));
     rownorm_kernel<<<unsigned(L.n_ssq), 256, sm, s>>>(S, M, v_in, v_out, inv, ssq, sync_out, d, k, r, beta2, eps,
                                                        lrc);
     LOGRA_LAUNCHED();
   }
-  dim3 grid(unsigned((k + kApplyCols - 1) / kApplyCols), unsigned((d + kApplyRows - 1) / kApplyRows));
-  const size_t sm = size_t(kApplyRows) * r * 4 + size_t(r) * 4 * 8;
-  auto run = [&](auto kern) -> int {
-    LOGRA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm)));
-    kern<<<grid, 256, sm, s>>>(W, Wb, out, accumulate, S, inv, d, k, r, key, scale, -lrc, dw2);
-    LOGRA_LAUNCHED();
-    return LOGRA_OK;
-  };
-  int st;
-  switch (mode) {
-    case 0: st = run(apply_simt_kernel<0>); break;
-    case 1: st = run(apply_simt_kernel<1>); break;
-    case 2: st = run(apply_simt_kernel<2>); break;
-    default: st = run(apply_simt_kernel<3>); break;
-  }
-  if (st) return st;
+  if (int st = launch_s_image(S, d, r, img, s)) return st;
+  int grid = 0;
+  if (int st = launch_apply_tc(mode, W, Wb, out, accumulate, d, k, r, key, -lrc, img, inv, dw2, &grid, ctl, s))
+    return st;
   if ((mode == 0 || mode == 1) && norms) {
-    norms_kernel<<<1, 256, 0, s>>>(ssq, L.n_ssq, dw2, L.n_dw2, norms);
+    norms_kernel<<<1, 256, 0, s>>>(ssq, L.n_ssq, dw2, grid, norms);
     LOGRA_LAUNCHED();
   }
   return LOGRA_OK;

@@ -15,10 +15,15 @@
 // backpropagation and G is never formed; academy.dair.ai summary: the random-
 // sign projection is redrawn per step and shared by the step's microbatches.)
 //
-// Roles per CTA: warp 0 = TMA producer, warp 1 = TMEM owner + MMA issuer,
-// warps 2..5 = epilogue (TMEM lane quadrant = warp % 4), warps 6..9 (project
-// only) = sign-tile generators.  Every wait is bounded; a wait that runs out
-// records LOGRA_ERR_TIMEOUT in the control block and the CTA drains and exits.
+// The operand streamed from HBM (X, dY) and the other operand (the generated
+// sign tile, the L2-resident P^T image) move through separate shared-memory
+// rings, so the HBM stream gets the deep ring its latency needs.
+//
+// Roles per CTA: warp 0 = producer of the first ring, warp 1 = TMEM owner +
+// MMA issuer, warps 2..5 = epilogue (TMEM lane quadrant = warp % 4), warps
+// 6..9 = sign-tile generators (project) / warp 6 = dY producer (accumulate).
+// Every wait is bounded; a wait that runs out records LOGRA_ERR_TIMEOUT in the
+// control block and the CTA drains and exits.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -34,7 +39,8 @@ namespace {
 constexpr int kTok = 128;      // tokens per project tile (MMA M)
 constexpr int kKc = 64;        // k per project stage (one sign word per row)
 constexpr int kChunk = 32;     // tokens per accumulate stage / image chunk
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 16;
+constexpr int kSmemBudget = 227 * 1024 - 1024 - 512;
 
 struct SketchShape {
   int64_t n, d, k;
@@ -42,34 +48,35 @@ struct SketchShape {
   int n_pad;                   // n rounded up to kChunk
   int tiles, splits, chunks_per_split, nchunks;      // project
   int ntile_n, dtiles, tsplits, tchunks_per_split;   // accumulate
-  int proj_stages, acc_stages;
+  int x_stages, g_stages;      // project rings: X tiles, sign tiles
+  int a_stages, b_stages;      // accumulate rings: P^T chunks, dY tiles
 };
 
 struct Shared {
-  uint64_t full[kMaxStages];     // project: TMA bytes; accumulate: TMA bytes
-  uint64_t gen[kMaxStages];      // project: 4 generator warps
-  uint64_t empty[kMaxStages];    // MMA commit
-  uint64_t tmem_full, tmem_empty, drain;
+  uint64_t s_full[kMaxStages], s_empty[kMaxStages];   // streamed operand (X / dY)
+  uint64_t o_full[kMaxStages], o_empty[kMaxStages];   // other operand (sign tile / P^T chunk)
+  uint64_t tmem_full[2], tmem_empty[4], drain;
+  uint2 nib[16];                                       // 4 sign bits -> 4 bf16 +-1
   uint32_t tmem_base;
   int abort;
+};
+
+struct Ring {
+  int stage = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++stage == n) { stage = 0; phase ^= 1u; }
+  }
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-__device__ __forceinline__ bool wait_or_abort(Shared* sh, uint64_t* bar, uint32_t parity, unsigned long long limit,
-                                              Control* ctl) {
-  while (!mbar_wait(bar, parity, limit / 8 + 1)) {
-    if (*reinterpret_cast<volatile int*>(&sh->abort)) return false;
-    limit -= limit / 8 + 1;
-    if (limit < 16) {
-      record_status(ctl, LOGRA_ERR_TIMEOUT);
-      *reinterpret_cast<volatile int*>(&sh->abort) = 1;
-      return false;
-    }
-  }
-  return true;
+// Copies still in flight land before the CTA exits: wait (bounded) for the
+// last phase issued on every stage of a ring; phases already consumed pass.
+__device__ __forceinline__ void drain_ring(uint64_t* full, const Ring& rg, int n, unsigned long long limit) {
+  for (int s = 0; s < n; ++s) mbar_wait(&full[s], (s < rg.stage) ? rg.phase : (rg.phase ^ 1u), limit);
 }
 
 }  // namespace
@@ -77,14 +84,17 @@ __device__ __forceinline__ bool wait_or_abort(Shared* sh, uint64_t* bar, uint32_
 // ============================================================================ project
 // Sigma tile for k-chunk c: rows b < r of 128 bytes (64 bf16 +-1), K-major,
 // 128-byte swizzle (16-byte chunk q of row b stored at chunk q ^ (b & 7)).
-__device__ __forceinline__ void gen_sigma_kmajor(uint8_t* tile, uint64_t key, int r, int c, int tid, int nthr) {
+__device__ __forceinline__ void gen_sigma_kmajor(uint8_t* tile, const uint2* nib, uint64_t key, int r, int c, int tid,
+                                                 int nthr) {
   for (int b = tid; b < r; b += nthr) {
     const uint64_t w = sign_word(key, uint32_t(b), uint32_t(c));
+    const uint32_t lo = uint32_t(w), hi = uint32_t(w >> 32);
     uint8_t* row = tile + size_t(b) * 128;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      const uint4 v = signs8_to_bf16(uint32_t(w >> (8 * q)) & 0xFFu);
-      *reinterpret_cast<uint4*>(row + ((q ^ (b & 7)) << 4)) = v;
+      const uint32_t byte = ((q < 4 ? lo : hi) >> (8 * (q & 3))) & 0xFFu;
+      const uint2 a = nib[byte & 15u], bb = nib[byte >> 4];
+      *reinterpret_cast<uint4*>(row + ((q ^ (b & 7)) << 4)) = make_uint4(a.x, a.y, bb.x, bb.y);
     }
   }
 }
@@ -95,30 +105,42 @@ __global__ void __launch_bounds__(320, 1)
   extern __shared__ uint8_t smem_raw[];
   const SketchShape& P = sh_;
   uint8_t* base = align1024(smem_raw);
-  const int S = P.proj_stages;
-  const uint32_t a_bytes = kTok * 128;
-  const uint32_t b_bytes = uint32_t(P.r) * 128;
-  uint8_t* a_tiles = base;
-  uint8_t* b_tiles = base + size_t(S) * a_bytes;
-  Shared* sh = reinterpret_cast<Shared*>(b_tiles + size_t(S) * b_bytes);
+  const int XS = P.x_stages, GS = P.g_stages;
+  const uint32_t x_bytes = kTok * 128;
+  const uint32_t g_bytes = uint32_t(P.r) * 128;
+  uint8_t* x_tiles = base;
+  uint8_t* g_tiles = base + size_t(XS) * x_bytes;
+  Shared* sh = reinterpret_cast<Shared*>(g_tiles + size_t(GS) * g_bytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned long long limit = ctl->wait_limit;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&sh->full[s], 1);
-      mbar_init(&sh->gen[s], 4);
-      mbar_init(&sh->empty[s], 1);
+    for (int s = 0; s < XS; ++s) {
+      mbar_init(&sh->s_full[s], 1);
+      mbar_init(&sh->s_empty[s], 1);
     }
-    mbar_init(&sh->tmem_full, 1);
-    mbar_init(&sh->tmem_empty, 4);
+    for (int s = 0; s < GS; ++s) {
+      mbar_init(&sh->o_full[s], 4);
+      mbar_init(&sh->o_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sh->tmem_full[b], 1);
+      mbar_init(&sh->tmem_empty[b], 4);
+    }
     mbar_init(&sh->drain, 1);
     sh->abort = 0;
     fence_mbar_init();
     prefetch_tmap(&tmap_x);
   }
-  uint32_t tmem_cols = 32;
-  while (tmem_cols < uint32_t(P.r)) tmem_cols <<= 1;
+  if (threadIdx.x < 16) {
+    const uint4 v = signs8_to_bf16(threadIdx.x);       // elements 0..3 of the nibble in .x, .y
+    sh->nib[threadIdx.x] = make_uint2(v.x, v.y);
+  }
+  // one accumulator of r columns, two (double buffered) when they fit
+  uint32_t acc_cols = 32;
+  while (acc_cols < uint32_t(P.r)) acc_cols <<= 1;
+  const int nbuf = acc_cols <= 256 ? 2 : 1;
+  const uint32_t tmem_cols = acc_cols * nbuf;
   if (warp == 1) {
     tmem_alloc(&sh->tmem_base, tmem_cols);
     tmem_relinquish();
@@ -130,39 +152,34 @@ __global__ void __launch_bounds__(320, 1)
   const int units = P.tiles * P.splits;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer (X tiles)
+    // ---------------------------------------------------------------- X tile producer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
+      Ring xr;
       int inject = ctl->inject_fault && blockIdx.x == 0;
       for (int u = blockIdx.x; u < units; u += gridDim.x) {
         const int tile = u % P.tiles, split = u / P.tiles;
         const int c0 = split * P.chunks_per_split;
         const int c1 = min(P.nchunks, c0 + P.chunks_per_split);
         for (int c = c0; c < c1; ++c) {
-          if (!wait_or_abort(sh, &sh->empty[stage], phase ^ 1u, limit, ctl)) goto producer_done;
+          if (!wait_or_abort(sh, &sh->s_empty[xr.stage], xr.phase ^ 1u, limit, ctl)) goto producer_done;
           if (inject && c == c0 + 1) {
             inject = 0;                      // test hook: this stage never fills
           } else {
-            mbar_arrive_expect_tx(&sh->full[stage], a_bytes);
-            tma_load_2d(a_tiles + size_t(stage) * a_bytes, &tmap_x, &sh->full[stage], c * kKc, tile * kTok);
+            mbar_arrive_expect_tx(&sh->s_full[xr.stage], x_bytes);
+            tma_load_2d(x_tiles + size_t(xr.stage) * x_bytes, &tmap_x, &sh->s_full[xr.stage], c * kKc, tile * kTok);
           }
-          if (++stage == S) { stage = 0; phase ^= 1u; }
+          xr.next(XS);
         }
       }
     producer_done:
-      // Copies still in flight land before the CTA exits: wait for the last
-      // phase issued on every stage (bounded; phases already consumed pass).
-      for (int s = 0; s < S; ++s) {
-        const uint32_t ph = (s < stage) ? phase : (phase ^ 1u);
-        mbar_wait(&sh->full[s], ph, limit);
-      }
+      drain_ring(sh->s_full, xr, XS, limit);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0, tphase = 0;
+      Ring xr, gr;
+      uint32_t tph[2] = {0, 0};
+      int buf = 0;
       const int nparts = P.r > 256 ? 2 : 1;
       const int npart = P.r / nparts;
       const uint32_t idesc = idesc_bf16(128, uint32_t(npart), 0, 0);
@@ -170,29 +187,33 @@ __global__ void __launch_bounds__(320, 1)
         const int split = u / P.tiles;
         const int c0 = split * P.chunks_per_split;
         const int c1 = min(P.nchunks, c0 + P.chunks_per_split);
-        if (!wait_or_abort(sh, &sh->tmem_empty, tphase ^ 1u, limit, ctl)) break;
+        if (!wait_or_abort(sh, &sh->tmem_empty[buf], tph[buf] ^ 1u, limit, ctl)) break;
         tc_fence_after();
+        const uint32_t dacc = tmem + uint32_t(buf) * acc_cols;
         bool first = true;
         for (int c = c0; c < c1; ++c) {
-          if (!wait_or_abort(sh, &sh->full[stage], phase, limit, ctl)) goto mma_done;
-          if (!wait_or_abort(sh, &sh->gen[stage], phase, limit, ctl)) goto mma_done;
+          if (!wait_or_abort(sh, &sh->s_full[xr.stage], xr.phase, limit, ctl)) goto mma_done;
+          if (!wait_or_abort(sh, &sh->o_full[gr.stage], gr.phase, limit, ctl)) goto mma_done;
           tc_fence_after();
-          const uint32_t a0 = smem_addr(a_tiles + size_t(stage) * a_bytes);
-          const uint32_t b0 = smem_addr(b_tiles + size_t(stage) * b_bytes);
+          const uint32_t a0 = smem_addr(x_tiles + size_t(xr.stage) * x_bytes);
+          const uint32_t b0 = smem_addr(g_tiles + size_t(gr.stage) * g_bytes);
 #pragma unroll
           for (int ks = 0; ks < kKc / 16; ++ks) {
             const uint64_t ad = smem_desc(a0 + ks * 32, 16, 1024, kSw128);
             for (int p = 0; p < nparts; ++p) {
               const uint64_t bd = smem_desc(b0 + uint32_t(p * npart) * 128 + ks * 32, 16, 1024, kSw128);
-              mma_bf16(tmem + uint32_t(p * npart), ad, bd, idesc, first ? 0u : 1u);
+              mma_bf16(dacc + uint32_t(p * npart), ad, bd, idesc, first ? 0u : 1u);
             }
             first = false;
           }
-          mma_commit(&sh->empty[stage]);
-          if (++stage == S) { stage = 0; phase ^= 1u; }
+          mma_commit(&sh->s_empty[xr.stage]);
+          mma_commit(&sh->o_empty[gr.stage]);
+          xr.next(XS);
+          gr.next(GS);
         }
-        mma_commit(&sh->tmem_full);
-        tphase ^= 1u;
+        mma_commit(&sh->tmem_full[buf]);
+        tph[buf] ^= 1u;
+        if (nbuf == 2) buf ^= 1;
       }
     mma_done:
       mma_commit(&sh->drain);
@@ -201,17 +222,18 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp < 6) {
     // ---------------------------------------------------------------- epilogue: TMEM -> P partials
     const int quad = warp & 3;
-    uint32_t tphase = 0;
+    uint32_t tph[2] = {0, 0};
+    int buf = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const int tile = u % P.tiles, split = u / P.tiles;
-      if (!wait_or_abort(sh, &sh->tmem_full, tphase, limit, ctl)) break;
-      tphase ^= 1u;
+      if (!warp_wait(sh, &sh->tmem_full[buf], tph[buf], limit, ctl)) break;
+      tph[buf] ^= 1u;
       tc_fence_after();
       const int64_t t = int64_t(tile) * kTok + quad * 32 + lane;
       float* dst = ppart + int64_t(split) * P.r * P.n_pad + t;
       for (int c = 0; c < P.r; c += 32) {
         uint32_t v[32];
-        tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + uint32_t(c), v);
+        tmem_ld32(tmem + uint32_t(buf) * acc_cols + (uint32_t(quad * 32) << 16) + uint32_t(c), v);
         tmem_ld_wait();
         if (t < P.n) {
 #pragma unroll
@@ -220,24 +242,24 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh->tmem_empty);
+      if (lane == 0) mbar_arrive(&sh->tmem_empty[buf]);
+      if (nbuf == 2) buf ^= 1;
     }
   } else {
     // ---------------------------------------------------------------- sign-tile generators
     const int gtid = threadIdx.x - 192;
-    int stage = 0;
-    uint32_t phase = 0;
+    Ring gr;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const int split = u / P.tiles;
       const int c0 = split * P.chunks_per_split;
       const int c1 = min(P.nchunks, c0 + P.chunks_per_split);
       for (int c = c0; c < c1; ++c) {
-        if (!wait_or_abort(sh, &sh->empty[stage], phase ^ 1u, limit, ctl)) goto gen_done;
-        gen_sigma_kmajor(b_tiles + size_t(stage) * b_bytes, key, P.r, c, gtid, 128);
+        if (!warp_wait(sh, &sh->o_empty[gr.stage], gr.phase ^ 1u, limit, ctl)) goto gen_done;
+        gen_sigma_kmajor(g_tiles + size_t(gr.stage) * g_bytes, sh->nib, key, P.r, c, gtid, 128);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->gen[stage]);
-        if (++stage == S) { stage = 0; phase ^= 1u; }
+        if (lane == 0) mbar_arrive(&sh->o_full[gr.stage]);
+        gr.next(GS);
       }
     }
   gen_done:;
@@ -292,29 +314,34 @@ __global__ void __launch_bounds__(256) split_kernel(const float* __restrict__ pp
 }
 
 // ============================================================================ accumulate
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
     accumulate_tc_kernel(const __grid_constant__ CUtensorMap tmap_dy, SketchShape sh_, const uint8_t* __restrict__ image,
                          float scale, float* __restrict__ S, Control* ctl) {
   extern __shared__ uint8_t smem_raw[];
   const SketchShape& P = sh_;
   uint8_t* base = align1024(smem_raw);
-  const int NS = P.acc_stages;
+  const int AS = P.a_stages, BS = P.b_stages;
   const int N = P.ntile_n;
   const uint32_t a_bytes = uint32_t(P.r_pad) * 128;
   const uint32_t b_bytes = uint32_t(N) * kChunk * 2;
-  const uint32_t stage_bytes = a_bytes + b_bytes;
-  Shared* sh = reinterpret_cast<Shared*>(base + size_t(NS) * stage_bytes);
+  uint8_t* a_tiles = base;
+  uint8_t* b_tiles = base + size_t(AS) * a_bytes;
+  Shared* sh = reinterpret_cast<Shared*>(b_tiles + size_t(BS) * b_bytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned long long limit = ctl->wait_limit;
   const int mblocks = P.r_pad / 128;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&sh->full[s], 1);
-      mbar_init(&sh->empty[s], 1);
+    for (int s = 0; s < BS; ++s) {
+      mbar_init(&sh->s_full[s], 1);
+      mbar_init(&sh->s_empty[s], 1);
     }
-    mbar_init(&sh->tmem_full, 1);
-    mbar_init(&sh->tmem_empty, 4);
+    for (int s = 0; s < AS; ++s) {
+      mbar_init(&sh->o_full[s], 1);
+      mbar_init(&sh->o_empty[s], 1);
+    }
+    mbar_init(&sh->tmem_full[0], 1);
+    for (int m = 0; m < 4; ++m) mbar_init(&sh->tmem_empty[m], 4);
     mbar_init(&sh->drain, 1);
     sh->abort = 0;
     fence_mbar_init();
@@ -334,75 +361,95 @@ __global__ void __launch_bounds__(192, 1)
   const int nchunks = P.n_pad / kChunk;
 
   if (warp == 0) {
+    // ---------------------------------------------------------------- P^T chunk producer (L2)
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
+      Ring ar;
       int inject = ctl->inject_fault && blockIdx.x == 0;
+      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const int ts = u / P.dtiles;
+        const int c0 = ts * P.tchunks_per_split, c1 = min(nchunks, c0 + P.tchunks_per_split);
+        for (int c = c0; c < c1; ++c) {
+          if (!wait_or_abort(sh, &sh->o_empty[ar.stage], ar.phase ^ 1u, limit, ctl)) goto a_done;
+          if (inject && c == c0 + 1) {
+            inject = 0;
+          } else {
+            mbar_arrive_expect_tx(&sh->o_full[ar.stage], a_bytes);
+            bulk_load(a_tiles + size_t(ar.stage) * a_bytes, image + size_t(c) * a_bytes, a_bytes,
+                      &sh->o_full[ar.stage]);
+          }
+          ar.next(AS);
+        }
+      }
+    a_done:
+      drain_ring(sh->o_full, ar, AS, limit);
+    }
+  } else if (warp == 6) {
+    // ---------------------------------------------------------------- dY tile producer (HBM)
+    if (lane == 0) {
+      Ring br;
       for (int u = blockIdx.x; u < units; u += gridDim.x) {
         const int dt = u % P.dtiles, ts = u / P.dtiles;
         const int c0 = ts * P.tchunks_per_split, c1 = min(nchunks, c0 + P.tchunks_per_split);
         for (int c = c0; c < c1; ++c) {
-          if (!wait_or_abort(sh, &sh->empty[stage], phase ^ 1u, limit, ctl)) goto producer_done;
-          if (inject && c == c0 + 1) {
-            inject = 0;
-          } else {
-            uint8_t* st = base + size_t(stage) * stage_bytes;
-            mbar_arrive_expect_tx(&sh->full[stage], stage_bytes);
-            bulk_load(st, image + size_t(c) * a_bytes, a_bytes, &sh->full[stage]);
-            for (int j = 0; j < N / 64; ++j)
-              tma_load_2d(st + a_bytes + j * (kChunk * 128), &tmap_dy, &sh->full[stage], dt * N + j * 64, c * kChunk);
-          }
-          if (++stage == NS) { stage = 0; phase ^= 1u; }
+          if (!wait_or_abort(sh, &sh->s_empty[br.stage], br.phase ^ 1u, limit, ctl)) goto b_done;
+          uint8_t* st = b_tiles + size_t(br.stage) * b_bytes;
+          mbar_arrive_expect_tx(&sh->s_full[br.stage], b_bytes);
+          for (int j = 0; j < N / 64; ++j)
+            tma_load_2d(st + j * (kChunk * 128), &tmap_dy, &sh->s_full[br.stage], dt * N + j * 64, c * kChunk);
+          br.next(BS);
         }
       }
-    producer_done:
-      for (int s = 0; s < NS; ++s) {
-        const uint32_t ph = (s < stage) ? phase : (phase ^ 1u);
-        mbar_wait(&sh->full[s], ph, limit);
-      }
+    b_done:
+      drain_ring(sh->s_full, br, BS, limit);
     }
   } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0, tphase = 0;
+      Ring ar, br;
+      uint32_t tphase = 0;
       const uint32_t idesc = idesc_bf16(128, uint32_t(N), 0, 1);
       for (int u = blockIdx.x; u < units && !sh->abort; u += gridDim.x) {
         const int ts = u / P.dtiles;
         const int c0 = ts * P.tchunks_per_split, c1 = min(nchunks, c0 + P.tchunks_per_split);
-        if (!wait_or_abort(sh, &sh->tmem_empty, tphase ^ 1u, limit, ctl)) break;
-        tc_fence_after();
-        bool first = true;
         for (int c = c0; c < c1; ++c) {
-          if (!wait_or_abort(sh, &sh->full[stage], phase, limit, ctl)) goto mma_done;
+          if (!wait_or_abort(sh, &sh->o_full[ar.stage], ar.phase, limit, ctl)) goto mma_done;
+          if (!wait_or_abort(sh, &sh->s_full[br.stage], br.phase, limit, ctl)) goto mma_done;
           tc_fence_after();
-          const uint32_t a0 = smem_addr(base + size_t(stage) * stage_bytes);
-          const uint32_t b0 = a0 + a_bytes;
+          const uint32_t a0 = smem_addr(a_tiles + size_t(ar.stage) * a_bytes);
+          const uint32_t b0 = smem_addr(b_tiles + size_t(br.stage) * b_bytes);
 #pragma unroll
           for (int ks = 0; ks < kChunk / 16; ++ks) {
             const uint64_t bd = smem_desc(b0 + ks * 2048, kChunk * 128, 1024, kSw128);
             for (int m = 0; m < mblocks; ++m) {
+              if (c == c0 && ks == 0) {
+                // M block m of the accumulator is free once the epilogue drained it
+                if (!wait_or_abort(sh, &sh->tmem_empty[m], tphase ^ 1u, limit, ctl)) goto mma_done;
+                tc_fence_after();
+              }
               const uint32_t am = a0 + m * (128 * 128) + ks * 32;
-              mma_bf16(tmem + uint32_t(m * N), smem_desc(am, 16, 1024, kSw128), bd, idesc, first ? 0u : 1u);
+              mma_bf16(tmem + uint32_t(m * N), smem_desc(am, 16, 1024, kSw128), bd, idesc, (c == c0 && ks == 0) ? 0u : 1u);
               mma_bf16(tmem + uint32_t(m * N), smem_desc(am + 64, 16, 1024, kSw128), bd, idesc, 1u);
             }
-            first = false;
           }
-          mma_commit(&sh->empty[stage]);
-          if (++stage == NS) { stage = 0; phase ^= 1u; }
+          mma_commit(&sh->o_empty[ar.stage]);
+          mma_commit(&sh->s_empty[br.stage]);
+          ar.next(AS);
+          br.next(BS);
         }
-        mma_commit(&sh->tmem_full);
+        mma_commit(&sh->tmem_full[0]);
         tphase ^= 1u;
       }
     mma_done:
       mma_commit(&sh->drain);
       mbar_wait(&sh->drain, 0, limit);
     }
-  } else {
+  } else if (warp < 6) {
+    // ---------------------------------------------------------------- epilogue: TMEM -> S (fp32 reductions)
     const int quad = warp & 3;
     uint32_t tphase = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const int dt = u % P.dtiles;
-      if (!wait_or_abort(sh, &sh->tmem_full, tphase, limit, ctl)) break;
+      if (!warp_wait(sh, &sh->tmem_full[0], tphase, limit, ctl)) break;
       tphase ^= 1u;
       tc_fence_after();
       for (int m = 0; m < mblocks; ++m) {
@@ -418,10 +465,10 @@ __global__ void __launch_bounds__(192, 1)
               if (d0 + j < P.d) red_add_f32(S + (d0 + j) * P.r + ridx, __uint_as_float(v[j]) * scale);
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->tmem_empty[m]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh->tmem_empty);
     }
   }
 
@@ -436,8 +483,9 @@ __global__ void __launch_bounds__(192, 1)
 // ============================================================================ host side
 static int ceil_div(int64_t a, int64_t b) { return int((a + b - 1) / b); }
 
-// Pick the number of token splits for `tiles` tiles over `sms` SMs: the best
-// fraction of busy SMs in the last wave, each split keeping >= min_chunks chunks.
+// Pick the number of splits of the contraction for `tiles` tiles over `sms`
+// SMs: the best fraction of busy SMs in the last wave, each split keeping at
+// least min_chunks chunks.
 static int pick_splits(int tiles, int sms, int nchunks, int min_chunks, int max_splits) {
   int best = 1;
   double best_eff = -1.0;
@@ -463,7 +511,7 @@ static SketchShape plan(int64_t n, int64_t d, int64_t k, int r, int sms) {
   P.n_pad = ceil_div(n, kChunk) * kChunk;
   P.tiles = ceil_div(n, kTok);
   P.nchunks = ceil_div(k, kKc);
-  P.splits = pick_splits(P.tiles, sms, P.nchunks, 8, 4);
+  P.splits = pick_splits(P.tiles, sms, P.nchunks, 8, 8);
   P.chunks_per_split = ceil_div(P.nchunks, P.splits);
   P.splits = ceil_div(P.nchunks, P.chunks_per_split);
   P.ntile_n = (P.r_pad <= 256) ? 256 : 128;
@@ -472,12 +520,24 @@ static SketchShape plan(int64_t n, int64_t d, int64_t k, int r, int sms) {
   P.tsplits = pick_splits(P.dtiles, sms, tchunks, 8, 16);
   P.tchunks_per_split = ceil_div(tchunks, P.tsplits);
   P.tsplits = ceil_div(tchunks, P.tchunks_per_split);
-  const int budget = 227 * 1024 - 1024 - int(sizeof(Shared)) - 64;
-  P.proj_stages = budget / (kTok * 128 + r * 128);
-  if (P.proj_stages > kMaxStages) P.proj_stages = kMaxStages;
-  P.acc_stages = budget / (P.r_pad * 128 + P.ntile_n * kChunk * 2);
-  if (P.acc_stages > kMaxStages) P.acc_stages = kMaxStages;
+  // project: two sign-tile stages, the rest of shared memory for X tiles
+  P.g_stages = 2;
+  P.x_stages = (kSmemBudget - 2 * r * 128) / (kTok * 128);
+  if (P.x_stages > kMaxStages) P.x_stages = kMaxStages;
+  // accumulate: P^T chunks come from L2 (three stages), dY from HBM (the rest)
+  const int a_bytes = P.r_pad * 128, b_bytes = P.ntile_n * kChunk * 2;
+  P.a_stages = P.r_pad >= 512 ? 2 : 3;
+  P.b_stages = (kSmemBudget - P.a_stages * a_bytes) / b_bytes;
+  if (P.b_stages > kMaxStages) P.b_stages = kMaxStages;
   return P;
+}
+
+static int proj_smem_bytes(const SketchShape& P) {
+  return 1024 + P.x_stages * kTok * 128 + P.g_stages * P.r * 128 + int(sizeof(Shared));
+}
+
+static int acc_smem_bytes(const SketchShape& P) {
+  return 1024 + P.a_stages * P.r_pad * 128 + P.b_stages * P.ntile_n * kChunk * 2 + int(sizeof(Shared));
 }
 
 size_t sketch_tc_workspace_bytes(int64_t n, int64_t d, int64_t k, int r, int sms) {
@@ -503,8 +563,8 @@ int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_
                             64, kChunk, CU_TENSOR_MAP_SWIZZLE_128B))
     return st;
 
-  const int proj_smem = 1024 + P.proj_stages * (kTok * 128 + r * 128) + int(sizeof(Shared)) + 64;
-  LOGRA_CUDA_TRY(cudaFuncSetAttribute(project_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, proj_smem));
+  const int proj_smem = proj_smem_bytes(P);
+  LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(project_tc_kernel), proj_smem));
   const int punits = P.tiles * P.splits;
   project_tc_kernel<<<punits < sms ? punits : sms, 320, proj_smem, s>>>(tx, P, key, ppart, ctl);
   LOGRA_LAUNCHED();
@@ -515,10 +575,10 @@ int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_
   split_kernel<<<sblocks, 256, 0, s>>>(ppart, P, image);
   LOGRA_LAUNCHED();
 
-  const int acc_smem = 1024 + P.acc_stages * (P.r_pad * 128 + P.ntile_n * kChunk * 2) + int(sizeof(Shared)) + 64;
-  LOGRA_CUDA_TRY(cudaFuncSetAttribute(accumulate_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, acc_smem));
+  const int acc_smem = acc_smem_bytes(P);
+  LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(accumulate_tc_kernel), acc_smem));
   const int aunits = P.dtiles * P.tsplits;
-  accumulate_tc_kernel<<<aunits < sms ? aunits : sms, 192, acc_smem, s>>>(tdy, P, image, scale, S, ctl);
+  accumulate_tc_kernel<<<aunits < sms ? aunits : sms, 224, acc_smem, s>>>(tdy, P, image, scale, S, ctl);
   LOGRA_LAUNCHED();
   return LOGRA_OK;
 }

@@ -57,6 +57,38 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
   return true;
 }
 
+// Bounded wait with a CTA-wide abort flag: keeps waiting in slices while no
+// other role has given up; past the limit it records LOGRA_ERR_TIMEOUT and
+// raises the flag so every role leaves its loop.
+template <class SH>
+__device__ __forceinline__ bool wait_or_abort(SH* sh, uint64_t* bar, uint32_t parity, unsigned long long limit,
+                                              Control* ctl) {
+  const unsigned long long slice = limit / 8 + 1;
+  unsigned long long spent = 0;
+  while (!mbar_wait(bar, parity, slice)) {
+    if (*reinterpret_cast<volatile int*>(&sh->abort)) return false;
+    spent += slice;
+    if (spent >= limit) {
+      record_status(ctl, LOGRA_ERR_TIMEOUT);
+      *reinterpret_cast<volatile int*>(&sh->abort) = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+// Warp-uniform version: lane 0 waits, the verdict is broadcast, and every lane
+// then observes the completed phase itself (acquire) before touching the data.
+template <class SH>
+__device__ __forceinline__ bool warp_wait(SH* sh, uint64_t* bar, uint32_t parity, unsigned long long limit,
+                                          Control* ctl) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = wait_or_abort(sh, bar, parity, limit, ctl) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) (void)mbar_try_wait(bar, parity);
+  return ok != 0;
+}
+
 // ----------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

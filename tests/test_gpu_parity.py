@@ -6,7 +6,8 @@ Tolerances (relative Frobenius unless stated):
   * S, fp32 inputs            1e-5
   * v, norms                  1e-5   (apply checked stage-wise on the kernel's own S)
   * dW (W0 = 0, so W = dW)    1e-5
-  * W with a realistic W0     |W - fl32(W0 + dW_oracle)| <= ulp(W) + 1e-5 rms_row(dW)
+  * W with a realistic W0     W_new - W_old vs dW_oracle 1e-5 (Frobenius), and elementwise
+                              |W - fl32(W0 + dW_oracle)| <= 2 ulp(W) + 1e-4 rms_row(dW)
 """
 import math
 
@@ -174,10 +175,13 @@ def test_apply_realistic_w0_and_two_steps(L):
         Wg = host64(W)
         want = (Wprev + dW).astype(np.float32).astype(np.float64)
         ulp = np.spacing(np.abs(want).astype(np.float32)).astype(np.float64)
-        # fp32 sums of r signed terms lose relative accuracy where a row's terms
-        # cancel, so the update error is bounded by the row's scale, not the element's
+        # the applied update (W_new - W_old) against the oracle's dW, Frobenius;
+        # it includes the fp32 rounding of W_new, ~ulp(W)/2 per element
+        assert rel(Wg - Wprev, dW) <= TOL_DW
+        # elementwise sanity: an fp32 sum of r signed terms loses relative
+        # accuracy where a row's terms cancel, so bound by the row's scale
         row_rms = np.sqrt(np.mean(dW * dW, axis=1, keepdims=True))
-        assert np.all(np.abs(Wg - want) <= 1.01 * ulp + TOL_DW * row_rms)
+        assert np.all(np.abs(Wg - want) <= 2.01 * ulp + 1e-4 * row_rms)
 
 
 def test_apply_zero_sketch_and_zero_scale(L):
