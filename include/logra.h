@@ -195,6 +195,36 @@ size_t logra_sketch_workspace_bytes(int64_t n, int64_t d, int64_t k, int r, int 
 size_t logra_apply_workspace_bytes(int64_t d, int64_t k, int r);
 
 /*
+ * logra_sketch_accumulate_noalloc -- logra_sketch_accumulate for bf16 inputs
+ * that never allocates device memory.  (The paper has no counterpart: this is
+ * a deployment variant of the same operation, same arguments minus the dtype.)
+ *
+ * Meant for callers that are not allowed to call cudaMalloc: frameworks
+ * whose caching allocator owns all device memory and forbids side
+ * allocations, latency-critical loops that must not block in the driver,
+ * and runtimes whose device memory is fixed at start-up.
+ *
+ * Scratch: instead of the per-stream workspace, the call uses one fixed
+ * device array compiled into the library (logra_noalloc_scratch_bytes()
+ * bytes, 32 MiB), which every GPU that loads the library holds until the
+ * process exits.  A shape whose scratch need
+ * (logra_sketch_workspace_bytes(n, d, k, r, LOGRA_BF16)) exceeds it returns
+ * LOGRA_ERR_UNSUPPORTED and launches nothing.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) and caches it;
+ * make that first call before any stream capture.  All calls, on every
+ * stream of a device, share the one array and the array keeps the last
+ * call's contents (the kernels overwrite every byte they read): calls whose
+ * execution overlaps on the GPU race and corrupt each other's results, so
+ * order them (one stream, or events).  S, X and dY rules as for
+ * logra_sketch_accumulate.
+ */
+int logra_sketch_accumulate_noalloc(const void* X, const void* dY, int64_t n, int64_t d, int64_t k, int r,
+                                    uint64_t seed, uint64_t step, float* S, logra_stream_t stream);
+
+/* Size in bytes of the fixed scratch array used by logra_sketch_accumulate_noalloc. */
+size_t logra_noalloc_scratch_bytes(void);
+
+/*
  * logra_debug_inject -- TEST ONLY.  fault = 1 makes the next pipelined kernel
  * launch drop one producer arrival, so that its consumer's bounded wait runs
  * out and the kernel records LOGRA_ERR_TIMEOUT and exits cleanly (no trap, no

@@ -35,6 +35,8 @@ SIGNATURES = {
     "logra_sketch_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I, _I]),
     "logra_apply_workspace_bytes": (_SZ, [_I64, _I64, _I]),
     "logra_debug_inject": (_I, [_I, _U64]),
+    "logra_sketch_accumulate_noalloc": (_I, [_VP, _VP, _I64, _I64, _I64, _I, _U64, _U64, _VP, _VP]),
+    "logra_noalloc_scratch_bytes": (_SZ, []),
 }
 
 _lib = None
