@@ -1,28 +1,36 @@
-// Tensor-core reconstruct-and-update (tcgen05 + TMEM + TMA):
+// Tensor-core reconstruct-and-update (tcgen05 + TMEM + TMA), and the row norms
+// that RowAdam needs before it.
 //
 //   for each 128-row block of W and each 256-column super-tile:
 //     D[128 x 256] = S_rows (hi + lo bf16, two MMAs) * Sigma[:, cols]   (TMEM)
 //   epilogue, 32 columns at a time, thread = row:
 //     apply    W_ij += f_i D_ij  with f_i = -lr c / (sqrt(r) sqrt(v_i + eps)),
-//              optional bf16 copy of W, sum of (f_i D_ij)^2 per row
+//              optional bf16 copy of W, sum of (f_i D_ij)^2
 //     predict  only the sum of squares
 //     rebuild  out_ij (+)= D_ij / sqrt(r)   (fp32 or bf16 output)
+//   row norms (mode 4): D = S_rows * M with M = Sigma Sigma^T (exact integers,
+//     split hi + lo), q_i = sum_b D_ib S_ib = r ||(S A)_i||^2, then
+//     v_i <- beta2 v_i + (1 - beta2) q_i / (r k), 1/sqrt(v_i + eps), the
+//     optional sync sketch and ||S||^2 partials.
 //
 // Ghat = S A is formed tile by tile and consumed in the same kernel, so the
 // d x k reconstruction never reaches memory (theclarity.today write-up, "Why
 // it matters": the full-size estimate exists only when the update is
-// applied).  RowAdam's per-row statistic v has been updated beforehand from
-// the exact row norms ||(S A)_i||^2 = S_i Sigma Sigma^T S_i^T / r.
+// applied).  RowAdam keeps one squared-row-magnitude statistic per row and no
+// first moment (same write-up, "What happened"); mode 4 updates it from the
+// exact row norms before the update pass uses it.
 //
 // Operands: A = the row block of S, pre-split into bf16 hi/lo and pre-swizzled
 // (one bulk copy per 64-wide rank chunk); B = Sigma rows of that chunk for the
 // super-tile's 256 columns, MN-major, generated in shared memory from the sign
-// hash.  W (and its bf16 copy) move by TMA in 128 x 32 sub-tiles.
+// hash (mode 4: the M image by bulk copy).  W (and its bf16 copy) move by TMA
+// in 128 x 32 sub-tiles; one store group stays in flight while the next
+// sub-tile is computed.
 //
-// Roles: warp 0 = A producer, warp 1 = TMEM owner + MMA issuer, warps 2..5 =
-// epilogue (TMEM lane quadrant = warp % 4), warps 6..9 = sign-tile generators,
-// warp 10 = W tile producer.  TMEM holds two 256-column accumulators so the
-// epilogue of one super-tile overlaps the MMAs of the next.
+// Roles: warp 0 = A (and mode-4 B) producer, warp 1 = TMEM owner + MMA issuer,
+// warps 2..5 = epilogue (TMEM lane quadrant = warp % 4), warps 6..9 = sign-tile
+// generators, warp 10 = W tile producer.  TMEM holds two 256-column
+// accumulators so the epilogue of one super-tile overlaps the MMAs of the next.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -40,7 +48,7 @@ constexpr int kCols = 256;        // MMA N: columns per super-tile
 constexpr int kRc = 64;           // ranks per K chunk
 constexpr int kSub = 32;          // epilogue sub-tile width (columns)
 constexpr int kAbStages = 2;
-constexpr int kWStages = 3;
+constexpr int kWStages = 4;
 constexpr uint32_t kABytes = 2 * kRows * 128;   // hi + lo: 32 KB
 constexpr uint32_t kBBytes = kRc * kCols * 2;   // 64 ranks x 256 columns bf16: 32 KB
 constexpr uint32_t kWBytes = kRows * kSub * 4;  // fp32 sub-tile: 16 KB
@@ -56,13 +64,12 @@ struct ApplyShared {
   double red[4];
 };
 
-constexpr size_t kApplySmem = 1024 + kAbStages * (kABytes + kBBytes) + kWStages * kWBytes + kHBytes +
+constexpr size_t kApplySmem = 1024 + kAbStages * (kABytes + kBBytes) + kWStages * kWBytes + 2 * kHBytes +
                               sizeof(ApplyShared) + 64;
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
-
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -80,24 +87,37 @@ __device__ __forceinline__ bool group_wait(ApplyShared* sh, uint64_t* bar, uint3
   return ok != 0;
 }
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  return uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
+         (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
+}
+
 }  // namespace
 
 struct ApplyArgs {
   int64_t d, k;
   int r;
-  int nsuper;                 // column super-tiles per row block
-  int units;                  // row blocks x super-tiles
+  int nsuper;                 // super-tiles per row block (columns of W; mode 4: of M)
+  int units;                  // modes 0-3: row blocks x super-tiles; mode 4: row blocks
+  int inner;                  // super-tiles per unit: 1, or nsuper in mode 4
+  int nck;                    // 64-rank chunks
   uint64_t key;
   float neg_lrc_scale;        // -lr c / sqrt(r)   (apply, predict)
   float scale;                // 1 / sqrt(r)       (rebuild)
+  float neg_lrc;              // -lr c             (mode 4 sync sketch)
+  float beta2, eps;
   int accumulate;             // rebuild: add into the output
   int write_bf16;             // apply: also store the bf16 copy
   const uint8_t* s_image;     // [row block][rank chunk][hi | lo][128 rows][128 B]
-  const float* inv_den;       // d values 1/sqrt(v_i + eps)
-  double* dw2_part;           // one per CTA
+  const uint8_t* m_image;     // [super-tile][rank chunk][hi, lo][32 KB]
+  const float* S;
+  const float* v_in;
+  float* v_out;
+  float* inv;                 // d values 1/sqrt(v_i + eps)
+  float* sync_out;
+  double* part;               // one per CTA
 };
 
-// MODE 0 apply, 1 predict, 2 rebuild fp32, 3 rebuild bf16.
 template <int MODE>
 __global__ void __launch_bounds__(352, 1)
     apply_tc_kernel(const __grid_constant__ CUtensorMap tmap_f32, const __grid_constant__ CUtensorMap tmap_b16,
@@ -106,13 +126,13 @@ __global__ void __launch_bounds__(352, 1)
   uint8_t* base = align1024(smem_raw);
   uint8_t* ab = base;                                              // [stage][A 32 KB | B 32 KB]
   uint8_t* wr = ab + kAbStages * (kABytes + kBBytes);              // [stage][16 KB]
-  uint8_t* hb = wr + kWStages * kWBytes;                           // 8 KB bf16 staging
-  ApplyShared* sh = reinterpret_cast<ApplyShared*>(hb + kHBytes);
+  uint8_t* hb = wr + kWStages * kWBytes;                           // 2 x 8 KB bf16 staging
+  ApplyShared* sh = reinterpret_cast<ApplyShared*>(hb + 2 * kHBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned long long limit = ctl->wait_limit;
-  const int nchunks = A.r / kRc + ((A.r % kRc) ? 1 : 0);
-  constexpr bool kLoadIn = (MODE == 0);
-  const bool load_in = kLoadIn || ((MODE == 2 || MODE == 3) && A.accumulate);
+  constexpr bool kNorm = (MODE == 4);
+  const int nchunks = kNorm ? 2 * A.nck : A.nck;      // mode 4: M_hi chunks, then M_lo chunks
+  const bool load_in = (MODE == 0) || ((MODE == 2 || MODE == 3) && A.accumulate);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAbStages; ++s) {
@@ -144,23 +164,32 @@ __global__ void __launch_bounds__(352, 1)
   const uint32_t tmem = sh->tmem_base;
 
   if (warp == 0) {
-    // ------------------------------------------------------------------ A producer (S hi/lo chunks)
+    // ------------------------------------------------------------------ A producer (S hi/lo chunks; mode 4: + M)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int inject = ctl->inject_fault && blockIdx.x == 0;
       for (int u = blockIdx.x; u < A.units; u += gridDim.x) {
-        const int rb = u / A.nsuper;
-        for (int c = 0; c < nchunks; ++c) {
-          if (!wait_or_abort(sh, &sh->ab_empty[stage], phase ^ 1u, limit, ctl)) goto a_done;
-          if (inject && c == 0) {
-            inject = 0;
-          } else {
-            mbar_arrive_expect_tx(&sh->ab_full[stage], kABytes);
-            bulk_load(ab + stage * (kABytes + kBBytes), A.s_image + (size_t(rb) * nchunks + c) * kABytes, kABytes,
-                      &sh->ab_full[stage]);
+        for (int t = 0; t < A.inner; ++t) {
+          const int rb = kNorm ? u : u / A.nsuper;
+          const int st = kNorm ? t : u % A.nsuper;
+          for (int cc = 0; cc < nchunks; ++cc) {
+            const int c = kNorm ? cc % A.nck : cc;
+            if (!wait_or_abort(sh, &sh->ab_empty[stage], phase ^ 1u, limit, ctl)) goto a_done;
+            uint8_t* dst = ab + stage * (kABytes + kBBytes);
+            if (inject && cc == 0) {
+              inject = 0;
+            } else {
+              mbar_arrive_expect_tx(&sh->ab_full[stage], kNorm ? kABytes + kBBytes : kABytes);
+              bulk_load(dst, A.s_image + (size_t(rb) * A.nck + c) * kABytes, kABytes, &sh->ab_full[stage]);
+              if (kNorm) {
+                const int term = cc / A.nck;
+                bulk_load(dst + kABytes, A.m_image + ((size_t(st) * A.nck + c) * 2 + term) * kBBytes, kBBytes,
+                          &sh->ab_full[stage]);
+              }
+            }
+            if (++stage == kAbStages) { stage = 0; phase ^= 1u; }
           }
-          if (++stage == kAbStages) { stage = 0; phase ^= 1u; }
         }
       }
     a_done:
@@ -196,27 +225,30 @@ __global__ void __launch_bounds__(352, 1)
       int buf = 0;
       const uint32_t idesc = idesc_bf16(kRows, kCols, 0, 1);
       for (int u = blockIdx.x; u < A.units && !sh->abort; u += gridDim.x) {
-        if (!wait_or_abort(sh, &sh->tmem_empty[buf], tph[buf] ^ 1u, limit, ctl)) break;
-        tc_fence_after();
-        const uint32_t dt = tmem + uint32_t(buf * kCols);
-        for (int c = 0; c < nchunks; ++c) {
-          if (!wait_or_abort(sh, &sh->ab_full[stage], phase, limit, ctl)) goto mma_done;
-          if (!wait_or_abort(sh, &sh->gen_full[stage], phase, limit, ctl)) goto mma_done;
+        for (int t = 0; t < A.inner; ++t) {
+          if (!wait_or_abort(sh, &sh->tmem_empty[buf], tph[buf] ^ 1u, limit, ctl)) goto mma_done;
           tc_fence_after();
-          const uint32_t a0 = smem_addr(ab + stage * (kABytes + kBBytes));
-          const uint32_t b0 = a0 + kABytes;
-          const int ksteps = min(kRc, A.r - c * kRc) / 16;
-          for (int ks = 0; ks < ksteps; ++ks) {
-            const uint64_t bd = smem_desc(b0 + ks * 2048, kRc * 128, 1024, kSw128);
-            mma_bf16(dt, smem_desc(a0 + ks * 32, 16, 1024, kSw128), bd, idesc, (c | ks) ? 1u : 0u);
-            mma_bf16(dt, smem_desc(a0 + kRows * 128 + ks * 32, 16, 1024, kSw128), bd, idesc, 1u);
+          const uint32_t dt = tmem + uint32_t(buf * kCols);
+          for (int cc = 0; cc < nchunks; ++cc) {
+            const int c = kNorm ? cc % A.nck : cc;
+            if (!wait_or_abort(sh, &sh->ab_full[stage], phase, limit, ctl)) goto mma_done;
+            if (!kNorm && !wait_or_abort(sh, &sh->gen_full[stage], phase, limit, ctl)) goto mma_done;
+            tc_fence_after();
+            const uint32_t a0 = smem_addr(ab + stage * (kABytes + kBBytes));
+            const uint32_t b0 = a0 + kABytes;
+            const int ksteps = min(kRc, A.r - c * kRc) / 16;
+            for (int ks = 0; ks < ksteps; ++ks) {
+              const uint64_t bd = smem_desc(b0 + ks * 2048, kRc * 128, 1024, kSw128);
+              mma_bf16(dt, smem_desc(a0 + ks * 32, 16, 1024, kSw128), bd, idesc, (cc | ks) ? 1u : 0u);
+              mma_bf16(dt, smem_desc(a0 + kRows * 128 + ks * 32, 16, 1024, kSw128), bd, idesc, 1u);
+            }
+            mma_commit(&sh->ab_empty[stage]);
+            if (++stage == kAbStages) { stage = 0; phase ^= 1u; }
           }
-          mma_commit(&sh->ab_empty[stage]);
-          if (++stage == kAbStages) { stage = 0; phase ^= 1u; }
+          mma_commit(&sh->tmem_full[buf]);
+          tph[buf] ^= 1u;
+          buf ^= 1;
         }
-        mma_commit(&sh->tmem_full[buf]);
-        tph[buf] ^= 1u;
-        buf ^= 1;
       }
     mma_done:
       mma_commit(&sh->drain);
@@ -229,147 +261,189 @@ __global__ void __launch_bounds__(352, 1)
     const int et = threadIdx.x - 64;                     // 0..127
     uint32_t tph[2] = {0, 0};
     int buf = 0;
-    int wstage = 0;
+    int wstage = 0, prev_stage = -1, sub = 0;
     uint32_t wphase = 0;
-    double dw2 = 0.0;
-    for (int u = blockIdx.x; u < A.units; u += gridDim.x) {
-      const int rb = u / A.nsuper, st = u % A.nsuper;
-      if (!group_wait(sh, &sh->tmem_full[buf], tph[buf], limit, ctl, et)) break;
-      tph[buf] ^= 1u;
-      tc_fence_after();
+    double acc_cta = 0.0;                                // dW^2 (modes 0, 1) or ||S||^2 (mode 4)
+    bool aborted = false;
+    for (int u = blockIdx.x; u < A.units && !aborted; u += gridDim.x) {
+      const int rb = kNorm ? u : u / A.nsuper;
       const int64_t row = int64_t(rb) * kRows + row_l;
       const bool row_ok = row < A.d;
-      float f = 0.f;
-      if (MODE == 0 || MODE == 1) f = row_ok ? A.neg_lrc_scale * A.inv_den[row] : 0.f;
-      else f = A.scale;
-      bool aborted = false;
-      for (int s = 0; s < kCols / kSub; ++s) {
-        const int64_t col0 = int64_t(st) * kCols + s * kSub;
-        if (col0 >= A.k) break;
-        uint32_t g[32];
-        tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + uint32_t(buf * kCols + s * kSub), g);
-        tmem_ld_wait();
-        const int ncol = int(A.k - col0 < kSub ? A.k - col0 : kSub);
-        if (MODE == 1) {
-          float acc = 0.f;
-          if (row_ok) {
+      double q = 0.0;                                    // mode 4: S_i M S_i^T over the row
+      for (int t = 0; t < A.inner && !aborted; ++t) {
+        const int st = kNorm ? t : u % A.nsuper;
+        if (!group_wait(sh, &sh->tmem_full[buf], tph[buf], limit, ctl, et)) { aborted = true; break; }
+        tph[buf] ^= 1u;
+        tc_fence_after();
+        float f = 0.f;
+        if (MODE == 0 || MODE == 1) f = row_ok ? A.neg_lrc_scale * A.inv[row] : 0.f;
+        else f = A.scale;
+        const int64_t ncols_total = kNorm ? int64_t(A.r) : A.k;
+        for (int s = 0; s < kCols / kSub; ++s) {
+          const int64_t col0 = int64_t(st) * kCols + s * kSub;
+          if (col0 >= ncols_total) break;
+          uint32_t g[32];
+          tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + uint32_t(buf * kCols + s * kSub), g);
+          tmem_ld_wait();
+          const int ncol = int(ncols_total - col0 < kSub ? ncols_total - col0 : kSub);
+          if (MODE == 4) {
+            if (row_ok) {
+              const float4* sp = reinterpret_cast<const float4*>(A.S + row * A.r + col0);
+              float dot = 0.f, ss = 0.f;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float dw = f * __uint_as_float(g[j]);
-              if (j < ncol) acc = fmaf(dw, dw, acc);
+              for (int q4 = 0; q4 < 8; ++q4) {
+                const float4 sv = sp[q4];
+                dot = fmaf(__uint_as_float(g[4 * q4 + 0]), sv.x, dot);
+                dot = fmaf(__uint_as_float(g[4 * q4 + 1]), sv.y, dot);
+                dot = fmaf(__uint_as_float(g[4 * q4 + 2]), sv.z, dot);
+                dot = fmaf(__uint_as_float(g[4 * q4 + 3]), sv.w, dot);
+                ss = fmaf(sv.x, sv.x, fmaf(sv.y, sv.y, fmaf(sv.z, sv.z, fmaf(sv.w, sv.w, ss))));
+              }
+              q += double(dot);
+              acc_cta += double(ss);
+            }
+            continue;
+          }
+          if (MODE == 1) {
+            float acc = 0.f;
+            if (row_ok) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float dw = f * __uint_as_float(g[j]);
+                if (j < ncol) acc = fmaf(dw, dw, acc);
+              }
+            }
+            acc_cta += double(acc);
+            continue;
+          }
+          uint8_t* wt = wr + wstage * kWBytes;
+          uint8_t* ht = hb + (sub & 1) * kHBytes;
+          if (load_in) {
+            if (!group_wait(sh, &sh->w_full[wstage], wphase, limit, ctl, et)) { aborted = true; break; }
+          }
+          if (MODE == 0 || MODE == 2) {
+            // fp32 sub-tile, 128-byte rows, 16-byte chunk q at q ^ (row & 7)
+            float acc = 0.f;
+            uint8_t* rowp = wt + row_l * 128;
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+              float4* p = reinterpret_cast<float4*>(rowp + ((q4 ^ (row_l & 7)) << 4));
+              float4 w = load_in ? *p : make_float4(0.f, 0.f, 0.f, 0.f);
+              const float d0 = f * __uint_as_float(g[4 * q4 + 0]), d1 = f * __uint_as_float(g[4 * q4 + 1]);
+              const float d2 = f * __uint_as_float(g[4 * q4 + 2]), d3 = f * __uint_as_float(g[4 * q4 + 3]);
+              if (MODE == 0) {
+                if (4 * q4 + 0 < ncol) acc = fmaf(d0, d0, acc);
+                if (4 * q4 + 1 < ncol) acc = fmaf(d1, d1, acc);
+                if (4 * q4 + 2 < ncol) acc = fmaf(d2, d2, acc);
+                if (4 * q4 + 3 < ncol) acc = fmaf(d3, d3, acc);
+              }
+              w.x += d0; w.y += d1; w.z += d2; w.w += d3;
+              *p = w;
+              if (MODE == 0 && A.write_bf16) {
+                // bf16 staging: 64-byte rows, 16-byte chunk h at h ^ ((row >> 1) & 3)
+                const int h = q4 >> 1;
+                *reinterpret_cast<uint2*>(ht + row_l * 64 + ((h ^ ((row_l >> 1) & 3)) << 4) + (q4 & 1) * 8) =
+                    make_uint2(pack_bf16x2(w.x, w.y), pack_bf16x2(w.z, w.w));
+              }
+            }
+            if (MODE == 0 && row_ok) acc_cta += double(acc);
+          } else {
+            // MODE 3: bf16 output sub-tile (64-byte rows) in the staging buffer
+            const uint8_t* src = wt + row_l * 64;
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const int off = (h ^ ((row_l >> 1) & 3)) << 4;
+              uint4 in = load_in ? *reinterpret_cast<const uint4*>(src + off) : make_uint4(0, 0, 0, 0);
+              const uint32_t iw[4] = {in.x, in.y, in.z, in.w};
+              uint32_t ow[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float lo = __uint_as_float(iw[e] << 16) + f * __uint_as_float(g[8 * h + 2 * e]);
+                const float hi = __uint_as_float(iw[e] & 0xFFFF0000u) + f * __uint_as_float(g[8 * h + 2 * e + 1]);
+                ow[e] = pack_bf16x2(lo, hi);
+              }
+              *reinterpret_cast<uint4*>(ht + row_l * 64 + off) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
             }
           }
-          dw2 += double(acc);
-          continue;
-        }
-        uint8_t* wt = wr + wstage * kWBytes;
-        if (load_in) {
-          if (!group_wait(sh, &sh->w_full[wstage], wphase, limit, ctl, et)) { aborted = true; break; }
-        }
-        if (MODE == 0 || MODE == 2) {
-          // fp32 sub-tile, 128-byte rows, 16-byte chunk q at q ^ (row & 7)
-          float acc = 0.f;
-          uint8_t* rowp = wt + row_l * 128;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            float4* p = reinterpret_cast<float4*>(rowp + ((q ^ (row_l & 7)) << 4));
-            float4 w = load_in ? *p : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float d0 = f * __uint_as_float(g[4 * q + 0]), d1 = f * __uint_as_float(g[4 * q + 1]);
-            const float d2 = f * __uint_as_float(g[4 * q + 2]), d3 = f * __uint_as_float(g[4 * q + 3]);
-            if (MODE == 0) {
-              if (4 * q + 0 < ncol) acc = fmaf(d0, d0, acc);
-              if (4 * q + 1 < ncol) acc = fmaf(d1, d1, acc);
-              if (4 * q + 2 < ncol) acc = fmaf(d2, d2, acc);
-              if (4 * q + 3 < ncol) acc = fmaf(d3, d3, acc);
-            }
-            w.x += d0; w.y += d1; w.z += d2; w.w += d3;
-            *p = w;
-            if (MODE == 0 && A.write_bf16) {
-              // bf16 staging: 64-byte rows, 16-byte chunk h at h ^ ((row >> 1) & 3)
-              const int h = q >> 1;
-              uint2 packed;
-              packed.x = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(w.x))) |
-                         (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(w.y))) << 16);
-              packed.y = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(w.z))) |
-                         (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(w.w))) << 16);
-              *reinterpret_cast<uint2*>(hb + row_l * 64 + ((h ^ ((row_l >> 1) & 3)) << 4) + (q & 1) * 8) = packed;
-            }
+          fence_proxy_async_smem();
+          epi_sync();
+          if (et == 0) {
+            if (MODE == 0 || MODE == 2) tma_store_2d(&tmap_f32, wt, int32_t(col0), rb * kRows);
+            if ((MODE == 0 && A.write_bf16) || MODE == 3) tma_store_2d(&tmap_b16, ht, int32_t(col0), rb * kRows);
+            bulk_commit();
+            // keep this sub-tile's stores in flight; once at most one group is
+            // outstanding, the previous sub-tile's stores have read their smem
+            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+            if (load_in && prev_stage >= 0) mbar_arrive(&sh->w_empty[prev_stage]);
           }
-          if (MODE == 0 && row_ok) dw2 += double(acc);
-        } else {
-          // MODE 3: bf16 output sub-tile (64-byte rows) in the staging buffer
-          const uint8_t* src = wt + row_l * 64;
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const int off = (h ^ ((row_l >> 1) & 3)) << 4;
-            uint4 in = load_in ? *reinterpret_cast<const uint4*>(src + off) : make_uint4(0, 0, 0, 0);
-            const uint32_t iw[4] = {in.x, in.y, in.z, in.w};
-            uint32_t ow[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float lo = __uint_as_float(iw[e] << 16) + f * __uint_as_float(g[8 * h + 2 * e]);
-              const float hi = __uint_as_float(iw[e] & 0xFFFF0000u) + f * __uint_as_float(g[8 * h + 2 * e + 1]);
-              ow[e] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
-                      (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
-            }
-            *reinterpret_cast<uint4*>(hb + row_l * 64 + off) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+          epi_sync();
+          prev_stage = load_in ? wstage : -1;
+          ++sub;
+          if (load_in || MODE == 2) {
+            if (++wstage == kWStages) { wstage = 0; wphase ^= 1u; }
           }
         }
-        fence_proxy_async_smem();
-        epi_sync();
-        if (et == 0) {
-          if (MODE == 0 || MODE == 2) tma_store_2d(&tmap_f32, wt, int32_t(col0), rb * kRows);
-          if ((MODE == 0 && A.write_bf16) || MODE == 3) tma_store_2d(&tmap_b16, hb, int32_t(col0), rb * kRows);
-          bulk_commit();
-          bulk_wait_read_all();
-          if (load_in) mbar_arrive(&sh->w_empty[wstage]);
-        }
-        epi_sync();
-        if (load_in) {
-          if (++wstage == kWStages) { wstage = 0; wphase ^= 1u; }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->tmem_empty[buf]);
+        buf ^= 1;
+      }
+      if (MODE == 4 && !aborted && row_ok) {
+        const float mean_sq = float(q) / (float(A.r) * float(A.k));
+        const float vn = A.beta2 * A.v_in[row] + (1.f - A.beta2) * mean_sq;
+        if (A.v_out) A.v_out[row] = vn;
+        const float inv = 1.f / sqrtf(vn + A.eps);
+        A.inv[row] = inv;
+        if (A.sync_out) {
+          const float fs = A.neg_lrc * inv;
+          const float4* sp = reinterpret_cast<const float4*>(A.S + row * A.r);
+          float4* op = reinterpret_cast<float4*>(A.sync_out + row * A.r);
+          for (int b = 0; b < A.r / 4; ++b) {
+            const float4 sv = sp[b];
+            op[b] = make_float4(fs * sv.x, fs * sv.y, fs * sv.z, fs * sv.w);
+          }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh->tmem_empty[buf]);
-      buf ^= 1;
-      if (aborted) break;
     }
-    if (et == 0) bulk_wait_all();
-    if (MODE == 0 || MODE == 1) {
-      // per-CTA sum of dW^2 over this CTA's rows and columns, fixed order
-      for (int o = 16; o; o >>= 1) dw2 += __shfl_xor_sync(0xffffffffu, dw2, o);
-      if (lane == 0) sh->red[quad] = dw2;
-      epi_sync();
-      if (et == 0) A.dw2_part[blockIdx.x] = sh->red[0] + sh->red[1] + sh->red[2] + sh->red[3];
+    if (et == 0) {
+      bulk_wait_all();
+      if (load_in && prev_stage >= 0 && !aborted) mbar_arrive(&sh->w_empty[prev_stage]);
     }
+    // per-CTA partial sum, fixed order
+    for (int o = 16; o; o >>= 1) acc_cta += __shfl_xor_sync(0xffffffffu, acc_cta, o);
+    if (lane == 0) sh->red[quad] = acc_cta;
+    epi_sync();
+    if (et == 0 && (MODE == 0 || MODE == 1 || MODE == 4))
+      A.part[blockIdx.x] = sh->red[0] + sh->red[1] + sh->red[2] + sh->red[3];
   } else if (warp < 10) {
     // ------------------------------------------------------------------ sign-tile generators (MN-major)
-    const int gtid = threadIdx.x - 192;
-    int stage = 0;
-    uint32_t phase = 0;
-    for (int u = blockIdx.x; u < A.units; u += gridDim.x) {
-      const int st = u % A.nsuper;
-      for (int c = 0; c < nchunks; ++c) {
-        if (!warp_wait(sh, &sh->ab_empty[stage], phase ^ 1u, limit, ctl)) goto gen_done;
-        uint8_t* bt = ab + stage * (kABytes + kBBytes) + kABytes;
-        // 4 groups of 64 columns x 64 rank rows; row = one sign word (64 columns)
-        for (int e = gtid; e < 4 * kRc; e += 128) {
-          const int grp = e / kRc, a_l = e % kRc;
-          const int a = c * kRc + a_l;
-          const uint64_t w = a < A.r ? sign_word(A.key, uint32_t(a), uint32_t(st * (kCols / 64) + grp)) : 0ull;
-          uint8_t* rowp = bt + grp * (kRc * 128) + a_l * 128;
+    if (!kNorm) {
+      const int gtid = threadIdx.x - 192;
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int u = blockIdx.x; u < A.units; u += gridDim.x) {
+        const int st = u % A.nsuper;
+        for (int c = 0; c < nchunks; ++c) {
+          if (!warp_wait(sh, &sh->ab_empty[stage], phase ^ 1u, limit, ctl)) goto gen_done;
+          uint8_t* bt = ab + stage * (kABytes + kBBytes) + kABytes;
+          // 4 groups of 64 columns x 64 rank rows; row = one sign word (64 columns)
+          for (int e = gtid; e < 4 * kRc; e += 128) {
+            const int grp = e / kRc, a_l = e % kRc;
+            const int a = c * kRc + a_l;
+            const uint64_t w = a < A.r ? sign_word(A.key, uint32_t(a), uint32_t(st * (kCols / 64) + grp)) : 0ull;
+            uint8_t* rowp = bt + grp * (kRc * 128) + a_l * 128;
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<uint4*>(rowp + ((q ^ (a_l & 7)) << 4)) = signs8_to_bf16(uint32_t(w >> (8 * q)) & 0xFFu);
+            for (int q = 0; q < 8; ++q)
+              *reinterpret_cast<uint4*>(rowp + ((q ^ (a_l & 7)) << 4)) = signs8_to_bf16(uint32_t(w >> (8 * q)) & 0xFFu);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh->gen_full[stage]);
+          if (++stage == kAbStages) { stage = 0; phase ^= 1u; }
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->gen_full[stage]);
-        if (++stage == kAbStages) { stage = 0; phase ^= 1u; }
       }
+    gen_done:;
     }
-  gen_done:;
   }
 
   tc_fence_before();
@@ -430,34 +504,49 @@ int launch_s_image(const float* S, int64_t d, int r, uint8_t* img, cudaStream_t 
   return LOGRA_OK;
 }
 
-int launch_apply_tc(int mode, float* W, __nv_bfloat16* Wb, void* out, int accumulate, int64_t d, int64_t k, int r,
-                    uint64_t key, float neg_lrc, const uint8_t* s_img, const float* inv_den, double* dw2_part,
-                    int* grid_out, Control* ctl, cudaStream_t s) {
+int launch_apply_tc(const ApplyLaunch& L, int* grid_out, Control* ctl, cudaStream_t s) {
   const int sms = sm_count();
+  const int mode = L.mode;
   ApplyArgs A{};
-  A.d = d; A.k = k; A.r = r;
-  A.nsuper = int((k + kCols - 1) / kCols);
-  const int64_t rbs = (d + kRows - 1) / kRows;
-  A.units = int(rbs * A.nsuper);
-  A.key = key;
-  A.scale = inv_sqrt_r(r);
-  A.neg_lrc_scale = neg_lrc * A.scale;
-  A.accumulate = accumulate;
-  A.write_bf16 = (mode == 0 && Wb) ? 1 : 0;
-  A.s_image = s_img;
-  A.inv_den = inv_den;
-  A.dw2_part = dw2_part;
+  A.d = L.d; A.k = L.k; A.r = L.r;
+  A.nck = (L.r + kRc - 1) / kRc;
+  const int64_t rbs = (L.d + kRows - 1) / kRows;
+  if (mode == 4) {
+    A.nsuper = (L.r + kCols - 1) / kCols;
+    A.units = int(rbs);
+    A.inner = A.nsuper;
+  } else {
+    A.nsuper = int((L.k + kCols - 1) / kCols);
+    A.units = int(rbs * A.nsuper);
+    A.inner = 1;
+  }
+  A.key = L.key;
+  A.scale = inv_sqrt_r(L.r);
+  A.neg_lrc_scale = L.neg_lrc * A.scale;
+  A.neg_lrc = L.neg_lrc;
+  A.beta2 = L.beta2;
+  A.eps = L.eps;
+  A.accumulate = L.accumulate;
+  A.write_bf16 = (mode == 0 && L.Wb) ? 1 : 0;
+  A.s_image = L.s_img;
+  A.m_image = L.m_img;
+  A.S = L.S;
+  A.v_in = L.v_in;
+  A.v_out = L.v_out;
+  A.inv = L.inv;
+  A.sync_out = L.sync_out;
+  A.part = L.part;
   CUtensorMap t32{}, t16{};
   if (mode == 0 || mode == 2) {
-    const void* p = mode == 0 ? static_cast<const void*>(W) : out;
-    if (int st = make_tmap_2d(&t32, p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(k), uint64_t(d), uint64_t(k) * 4,
-                              kSub, kRows, CU_TENSOR_MAP_SWIZZLE_128B))
+    const void* p = mode == 0 ? static_cast<const void*>(L.W) : L.out;
+    if (int st = make_tmap_2d(&t32, p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(L.k), uint64_t(L.d),
+                              uint64_t(L.k) * 4, kSub, kRows, CU_TENSOR_MAP_SWIZZLE_128B))
       return st;
   }
-  if ((mode == 0 && Wb) || mode == 3) {
-    const void* p = mode == 0 ? static_cast<const void*>(Wb) : out;
-    if (int st = make_tmap_2d(&t16, p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, uint64_t(k), uint64_t(d),
-                              uint64_t(k) * 2, kSub, kRows, CU_TENSOR_MAP_SWIZZLE_64B))
+  if ((mode == 0 && L.Wb) || mode == 3) {
+    const void* p = mode == 0 ? static_cast<const void*>(L.Wb) : L.out;
+    if (int st = make_tmap_2d(&t16, p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, uint64_t(L.k), uint64_t(L.d),
+                              uint64_t(L.k) * 2, kSub, kRows, CU_TENSOR_MAP_SWIZZLE_64B))
       return st;
   }
   const int grid = A.units < sms ? A.units : sms;
@@ -472,7 +561,8 @@ int launch_apply_tc(int mode, float* W, __nv_bfloat16* Wb, void* out, int accumu
     case 0: return run(apply_tc_kernel<0>);
     case 1: return run(apply_tc_kernel<1>);
     case 2: return run(apply_tc_kernel<2>);
-    default: return run(apply_tc_kernel<3>);
+    case 3: return run(apply_tc_kernel<3>);
+    default: return run(apply_tc_kernel<4>);
   }
 }
 

@@ -11,14 +11,14 @@ namespace logra {
 struct Control;
 
 struct ApplyWorkspace {
-  size_t words_off, gram_off, inv_off, ssq_off, dw2_off, img_off, bytes;
-  int n_ssq;
+  size_t words_off, counts_off, gram_off, inv_off, ssq_off, dw2_off, img_off, bytes;
 };
 
 ApplyWorkspace apply_workspace_layout(int64_t d, int64_t k, int r);
 
 int launch_sign_matrix(uint64_t key, int r, int64_t k, float scale, float* A, cudaStream_t s);
-int launch_gram(uint64_t key, int r, int64_t k, uint64_t* words, float* M, cudaStream_t s);
+size_t gram_image_bytes(int r);
+int launch_gram(uint64_t key, int r, int64_t k, uint64_t* words, int* counts, uint8_t* img, cudaStream_t s);
 
 int launch_sketch_simt(const void* X, const void* dY, int dtype, int64_t n, int64_t d, int64_t k, int r,
                        uint64_t key, float scale, float* S, float* P, cudaStream_t s);
@@ -29,9 +29,30 @@ int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_
 
 size_t s_image_bytes(int64_t d, int r);
 int launch_s_image(const float* S, int64_t d, int r, uint8_t* img, cudaStream_t s);
-int launch_apply_tc(int mode, float* W, __nv_bfloat16* Wb, void* out, int accumulate, int64_t d, int64_t k, int r,
-                    uint64_t key, float neg_lrc, const uint8_t* s_img, const float* inv_den, double* dw2_part,
-                    int* grid_out, Control* ctl, cudaStream_t s);
+// The tensor-core kernel behind the apply: mode 0 apply, 1 predict (dW^2 only),
+// 2 rebuild fp32, 3 rebuild bf16, 4 row norms (v, 1/sqrt(v+eps), sync sketch,
+// ||S||^2 partials) from the Gram image.
+struct ApplyLaunch {
+  int mode;
+  float* W;
+  __nv_bfloat16* Wb;
+  void* out;
+  int accumulate;
+  int64_t d, k;
+  int r;
+  uint64_t key;
+  float neg_lrc;            // -lr c
+  const uint8_t* s_img;
+  const uint8_t* m_img;     // mode 4
+  const float* S;           // mode 4
+  const float* v_in;        // mode 4
+  float* v_out;             // mode 4 (nullable: predict)
+  float* inv;               // written by mode 4, read by modes 0 and 1
+  float* sync_out;          // mode 4 (nullable)
+  float beta2, eps;
+  double* part;             // per-CTA partials: dW^2 (modes 0, 1) or ||S||^2 (mode 4)
+};
+int launch_apply_tc(const ApplyLaunch& L, int* grid_out, Control* ctl, cudaStream_t s);
 
 // mode 0 apply, 1 predict, 2 reconstruct fp32, 3 reconstruct bf16.
 int launch_rowadam(int mode, float* W, __nv_bfloat16* Wb, void* out, int accumulate, const float* S,
