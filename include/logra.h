@@ -213,7 +213,8 @@ size_t logra_apply_workspace_bytes(int64_t d, int64_t k, int r);
  * looks up the array's device address (cudaGetSymbolAddress) and caches it;
  * make that first call before any stream capture.  All calls, on every
  * stream of a device, share the one array and the array keeps the last
- * call's contents (the kernels overwrite every byte they read): calls whose
+ * call's contents (each call clears, with cudaMemsetAsync, the part it
+ * accumulates into and overwrites the rest before reading it): calls whose
  * execution overlaps on the GPU race and corrupt each other's results, so
  * order them (one stream, or events).  S, X and dY rules as for
  * logra_sketch_accumulate.

@@ -3,13 +3,14 @@
 //   project   P_s^T = Sigma X_s^T for a k-range s  (D[128 tokens x r] in TMEM;
 //             A = X tile by TMA, B = Sigma tile generated in shared memory
 //             from the sign hash; k split over s for occupancy)
-//   split     P^T = sum_s P_s^T, stored as a two-term bf16 expansion
+//   split     P^T (the k-splits summed by fp32 reductions into one buffer)
+//             stored as a two-term bf16 expansion
 //             P^T = hi + lo, written pre-swizzled in 32-token chunks so the
 //             next kernel loads one chunk with a single bulk copy
 //   accumulate S += (P^T dY)^T / sqrt(r): D[r x N d-columns] in TMEM with
 //             A = P^T chunk (hi and lo, two MMAs into one accumulator),
 //             B = dY tile (MN-major, TMA), tokens split over units; each unit
-//             adds its tile into S with coalesced fp32 reductions.
+//             adds its tile into S with TMA tensor reduce-adds (fp32).
 //
 // (theclarity.today write-up, "Why it matters": S = G A^T is accumulated during
 // backpropagation and G is never formed; academy.dair.ai summary: the random-
@@ -21,7 +22,7 @@
 //
 // Roles per CTA: warp 0 = producer of the first ring, warp 1 = TMEM owner +
 // MMA issuer, warps 2..5 = epilogue (TMEM lane quadrant = warp % 4), warps
-// 6..9 = sign-tile generators (project) / warp 6 = dY producer (accumulate).
+// 6..13 = sign-tile generators (project) / warp 6 = dY producer (accumulate).
 // Every wait is bounded; a wait that runs out records LOGRA_ERR_TIMEOUT in the
 // control block and the CTA drains and exits.
 #include <cuda.h>
@@ -41,12 +42,15 @@ constexpr int kKc = 64;        // k per project stage (one sign word per row)
 constexpr int kChunk = 32;     // tokens per accumulate stage / image chunk
 constexpr int kMaxStages = 16;
 constexpr int kSmemBudget = 227 * 1024 - 1024 - 512;
+constexpr int kStageTile = 32 * 32 * 4;        // one epilogue warp's fp32 staging tile
+constexpr int kStagingBytes = 4 * 2 * kStageTile;   // 4 epilogue warps x 2 tiles
 
 struct SketchShape {
   int64_t n, d, k;
   int r, r_pad;                // r_pad: r rounded up to 128 (accumulate M blocks)
   int n_pad;                   // n rounded up to kChunk
-  int tiles, splits, chunks_per_split, nchunks;      // project
+  int tiles, tgroup, groups;  // project: 128-token tiles, tiles per unit, tile groups
+  int splits, chunks_per_split, nchunks;             // project k-splits
   int ntile_n, dtiles, tsplits, tchunks_per_split;   // accumulate
   int x_stages, g_stages;      // project rings: X tiles, sign tiles
   int a_stages, b_stages;      // accumulate rings: P^T chunks, dY tiles
@@ -55,7 +59,7 @@ struct SketchShape {
 struct Shared {
   uint64_t s_full[kMaxStages], s_empty[kMaxStages];   // streamed operand (X / dY)
   uint64_t o_full[kMaxStages], o_empty[kMaxStages];   // other operand (sign tile / P^T chunk)
-  uint64_t tmem_full[2], tmem_empty[4], drain;
+  uint64_t tmem_full[2], tmem_empty[4], drain;     // tmem_empty: one per accumulator block
   uint2 nib[16];                                       // 4 sign bits -> 4 bf16 +-1
   uint32_t tmem_base;
   int abort;
@@ -99,18 +103,25 @@ __device__ __forceinline__ void gen_sigma_kmajor(uint8_t* tile, const uint2* nib
   }
 }
 
-__global__ void __launch_bounds__(320, 1)
-    project_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, SketchShape sh_, uint64_t key,
-                      float* __restrict__ ppart, Control* ctl) {
+// One unit = (group of `tgroup` 128-token tiles, k-split): each generated sign
+// tile feeds the MMAs of every token tile of the group, so the generation cost
+// per MMA falls with the group size.  The epilogue stages 32 x 32 fp32 tiles in
+// shared memory and hands them to TMA: a plain tensor store when k is not split,
+// a tensor reduce-add (performed by the TMA unit and L2) into the zeroed P^T
+// buffer when it is.
+__global__ void __launch_bounds__(448, 1)
+    project_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_p,
+                      SketchShape sh_, uint64_t key, Control* ctl) {
   extern __shared__ uint8_t smem_raw[];
   const SketchShape& P = sh_;
   uint8_t* base = align1024(smem_raw);
-  const int XS = P.x_stages, GS = P.g_stages;
-  const uint32_t x_bytes = kTok * 128;
+  const int XS = P.x_stages, GS = P.g_stages, T = P.tgroup;
+  const uint32_t x_bytes = uint32_t(T) * kTok * 128;
   const uint32_t g_bytes = uint32_t(P.r) * 128;
   uint8_t* x_tiles = base;
   uint8_t* g_tiles = base + size_t(XS) * x_bytes;
-  Shared* sh = reinterpret_cast<Shared*>(g_tiles + size_t(GS) * g_bytes);
+  uint8_t* staging = g_tiles + size_t(GS) * g_bytes;
+  Shared* sh = reinterpret_cast<Shared*>(staging + kStagingBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned long long limit = ctl->wait_limit;
 
@@ -120,27 +131,26 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&sh->s_empty[s], 1);
     }
     for (int s = 0; s < GS; ++s) {
-      mbar_init(&sh->o_full[s], 4);
+      mbar_init(&sh->o_full[s], 8);
       mbar_init(&sh->o_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&sh->tmem_full[b], 1);
-      mbar_init(&sh->tmem_empty[b], 4);
-    }
+    mbar_init(&sh->tmem_full[0], 1);
+    for (int t = 0; t < 4; ++t) mbar_init(&sh->tmem_empty[t], 4);
     mbar_init(&sh->drain, 1);
     sh->abort = 0;
     fence_mbar_init();
     prefetch_tmap(&tmap_x);
+    prefetch_tmap(&tmap_p);
   }
   if (threadIdx.x < 16) {
     const uint4 v = signs8_to_bf16(threadIdx.x);       // elements 0..3 of the nibble in .x, .y
     sh->nib[threadIdx.x] = make_uint2(v.x, v.y);
   }
-  // one accumulator of r columns, two (double buffered) when they fit
+  // one accumulator of acc_cols (>= r) columns per token tile of the group
   uint32_t acc_cols = 32;
   while (acc_cols < uint32_t(P.r)) acc_cols <<= 1;
-  const int nbuf = acc_cols <= 256 ? 2 : 1;
-  const uint32_t tmem_cols = acc_cols * nbuf;
+  uint32_t tmem_cols = 32;
+  while (tmem_cols < acc_cols * uint32_t(T)) tmem_cols <<= 1;
   if (warp == 1) {
     tmem_alloc(&sh->tmem_base, tmem_cols);
     tmem_relinquish();
@@ -149,15 +159,15 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh->tmem_base;
-  const int units = P.tiles * P.splits;
+  const int units = P.groups * P.splits;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- X tile producer
+    // ---------------------------------------------------------------- X tile producer (T tiles per stage)
     if (lane == 0) {
       Ring xr;
       int inject = ctl->inject_fault && blockIdx.x == 0;
       for (int u = blockIdx.x; u < units; u += gridDim.x) {
-        const int tile = u % P.tiles, split = u / P.tiles;
+        const int grp = u % P.groups, split = u / P.groups;
         const int c0 = split * P.chunks_per_split;
         const int c1 = min(P.nchunks, c0 + P.chunks_per_split);
         for (int c = c0; c < c1; ++c) {
@@ -165,8 +175,10 @@ __global__ void __launch_bounds__(320, 1)
           if (inject && c == c0 + 1) {
             inject = 0;                      // test hook: this stage never fills
           } else {
+            uint8_t* dst = x_tiles + size_t(xr.stage) * x_bytes;
             mbar_arrive_expect_tx(&sh->s_full[xr.stage], x_bytes);
-            tma_load_2d(x_tiles + size_t(xr.stage) * x_bytes, &tmap_x, &sh->s_full[xr.stage], c * kKc, tile * kTok);
+            for (int t = 0; t < T; ++t)
+              tma_load_2d(dst + t * (kTok * 128), &tmap_x, &sh->s_full[xr.stage], c * kKc, (grp * T + t) * kTok);
           }
           xr.next(XS);
         }
@@ -178,19 +190,14 @@ __global__ void __launch_bounds__(320, 1)
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       Ring xr, gr;
-      uint32_t tph[2] = {0, 0};
-      int buf = 0;
+      uint32_t tphase = 0;
       const int nparts = P.r > 256 ? 2 : 1;
       const int npart = P.r / nparts;
       const uint32_t idesc = idesc_bf16(128, uint32_t(npart), 0, 0);
       for (int u = blockIdx.x; u < units && !sh->abort; u += gridDim.x) {
-        const int split = u / P.tiles;
+        const int split = u / P.groups;
         const int c0 = split * P.chunks_per_split;
         const int c1 = min(P.nchunks, c0 + P.chunks_per_split);
-        if (!wait_or_abort(sh, &sh->tmem_empty[buf], tph[buf] ^ 1u, limit, ctl)) break;
-        tc_fence_after();
-        const uint32_t dacc = tmem + uint32_t(buf) * acc_cols;
-        bool first = true;
         for (int c = c0; c < c1; ++c) {
           if (!wait_or_abort(sh, &sh->s_full[xr.stage], xr.phase, limit, ctl)) goto mma_done;
           if (!wait_or_abort(sh, &sh->o_full[gr.stage], gr.phase, limit, ctl)) goto mma_done;
@@ -199,63 +206,84 @@ __global__ void __launch_bounds__(320, 1)
           const uint32_t b0 = smem_addr(g_tiles + size_t(gr.stage) * g_bytes);
 #pragma unroll
           for (int ks = 0; ks < kKc / 16; ++ks) {
-            const uint64_t ad = smem_desc(a0 + ks * 32, 16, 1024, kSw128);
-            for (int p = 0; p < nparts; ++p) {
-              const uint64_t bd = smem_desc(b0 + uint32_t(p * npart) * 128 + ks * 32, 16, 1024, kSw128);
-              mma_bf16(dacc + uint32_t(p * npart), ad, bd, idesc, first ? 0u : 1u);
+            for (int t = 0; t < T; ++t) {
+              if (c == c0 && ks == 0) {
+                // accumulator t is free once the epilogue has drained it
+                if (!wait_or_abort(sh, &sh->tmem_empty[t], tphase ^ 1u, limit, ctl)) goto mma_done;
+                tc_fence_after();
+              }
+              const uint64_t ad = smem_desc(a0 + t * (kTok * 128) + ks * 32, 16, 1024, kSw128);
+              for (int p = 0; p < nparts; ++p) {
+                const uint64_t bd = smem_desc(b0 + uint32_t(p * npart) * 128 + ks * 32, 16, 1024, kSw128);
+                mma_bf16(tmem + uint32_t(t) * acc_cols + uint32_t(p * npart), ad, bd, idesc,
+                         (c == c0 && ks == 0) ? 0u : 1u);
+              }
             }
-            first = false;
           }
           mma_commit(&sh->s_empty[xr.stage]);
           mma_commit(&sh->o_empty[gr.stage]);
           xr.next(XS);
           gr.next(GS);
         }
-        mma_commit(&sh->tmem_full[buf]);
-        tph[buf] ^= 1u;
-        if (nbuf == 2) buf ^= 1;
+        mma_commit(&sh->tmem_full[0]);
+        tphase ^= 1u;
       }
     mma_done:
       mma_commit(&sh->drain);
       mbar_wait(&sh->drain, 0, limit);
     }
   } else if (warp < 6) {
-    // ---------------------------------------------------------------- epilogue: TMEM -> P partials
+    // ---------------------------------------------------------------- epilogue: TMEM -> smem -> TMA into P^T
     const int quad = warp & 3;
-    uint32_t tph[2] = {0, 0};
-    int buf = 0;
+    float* stg = reinterpret_cast<float*>(staging + (warp - 2) * 2 * kStageTile);
+    uint32_t tphase = 0;
+    int sb = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const int tile = u % P.tiles, split = u / P.tiles;
-      if (!warp_wait(sh, &sh->tmem_full[buf], tph[buf], limit, ctl)) break;
-      tph[buf] ^= 1u;
+      const int grp = u % P.groups;
+      if (!warp_wait(sh, &sh->tmem_full[0], tphase, limit, ctl)) break;
+      tphase ^= 1u;
       tc_fence_after();
-      const int64_t t = int64_t(tile) * kTok + quad * 32 + lane;
-      float* dst = ppart + int64_t(split) * P.r * P.n_pad + t;
-      for (int c = 0; c < P.r; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + uint32_t(buf) * acc_cols + (uint32_t(quad * 32) << 16) + uint32_t(c), v);
-        tmem_ld_wait();
-        if (t < P.n) {
+      for (int t = 0; t < T; ++t) {
+        const int x0 = (grp * T + t) * kTok + quad * 32;   // first token of this warp's lanes
+        for (int c = 0; c < P.r; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem + uint32_t(t) * acc_cols + (uint32_t(quad * 32) << 16) + uint32_t(c), v);
+          tmem_ld_wait();
+          // staging tile [32 ranks][32 tokens]: lane = token, so each row store is one 128-byte line
+          float* tile = stg + sb * (32 * 32);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) dst[int64_t(c + j) * P.n_pad] = __uint_as_float(v[j]);
+          for (int j = 0; j < 32; ++j) tile[j * 32 + lane] = __uint_as_float(v[j]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (x0 < P.n_pad) {
+              if (P.splits == 1) tma_store_2d(&tmap_p, tile, x0, c);
+              else tma_reduce_add_2d(&tmap_p, tile, x0, c);
+            }
+            bulk_commit();
+            bulk_wait_read_1();      // the other staging tile is free again
+          }
+          __syncwarp();
+          sb ^= 1;
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->tmem_empty[t]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh->tmem_empty[buf]);
-      if (nbuf == 2) buf ^= 1;
     }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   } else {
-    // ---------------------------------------------------------------- sign-tile generators
+    // ---------------------------------------------------------------- sign-tile generators (8 warps)
     const int gtid = threadIdx.x - 192;
     Ring gr;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const int split = u / P.tiles;
+      const int split = u / P.groups;
       const int c0 = split * P.chunks_per_split;
       const int c1 = min(P.nchunks, c0 + P.chunks_per_split);
       for (int c = c0; c < c1; ++c) {
         if (!warp_wait(sh, &sh->o_empty[gr.stage], gr.phase ^ 1u, limit, ctl)) goto gen_done;
-        gen_sigma_kmajor(g_tiles + size_t(gr.stage) * g_bytes, sh->nib, key, P.r, c, gtid, 128);
+        gen_sigma_kmajor(g_tiles + size_t(gr.stage) * g_bytes, sh->nib, key, P.r, c, gtid, 256);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->o_full[gr.stage]);
@@ -288,12 +316,10 @@ __global__ void __launch_bounds__(256) split_kernel(const float* __restrict__ pp
     const int64_t t0 = c * kChunk + g * 8;
     float p[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     if (row < P.r) {
-      for (int s = 0; s < P.splits; ++s) {
-        const float4* src = reinterpret_cast<const float4*>(ppart + (int64_t(s) * P.r + row) * P.n_pad + t0);
-        const float4 x0 = src[0], x1 = src[1];
-        p[0] += x0.x; p[1] += x0.y; p[2] += x0.z; p[3] += x0.w;
-        p[4] += x1.x; p[5] += x1.y; p[6] += x1.z; p[7] += x1.w;
-      }
+      const float4* src = reinterpret_cast<const float4*>(ppart + int64_t(row) * P.n_pad + t0);
+      const float4 x0 = src[0], x1 = src[1];
+      p[0] = x0.x; p[1] = x0.y; p[2] = x0.z; p[3] = x0.w;
+      p[4] = x1.x; p[5] = x1.y; p[6] = x1.z; p[7] = x1.w;
 #pragma unroll
       for (int i = 0; i < 8; ++i)
         if (t0 + i >= P.n) p[i] = 0.f;
@@ -315,8 +341,8 @@ __global__ void __launch_bounds__(256) split_kernel(const float* __restrict__ pp
 
 // ============================================================================ accumulate
 __global__ void __launch_bounds__(224, 1)
-    accumulate_tc_kernel(const __grid_constant__ CUtensorMap tmap_dy, SketchShape sh_, const uint8_t* __restrict__ image,
-                         float scale, float* __restrict__ S, Control* ctl) {
+    accumulate_tc_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_s,
+                         SketchShape sh_, const uint8_t* __restrict__ image, float scale, Control* ctl) {
   extern __shared__ uint8_t smem_raw[];
   const SketchShape& P = sh_;
   uint8_t* base = align1024(smem_raw);
@@ -326,7 +352,8 @@ __global__ void __launch_bounds__(224, 1)
   const uint32_t b_bytes = uint32_t(N) * kChunk * 2;
   uint8_t* a_tiles = base;
   uint8_t* b_tiles = base + size_t(AS) * a_bytes;
-  Shared* sh = reinterpret_cast<Shared*>(b_tiles + size_t(BS) * b_bytes);
+  uint8_t* staging = b_tiles + size_t(BS) * b_bytes;
+  Shared* sh = reinterpret_cast<Shared*>(staging + kStagingBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned long long limit = ctl->wait_limit;
   const int mblocks = P.r_pad / 128;
@@ -444,32 +471,44 @@ __global__ void __launch_bounds__(224, 1)
       mbar_wait(&sh->drain, 0, limit);
     }
   } else if (warp < 6) {
-    // ---------------------------------------------------------------- epilogue: TMEM -> S (fp32 reductions)
+    // ---------------------------------------------------------------- epilogue: TMEM -> smem -> TMA reduce-add into S
     const int quad = warp & 3;
+    float* stg = reinterpret_cast<float*>(staging + (warp - 2) * 2 * kStageTile);
     uint32_t tphase = 0;
+    int sb = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const int dt = u % P.dtiles;
       if (!warp_wait(sh, &sh->tmem_full[0], tphase, limit, ctl)) break;
       tphase ^= 1u;
       tc_fence_after();
       for (int m = 0; m < mblocks; ++m) {
-        const int ridx = m * 128 + quad * 32 + lane;
+        const int r0 = m * 128 + quad * 32;              // first rank of this warp's lanes
         for (int c = 0; c < N; c += 32) {
           uint32_t v[32];
           tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + uint32_t(m * N + c), v);
           tmem_ld_wait();
-          const int64_t d0 = int64_t(dt) * N + c;
-          if (ridx < P.r) {
+          // staging tile [32 d-rows][32 ranks] = a box of S (d x r, row-major); lane = rank
+          float* tile = stg + sb * (32 * 32);
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (d0 + j < P.d) red_add_f32(S + (d0 + j) * P.r + ridx, __uint_as_float(v[j]) * scale);
+          for (int j = 0; j < 32; ++j) tile[j * 32 + lane] = __uint_as_float(v[j]) * scale;
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int64_t d0 = int64_t(dt) * N + c;
+            if (r0 < P.r && d0 < P.d) tma_reduce_add_2d(&tmap_s, tile, r0, int32_t(d0));
+            bulk_commit();
+            bulk_wait_read_1();      // the other staging tile is free again
           }
+          __syncwarp();
+          sb ^= 1;
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->tmem_empty[m]);
       }
     }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -510,8 +549,11 @@ static SketchShape plan(int64_t n, int64_t d, int64_t k, int r, int sms) {
   P.r_pad = ceil_div(r, 128) * 128;
   P.n_pad = ceil_div(n, kChunk) * kChunk;
   P.tiles = ceil_div(n, kTok);
+  // two token tiles share each generated sign tile when their accumulators fit TMEM together
+  P.tgroup = (r <= 256 && P.tiles > 1) ? 2 : 1;
+  P.groups = ceil_div(P.tiles, P.tgroup);
   P.nchunks = ceil_div(k, kKc);
-  P.splits = pick_splits(P.tiles, sms, P.nchunks, 8, 8);
+  P.splits = pick_splits(P.groups, sms, P.nchunks, 8, 8);
   P.chunks_per_split = ceil_div(P.nchunks, P.splits);
   P.splits = ceil_div(P.nchunks, P.chunks_per_split);
   P.ntile_n = (P.r_pad <= 256) ? 256 : 128;
@@ -522,27 +564,28 @@ static SketchShape plan(int64_t n, int64_t d, int64_t k, int r, int sms) {
   P.tsplits = ceil_div(tchunks, P.tchunks_per_split);
   // project: two sign-tile stages, the rest of shared memory for X tiles
   P.g_stages = 2;
-  P.x_stages = (kSmemBudget - 2 * r * 128) / (kTok * 128);
+  P.x_stages = (kSmemBudget - kStagingBytes - 2 * r * 128) / (P.tgroup * kTok * 128);
   if (P.x_stages > kMaxStages) P.x_stages = kMaxStages;
   // accumulate: P^T chunks come from L2 (three stages), dY from HBM (the rest)
   const int a_bytes = P.r_pad * 128, b_bytes = P.ntile_n * kChunk * 2;
   P.a_stages = P.r_pad >= 512 ? 2 : 3;
-  P.b_stages = (kSmemBudget - P.a_stages * a_bytes) / b_bytes;
+  P.b_stages = (kSmemBudget - kStagingBytes - P.a_stages * a_bytes) / b_bytes;
   if (P.b_stages > kMaxStages) P.b_stages = kMaxStages;
   return P;
 }
 
 static int proj_smem_bytes(const SketchShape& P) {
-  return 1024 + P.x_stages * kTok * 128 + P.g_stages * P.r * 128 + int(sizeof(Shared));
+  return 1024 + P.x_stages * P.tgroup * kTok * 128 + P.g_stages * P.r * 128 + kStagingBytes + int(sizeof(Shared));
 }
 
 static int acc_smem_bytes(const SketchShape& P) {
-  return 1024 + P.a_stages * P.r_pad * 128 + P.b_stages * P.ntile_n * kChunk * 2 + int(sizeof(Shared));
+  return 1024 + P.a_stages * P.r_pad * 128 + P.b_stages * P.ntile_n * kChunk * 2 + kStagingBytes +
+         int(sizeof(Shared));
 }
 
 size_t sketch_tc_workspace_bytes(int64_t n, int64_t d, int64_t k, int r, int sms) {
   const SketchShape P = plan(n, d, k, r, sms);
-  const size_t part = size_t(P.splits) * P.r * P.n_pad * 4;
+  const size_t part = size_t(P.r) * P.n_pad * 4;
   const size_t img = size_t(P.n_pad) * P.r_pad * 4;
   return ((part + 1023) & ~size_t(1023)) + img;
 }
@@ -552,21 +595,29 @@ int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_
   const int sms = sm_count();
   const SketchShape P = plan(n, d, k, r, sms);
   float* ppart = static_cast<float*>(ws);
-  const size_t part = size_t(P.splits) * P.r * P.n_pad * 4;
+  const size_t part = size_t(P.r) * P.n_pad * 4;
   uint8_t* image = static_cast<uint8_t*>(ws) + ((part + 1023) & ~size_t(1023));
 
-  CUtensorMap tx, tdy;
+  CUtensorMap tx, tdy, tp, ts;
   if (int st = make_tmap_2d(&tx, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, uint64_t(k), uint64_t(n), uint64_t(k) * 2,
                             kKc, kTok, CU_TENSOR_MAP_SWIZZLE_128B))
     return st;
   if (int st = make_tmap_2d(&tdy, dY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, uint64_t(d), uint64_t(n), uint64_t(d) * 2,
                             64, kChunk, CU_TENSOR_MAP_SWIZZLE_128B))
     return st;
+  // P^T (r x n_pad fp32) and S (d x r fp32) in 32 x 32 boxes for the epilogues' TMA store / reduce-add
+  if (int st = make_tmap_2d(&tp, ppart, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(P.n_pad), uint64_t(r),
+                            uint64_t(P.n_pad) * 4, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return st;
+  if (int st = make_tmap_2d(&ts, S, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(r), uint64_t(d), uint64_t(r) * 4,
+                            32, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return st;
 
   const int proj_smem = proj_smem_bytes(P);
   LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(project_tc_kernel), proj_smem));
-  const int punits = P.tiles * P.splits;
-  project_tc_kernel<<<punits < sms ? punits : sms, 320, proj_smem, s>>>(tx, P, key, ppart, ctl);
+  const int punits = P.groups * P.splits;
+  if (P.splits > 1) LOGRA_CUDA_TRY(cudaMemsetAsync(ppart, 0, part, s));   // the k-splits reduce-add into it
+  project_tc_kernel<<<punits < sms ? punits : sms, 448, proj_smem, s>>>(tx, tp, P, key, ctl);
   LOGRA_LAUNCHED();
 
   const int64_t stotal = int64_t(P.n_pad / kChunk) * P.r_pad * 4;
@@ -578,7 +629,7 @@ int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_
   const int acc_smem = acc_smem_bytes(P);
   LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(accumulate_tc_kernel), acc_smem));
   const int aunits = P.dtiles * P.tsplits;
-  accumulate_tc_kernel<<<aunits < sms ? aunits : sms, 224, acc_smem, s>>>(tdy, P, image, scale, S, ctl);
+  accumulate_tc_kernel<<<aunits < sms ? aunits : sms, 224, acc_smem, s>>>(tdy, ts, P, image, scale, ctl);
   LOGRA_LAUNCHED();
   return LOGRA_OK;
 }
