@@ -398,7 +398,8 @@ def run_e2e(args, L, dp, mats, w, r, dt, dev, stream, sk_f, world):
     maxd = max(m["d"] for m in mats)
     bufX = [torch.empty(n * maxk, dtype=dt, device=dev) for _ in range(2)]
     bufY = [torch.empty(n * maxd, dtype=dt, device=dev) for _ in range(2)]
-    copy = torch.cuda.Stream(device=dev)
+    # two copy streams, each moving half of every tensor, so two copy engines work at once
+    copies = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
     norms_h = torch.empty((len(mats), 2), dtype=torch.float64).pin_memory()
     h2d = d2h = 0
 
@@ -411,17 +412,22 @@ def run_e2e(args, L, dp, mats, w, r, dt, dev, stream, sk_f, world):
             m["S"].zero_()
             for mb in range(nmb):
                 slot = i % 2
-                with torch.cuda.stream(copy):
-                    if done[slot] is not None:
-                        copy.wait_event(done[slot])
-                    Xd = bufX[slot][: n * m["k"]].view(n, m["k"])
-                    Yd = bufY[slot][: n * m["d"]].view(n, m["d"])
-                    Xd.copy_(Xh, non_blocking=True)
-                    Yd.copy_(Yh, non_blocking=True)
-                    ready = torch.cuda.Event()
-                    ready.record(copy)
+                Xd = bufX[slot][: n * m["k"]].view(n, m["k"])
+                Yd = bufY[slot][: n * m["d"]].view(n, m["d"])
+                readies = []
+                for half, cs in enumerate(copies):
+                    with torch.cuda.stream(cs):
+                        if done[slot] is not None:
+                            cs.wait_event(done[slot])
+                        lo, hi = (0, n // 2) if half == 0 else (n // 2, n)
+                        Xd[lo:hi].copy_(Xh[lo:hi], non_blocking=True)
+                        Yd[lo:hi].copy_(Yh[lo:hi], non_blocking=True)
+                        ev_r = torch.cuda.Event()
+                        ev_r.record(cs)
+                        readies.append(ev_r)
                 h2d += Xh.numel() * Xh.element_size() + Yh.numel() * Yh.element_size()
-                stream.wait_event(ready)
+                for ev_r in readies:
+                    stream.wait_event(ev_r)
                 L.logra_sketch_accumulate(Xd, Yd, m["S"], m["seed"], step_idx)
                 ev = torch.cuda.Event()
                 ev.record(stream)

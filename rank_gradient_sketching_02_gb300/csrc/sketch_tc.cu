@@ -22,7 +22,8 @@
 //
 // Roles per CTA: warp 0 = producer of the first ring, warp 1 = TMEM owner +
 // MMA issuer, warps 2..5 = epilogue (TMEM lane quadrant = warp % 4), warps
-// 6..13 = sign-tile generators (project) / warp 6 = dY producer (accumulate).
+// 6..15 except 9 and 13 = sign-tile generators (project; the two skipped warps
+// share the MMA warp's scheduler) / warp 6 = dY producer (accumulate).
 // Every wait is bounded; a wait that runs out records LOGRA_ERR_TIMEOUT in the
 // control block and the CTA drains and exits.
 #include <cuda.h>
@@ -109,7 +110,7 @@ __device__ __forceinline__ void gen_sigma_kmajor(uint8_t* tile, const uint2* nib
 // shared memory and hands them to TMA: a plain tensor store when k is not split,
 // a tensor reduce-add (performed by the TMA unit and L2) into the zeroed P^T
 // buffer when it is.
-__global__ void __launch_bounds__(448, 1)
+__global__ void __launch_bounds__(512, 1)
     project_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_p,
                       SketchShape sh_, uint64_t key, Control* ctl) {
   extern __shared__ uint8_t smem_raw[];
@@ -273,9 +274,11 @@ __global__ void __launch_bounds__(448, 1)
     }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
-  } else {
+  } else if (warp != 9 && warp != 13) {
     // ---------------------------------------------------------------- sign-tile generators (8 warps)
-    const int gtid = threadIdx.x - 192;
+    // Warps 9 and 13 stay idle so that no generator shares the MMA warp's
+    // scheduler (warp % 4 == 1): the single issuing thread keeps its issue slots.
+    const int gtid = (warp - 6 - (warp > 9) - (warp > 13)) * 32 + lane;
     Ring gr;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const int split = u / P.groups;
@@ -340,7 +343,7 @@ __global__ void __launch_bounds__(256) split_kernel(const float* __restrict__ pp
 }
 
 // ============================================================================ accumulate
-__global__ void __launch_bounds__(224, 1)
+__global__ void __launch_bounds__(352, 1)
     accumulate_tc_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_s,
                          SketchShape sh_, const uint8_t* __restrict__ image, float scale, Control* ctl) {
   extern __shared__ uint8_t smem_raw[];
@@ -368,7 +371,7 @@ __global__ void __launch_bounds__(224, 1)
       mbar_init(&sh->o_empty[s], 1);
     }
     mbar_init(&sh->tmem_full[0], 1);
-    for (int m = 0; m < 4; ++m) mbar_init(&sh->tmem_empty[m], 4);
+    for (int m = 0; m < 4; ++m) mbar_init(&sh->tmem_empty[m], 8);
     mbar_init(&sh->drain, 1);
     sh->abort = 0;
     fence_mbar_init();
@@ -470,12 +473,17 @@ __global__ void __launch_bounds__(224, 1)
       mma_commit(&sh->drain);
       mbar_wait(&sh->drain, 0, limit);
     }
-  } else if (warp < 6) {
+  } else if ((warp >= 2 && warp < 6) || (warp >= 7 && warp < 11)) {
     // ---------------------------------------------------------------- epilogue: TMEM -> smem -> TMA reduce-add into S
+    // Two groups of four warps (2..5 and 7..10) cover all four TMEM lane
+    // quadrants each; group g drains columns [g N/2, (g+1) N/2) of every M
+    // block, so an accumulator is free again after half the drain time.
     const int quad = warp & 3;
-    float* stg = reinterpret_cast<float*>(staging + (warp - 2) * 2 * kStageTile);
+    const int grp = warp >= 7 ? 1 : 0;
+    const int eidx = grp * 4 + (warp - (grp ? 7 : 2));
+    float* tile = reinterpret_cast<float*>(staging + eidx * kStageTile);
+    const int cbeg = grp * (N / 2), cend = cbeg + N / 2;
     uint32_t tphase = 0;
-    int sb = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const int dt = u % P.dtiles;
       if (!warp_wait(sh, &sh->tmem_full[0], tphase, limit, ctl)) break;
@@ -483,12 +491,11 @@ __global__ void __launch_bounds__(224, 1)
       tc_fence_after();
       for (int m = 0; m < mblocks; ++m) {
         const int r0 = m * 128 + quad * 32;              // first rank of this warp's lanes
-        for (int c = 0; c < N; c += 32) {
+        for (int c = cbeg; c < cend; c += 32) {
           uint32_t v[32];
           tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + uint32_t(m * N + c), v);
           tmem_ld_wait();
           // staging tile [32 d-rows][32 ranks] = a box of S (d x r, row-major); lane = rank
-          float* tile = stg + sb * (32 * 32);
 #pragma unroll
           for (int j = 0; j < 32; ++j) tile[j * 32 + lane] = __uint_as_float(v[j]) * scale;
           fence_proxy_async_smem();
@@ -497,10 +504,9 @@ __global__ void __launch_bounds__(224, 1)
             const int64_t d0 = int64_t(dt) * N + c;
             if (r0 < P.r && d0 < P.d) tma_reduce_add_2d(&tmap_s, tile, r0, int32_t(d0));
             bulk_commit();
-            bulk_wait_read_1();      // the other staging tile is free again
+            bulk_wait_read_all();    // the staging tile is free again
           }
           __syncwarp();
-          sb ^= 1;
         }
         tc_fence_before();
         __syncwarp();
@@ -553,7 +559,7 @@ static SketchShape plan(int64_t n, int64_t d, int64_t k, int r, int sms) {
   P.tgroup = (r <= 256 && P.tiles > 1) ? 2 : 1;
   P.groups = ceil_div(P.tiles, P.tgroup);
   P.nchunks = ceil_div(k, kKc);
-  P.splits = pick_splits(P.groups, sms, P.nchunks, 8, 8);
+  P.splits = pick_splits(P.groups, sms, P.nchunks, 8, 12);
   P.chunks_per_split = ceil_div(P.nchunks, P.splits);
   P.splits = ceil_div(P.nchunks, P.chunks_per_split);
   P.ntile_n = (P.r_pad <= 256) ? 256 : 128;
@@ -617,7 +623,7 @@ int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_
   LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(project_tc_kernel), proj_smem));
   const int punits = P.groups * P.splits;
   if (P.splits > 1) LOGRA_CUDA_TRY(cudaMemsetAsync(ppart, 0, part, s));   // the k-splits reduce-add into it
-  project_tc_kernel<<<punits < sms ? punits : sms, 448, proj_smem, s>>>(tx, tp, P, key, ctl);
+  project_tc_kernel<<<punits < sms ? punits : sms, 512, proj_smem, s>>>(tx, tp, P, key, ctl);
   LOGRA_LAUNCHED();
 
   const int64_t stotal = int64_t(P.n_pad / kChunk) * P.r_pad * 4;
@@ -629,7 +635,7 @@ int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_
   const int acc_smem = acc_smem_bytes(P);
   LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(accumulate_tc_kernel), acc_smem));
   const int aunits = P.dtiles * P.tsplits;
-  accumulate_tc_kernel<<<aunits < sms ? aunits : sms, 224, acc_smem, s>>>(tdy, ts, P, image, scale, ctl);
+  accumulate_tc_kernel<<<aunits < sms ? aunits : sms, 352, acc_smem, s>>>(tdy, ts, P, image, scale, ctl);
   LOGRA_LAUNCHED();
   return LOGRA_OK;
 }
