@@ -3,7 +3,7 @@
 //   project   P_s^T = Sigma X_s^T for a k-range s  (D[128 tokens x r] in TMEM;
 //             A = X tile by TMA, B = Sigma tile generated in shared memory
 //             from the sign hash; k split over s for occupancy)
-//   split     P^T (the k-splits summed by fp32 reductions into one buffer)
+//   split     P^T (partial k ranges summed by fp32 reductions into one buffer)
 //             stored as a two-term bf16 expansion
 //             P^T = hi + lo, written pre-swizzled in 32-token chunks so the
 //             next kernel loads one chunk with a single bulk copy
@@ -51,8 +51,9 @@ struct SketchShape {
   int r, r_pad;                // r_pad: r rounded up to 128 (accumulate M blocks)
   int n_pad;                   // n rounded up to kChunk
   int tiles, tgroup, groups;  // project: 128-token tiles, tiles per unit, tile groups
-  int splits, chunks_per_split, nchunks;             // project k-splits
-  int ntile_n, dtiles, tsplits, tchunks_per_split;   // accumulate
+  int nchunks;                 // project k-chunks per token group
+  int proj_ctas, proj_partial; // project grid; some segment covers only part of the k range
+  int ntile_n, dtiles, acc_ctas;   // accumulate: d tile width, d tiles, grid
   int x_stages, g_stages;      // project rings: X tiles, sign tiles
   int a_stages, b_stages;      // accumulate rings: P^T chunks, dY tiles
 };
@@ -71,6 +72,30 @@ struct Ring {
   uint32_t phase = 0;
   __device__ __forceinline__ void next(int n) {
     if (++stage == n) { stage = 0; phase ^= 1u; }
+  }
+};
+
+// Stream-K work split: the flattened (tile, chunk) space of `total` chunks,
+// `per` chunks per tile, is cut into gridDim.x equal contiguous ranges, one per
+// CTA.  A CTA's range falls into segments at tile boundaries; every segment
+// ends with one accumulator drain.  Equal ranges keep the CTAs busy to the end,
+// and because the ranges start at different offsets within a tile, the drains
+// of different CTAs are spread over the run instead of landing together.
+struct SegIter {
+  int64_t f, f1;
+  int per;
+  __device__ __forceinline__ SegIter(int64_t total, int per_) : per(per_) {
+    f = total * blockIdx.x / gridDim.x;
+    f1 = total * (blockIdx.x + 1) / gridDim.x;
+  }
+  __device__ __forceinline__ bool next(int& tile, int& c0, int& c1) {
+    if (f >= f1) return false;
+    tile = int(f / per);
+    c0 = int(f - int64_t(tile) * per);
+    const int64_t rem = f1 - f;
+    c1 = (rem < int64_t(per - c0)) ? c0 + int(rem) : per;
+    f += c1 - c0;
+    return true;
   }
 };
 
@@ -104,12 +129,14 @@ __device__ __forceinline__ void gen_sigma_kmajor(uint8_t* tile, const uint2* nib
   }
 }
 
-// One unit = (group of `tgroup` 128-token tiles, k-split): each generated sign
-// tile feeds the MMAs of every token tile of the group, so the generation cost
-// per MMA falls with the group size.  The epilogue stages 32 x 32 fp32 tiles in
-// shared memory and hands them to TMA: a plain tensor store when k is not split,
-// a tensor reduce-add (performed by the TMA unit and L2) into the zeroed P^T
-// buffer when it is.
+// A segment is (group of `tgroup` 128-token tiles, k-chunk range): each
+// generated sign tile feeds the MMAs of every token tile of the group, so the
+// generation cost per MMA falls with the group size.  The epilogue stages
+// 32 x 32 fp32 tiles in shared memory and hands them to TMA: a plain tensor
+// store when the segment covers the whole k range, else a tensor reduce-add
+// (performed by the TMA unit and L2) into the zeroed P^T buffer.  When two
+// groups' accumulators fit TMEM together, consecutive segments alternate
+// between them, so the drain of one overlaps the MMAs of the next.
 __global__ void __launch_bounds__(512, 1)
     project_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_p,
                       SketchShape sh_, uint64_t key, Control* ctl) {
@@ -125,6 +152,14 @@ __global__ void __launch_bounds__(512, 1)
   Shared* sh = reinterpret_cast<Shared*>(staging + kStagingBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned long long limit = ctl->wait_limit;
+  // one accumulator of acc_cols (>= r) columns per token tile of the group,
+  // and nacc (1 or 2) such sets used by alternate segments
+  uint32_t acc_cols = 32;
+  while (acc_cols < uint32_t(P.r)) acc_cols <<= 1;
+  const int nacc = (acc_cols * uint32_t(T) * 2u <= 512u) ? 2 : 1;
+  uint32_t tmem_cols = 32;
+  while (tmem_cols < acc_cols * uint32_t(T * nacc)) tmem_cols <<= 1;
+  const int64_t total = int64_t(P.groups) * P.nchunks;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < XS; ++s) {
@@ -135,7 +170,7 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&sh->o_full[s], 8);
       mbar_init(&sh->o_empty[s], 1);
     }
-    mbar_init(&sh->tmem_full[0], 1);
+    for (int a = 0; a < 2; ++a) mbar_init(&sh->tmem_full[a], 1);
     for (int t = 0; t < 4; ++t) mbar_init(&sh->tmem_empty[t], 4);
     mbar_init(&sh->drain, 1);
     sh->abort = 0;
@@ -147,11 +182,6 @@ __global__ void __launch_bounds__(512, 1)
     const uint4 v = signs8_to_bf16(threadIdx.x);       // elements 0..3 of the nibble in .x, .y
     sh->nib[threadIdx.x] = make_uint2(v.x, v.y);
   }
-  // one accumulator of acc_cols (>= r) columns per token tile of the group
-  uint32_t acc_cols = 32;
-  while (acc_cols < uint32_t(P.r)) acc_cols <<= 1;
-  uint32_t tmem_cols = 32;
-  while (tmem_cols < acc_cols * uint32_t(T)) tmem_cols <<= 1;
   if (warp == 1) {
     tmem_alloc(&sh->tmem_base, tmem_cols);
     tmem_relinquish();
@@ -160,17 +190,15 @@ __global__ void __launch_bounds__(512, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh->tmem_base;
-  const int units = P.groups * P.splits;
+  int grp, c0, c1;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- X tile producer (T tiles per stage)
     if (lane == 0) {
       Ring xr;
       int inject = ctl->inject_fault && blockIdx.x == 0;
-      for (int u = blockIdx.x; u < units; u += gridDim.x) {
-        const int grp = u % P.groups, split = u / P.groups;
-        const int c0 = split * P.chunks_per_split;
-        const int c1 = min(P.nchunks, c0 + P.chunks_per_split);
+      SegIter it(total, P.nchunks);
+      while (it.next(grp, c0, c1)) {
         for (int c = c0; c < c1; ++c) {
           if (!wait_or_abort(sh, &sh->s_empty[xr.stage], xr.phase ^ 1u, limit, ctl)) goto producer_done;
           if (inject && c == c0 + 1) {
@@ -191,14 +219,14 @@ __global__ void __launch_bounds__(512, 1)
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       Ring xr, gr;
-      uint32_t tphase = 0;
       const int nparts = P.r > 256 ? 2 : 1;
       const int npart = P.r / nparts;
       const uint32_t idesc = idesc_bf16(128, uint32_t(npart), 0, 0);
-      for (int u = blockIdx.x; u < units && !sh->abort; u += gridDim.x) {
-        const int split = u / P.groups;
-        const int c0 = split * P.chunks_per_split;
-        const int c1 = min(P.nchunks, c0 + P.chunks_per_split);
+      SegIter it(total, P.nchunks);
+      for (int seg = 0; !sh->abort && it.next(grp, c0, c1); ++seg) {
+        const int ab = seg & (nacc - 1);
+        const uint32_t uphase = uint32_t(seg / nacc) & 1u;
+        const uint32_t acc0 = tmem + uint32_t(ab * T) * acc_cols;
         for (int c = c0; c < c1; ++c) {
           if (!wait_or_abort(sh, &sh->s_full[xr.stage], xr.phase, limit, ctl)) goto mma_done;
           if (!wait_or_abort(sh, &sh->o_full[gr.stage], gr.phase, limit, ctl)) goto mma_done;
@@ -209,14 +237,14 @@ __global__ void __launch_bounds__(512, 1)
           for (int ks = 0; ks < kKc / 16; ++ks) {
             for (int t = 0; t < T; ++t) {
               if (c == c0 && ks == 0) {
-                // accumulator t is free once the epilogue has drained it
-                if (!wait_or_abort(sh, &sh->tmem_empty[t], tphase ^ 1u, limit, ctl)) goto mma_done;
+                // accumulator t of this set is free once the epilogue has drained it
+                if (!wait_or_abort(sh, &sh->tmem_empty[ab * T + t], uphase ^ 1u, limit, ctl)) goto mma_done;
                 tc_fence_after();
               }
               const uint64_t ad = smem_desc(a0 + t * (kTok * 128) + ks * 32, 16, 1024, kSw128);
               for (int p = 0; p < nparts; ++p) {
                 const uint64_t bd = smem_desc(b0 + uint32_t(p * npart) * 128 + ks * 32, 16, 1024, kSw128);
-                mma_bf16(tmem + uint32_t(t) * acc_cols + uint32_t(p * npart), ad, bd, idesc,
+                mma_bf16(acc0 + uint32_t(t) * acc_cols + uint32_t(p * npart), ad, bd, idesc,
                          (c == c0 && ks == 0) ? 0u : 1u);
               }
             }
@@ -226,8 +254,7 @@ __global__ void __launch_bounds__(512, 1)
           xr.next(XS);
           gr.next(GS);
         }
-        mma_commit(&sh->tmem_full[0]);
-        tphase ^= 1u;
+        mma_commit(&sh->tmem_full[ab]);
       }
     mma_done:
       mma_commit(&sh->drain);
@@ -237,18 +264,20 @@ __global__ void __launch_bounds__(512, 1)
     // ---------------------------------------------------------------- epilogue: TMEM -> smem -> TMA into P^T
     const int quad = warp & 3;
     float* stg = reinterpret_cast<float*>(staging + (warp - 2) * 2 * kStageTile);
-    uint32_t tphase = 0;
     int sb = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const int grp = u % P.groups;
-      if (!warp_wait(sh, &sh->tmem_full[0], tphase, limit, ctl)) break;
-      tphase ^= 1u;
+    SegIter it(total, P.nchunks);
+    for (int seg = 0; it.next(grp, c0, c1); ++seg) {
+      const int ab = seg & (nacc - 1);
+      const uint32_t uphase = uint32_t(seg / nacc) & 1u;
+      const bool whole = (c0 == 0 && c1 == P.nchunks);
+      if (!warp_wait(sh, &sh->tmem_full[ab], uphase, limit, ctl)) break;
       tc_fence_after();
       for (int t = 0; t < T; ++t) {
+        const uint32_t acc = tmem + uint32_t(ab * T + t) * acc_cols;
         const int x0 = (grp * T + t) * kTok + quad * 32;   // first token of this warp's lanes
         for (int c = 0; c < P.r; c += 32) {
           uint32_t v[32];
-          tmem_ld32(tmem + uint32_t(t) * acc_cols + (uint32_t(quad * 32) << 16) + uint32_t(c), v);
+          tmem_ld32(acc + (uint32_t(quad * 32) << 16) + uint32_t(c), v);
           tmem_ld_wait();
           // staging tile [32 ranks][32 tokens]: lane = token, so each row store is one 128-byte line
           float* tile = stg + sb * (32 * 32);
@@ -258,7 +287,7 @@ __global__ void __launch_bounds__(512, 1)
           __syncwarp();
           if (lane == 0) {
             if (x0 < P.n_pad) {
-              if (P.splits == 1) tma_store_2d(&tmap_p, tile, x0, c);
+              if (whole) tma_store_2d(&tmap_p, tile, x0, c);
               else tma_reduce_add_2d(&tmap_p, tile, x0, c);
             }
             bulk_commit();
@@ -269,7 +298,7 @@ __global__ void __launch_bounds__(512, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->tmem_empty[t]);
+        if (lane == 0) mbar_arrive(&sh->tmem_empty[ab * T + t]);
       }
     }
     if (lane == 0) bulk_wait_all();
@@ -280,10 +309,8 @@ __global__ void __launch_bounds__(512, 1)
     // scheduler (warp % 4 == 1): the single issuing thread keeps its issue slots.
     const int gtid = (warp - 6 - (warp > 9) - (warp > 13)) * 32 + lane;
     Ring gr;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const int split = u / P.groups;
-      const int c0 = split * P.chunks_per_split;
-      const int c1 = min(P.nchunks, c0 + P.chunks_per_split);
+    SegIter it(total, P.nchunks);
+    while (it.next(grp, c0, c1)) {
       for (int c = c0; c < c1; ++c) {
         if (!warp_wait(sh, &sh->o_empty[gr.stage], gr.phase ^ 1u, limit, ctl)) goto gen_done;
         gen_sigma_kmajor(g_tiles + size_t(gr.stage) * g_bytes, sh->nib, key, P.r, c, gtid, 256);
@@ -343,6 +370,9 @@ __global__ void __launch_bounds__(256) split_kernel(const float* __restrict__ pp
 }
 
 // ============================================================================ accumulate
+// A segment is (d tile of N columns, token-chunk range).  When two segments'
+// accumulators fit TMEM together (r <= 128), consecutive segments alternate
+// between them so the drain of one overlaps the MMAs of the next.
 __global__ void __launch_bounds__(352, 1)
     accumulate_tc_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_s,
                          SketchShape sh_, const uint8_t* __restrict__ image, float scale, Control* ctl) {
@@ -360,6 +390,9 @@ __global__ void __launch_bounds__(352, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned long long limit = ctl->wait_limit;
   const int mblocks = P.r_pad / 128;
+  const int nacc = (mblocks * N * 2 <= 512) ? 2 : 1;
+  const int nchunks = P.n_pad / kChunk;
+  const int64_t total = int64_t(P.dtiles) * nchunks;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < BS; ++s) {
@@ -370,7 +403,7 @@ __global__ void __launch_bounds__(352, 1)
       mbar_init(&sh->o_full[s], 1);
       mbar_init(&sh->o_empty[s], 1);
     }
-    mbar_init(&sh->tmem_full[0], 1);
+    for (int a = 0; a < 2; ++a) mbar_init(&sh->tmem_full[a], 1);
     for (int m = 0; m < 4; ++m) mbar_init(&sh->tmem_empty[m], 8);
     mbar_init(&sh->drain, 1);
     sh->abort = 0;
@@ -378,7 +411,7 @@ __global__ void __launch_bounds__(352, 1)
     prefetch_tmap(&tmap_dy);
   }
   uint32_t tmem_cols = 32;
-  while (tmem_cols < uint32_t(mblocks * N)) tmem_cols <<= 1;
+  while (tmem_cols < uint32_t(nacc * mblocks * N)) tmem_cols <<= 1;
   if (warp == 1) {
     tmem_alloc(&sh->tmem_base, tmem_cols);
     tmem_relinquish();
@@ -387,17 +420,15 @@ __global__ void __launch_bounds__(352, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh->tmem_base;
-  const int units = P.dtiles * P.tsplits;
-  const int nchunks = P.n_pad / kChunk;
+  int dt, c0, c1;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- P^T chunk producer (L2)
     if (lane == 0) {
       Ring ar;
       int inject = ctl->inject_fault && blockIdx.x == 0;
-      for (int u = blockIdx.x; u < units; u += gridDim.x) {
-        const int ts = u / P.dtiles;
-        const int c0 = ts * P.tchunks_per_split, c1 = min(nchunks, c0 + P.tchunks_per_split);
+      SegIter it(total, nchunks);
+      while (it.next(dt, c0, c1)) {
         for (int c = c0; c < c1; ++c) {
           if (!wait_or_abort(sh, &sh->o_empty[ar.stage], ar.phase ^ 1u, limit, ctl)) goto a_done;
           if (inject && c == c0 + 1) {
@@ -417,9 +448,8 @@ __global__ void __launch_bounds__(352, 1)
     // ---------------------------------------------------------------- dY tile producer (HBM)
     if (lane == 0) {
       Ring br;
-      for (int u = blockIdx.x; u < units; u += gridDim.x) {
-        const int dt = u % P.dtiles, ts = u / P.dtiles;
-        const int c0 = ts * P.tchunks_per_split, c1 = min(nchunks, c0 + P.tchunks_per_split);
+      SegIter it(total, nchunks);
+      while (it.next(dt, c0, c1)) {
         for (int c = c0; c < c1; ++c) {
           if (!wait_or_abort(sh, &sh->s_empty[br.stage], br.phase ^ 1u, limit, ctl)) goto b_done;
           uint8_t* st = b_tiles + size_t(br.stage) * b_bytes;
@@ -436,11 +466,12 @@ __global__ void __launch_bounds__(352, 1)
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       Ring ar, br;
-      uint32_t tphase = 0;
       const uint32_t idesc = idesc_bf16(128, uint32_t(N), 0, 1);
-      for (int u = blockIdx.x; u < units && !sh->abort; u += gridDim.x) {
-        const int ts = u / P.dtiles;
-        const int c0 = ts * P.tchunks_per_split, c1 = min(nchunks, c0 + P.tchunks_per_split);
+      SegIter it(total, nchunks);
+      for (int seg = 0; !sh->abort && it.next(dt, c0, c1); ++seg) {
+        const int ab = seg & (nacc - 1);
+        const uint32_t uphase = uint32_t(seg / nacc) & 1u;
+        const uint32_t acc0 = tmem + uint32_t(ab * mblocks * N);
         for (int c = c0; c < c1; ++c) {
           if (!wait_or_abort(sh, &sh->o_full[ar.stage], ar.phase, limit, ctl)) goto mma_done;
           if (!wait_or_abort(sh, &sh->s_full[br.stage], br.phase, limit, ctl)) goto mma_done;
@@ -452,13 +483,14 @@ __global__ void __launch_bounds__(352, 1)
             const uint64_t bd = smem_desc(b0 + ks * 2048, kChunk * 128, 1024, kSw128);
             for (int m = 0; m < mblocks; ++m) {
               if (c == c0 && ks == 0) {
-                // M block m of the accumulator is free once the epilogue drained it
-                if (!wait_or_abort(sh, &sh->tmem_empty[m], tphase ^ 1u, limit, ctl)) goto mma_done;
+                // M block m of this accumulator set is free once the epilogue drained it
+                if (!wait_or_abort(sh, &sh->tmem_empty[ab * mblocks + m], uphase ^ 1u, limit, ctl)) goto mma_done;
                 tc_fence_after();
               }
               const uint32_t am = a0 + m * (128 * 128) + ks * 32;
-              mma_bf16(tmem + uint32_t(m * N), smem_desc(am, 16, 1024, kSw128), bd, idesc, (c == c0 && ks == 0) ? 0u : 1u);
-              mma_bf16(tmem + uint32_t(m * N), smem_desc(am + 64, 16, 1024, kSw128), bd, idesc, 1u);
+              const uint32_t acc = acc0 + uint32_t(m * N);
+              mma_bf16(acc, smem_desc(am, 16, 1024, kSw128), bd, idesc, (c == c0 && ks == 0) ? 0u : 1u);
+              mma_bf16(acc, smem_desc(am + 64, 16, 1024, kSw128), bd, idesc, 1u);
             }
           }
           mma_commit(&sh->o_empty[ar.stage]);
@@ -466,8 +498,7 @@ __global__ void __launch_bounds__(352, 1)
           ar.next(AS);
           br.next(BS);
         }
-        mma_commit(&sh->tmem_full[0]);
-        tphase ^= 1u;
+        mma_commit(&sh->tmem_full[ab]);
       }
     mma_done:
       mma_commit(&sh->drain);
@@ -483,17 +514,18 @@ __global__ void __launch_bounds__(352, 1)
     const int eidx = grp * 4 + (warp - (grp ? 7 : 2));
     float* tile = reinterpret_cast<float*>(staging + eidx * kStageTile);
     const int cbeg = grp * (N / 2), cend = cbeg + N / 2;
-    uint32_t tphase = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const int dt = u % P.dtiles;
-      if (!warp_wait(sh, &sh->tmem_full[0], tphase, limit, ctl)) break;
-      tphase ^= 1u;
+    SegIter it(total, nchunks);
+    for (int seg = 0; it.next(dt, c0, c1); ++seg) {
+      const int ab = seg & (nacc - 1);
+      const uint32_t uphase = uint32_t(seg / nacc) & 1u;
+      if (!warp_wait(sh, &sh->tmem_full[ab], uphase, limit, ctl)) break;
       tc_fence_after();
       for (int m = 0; m < mblocks; ++m) {
         const int r0 = m * 128 + quad * 32;              // first rank of this warp's lanes
+        const uint32_t acc = tmem + uint32_t((ab * mblocks + m) * N);
         for (int c = cbeg; c < cend; c += 32) {
           uint32_t v[32];
-          tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + uint32_t(m * N + c), v);
+          tmem_ld32(acc + (uint32_t(quad * 32) << 16) + uint32_t(c), v);
           tmem_ld_wait();
           // staging tile [32 d-rows][32 ranks] = a box of S (d x r, row-major); lane = rank
 #pragma unroll
@@ -510,7 +542,7 @@ __global__ void __launch_bounds__(352, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->tmem_empty[m]);
+        if (lane == 0) mbar_arrive(&sh->tmem_empty[ab * mblocks + m]);
       }
     }
     if (lane == 0) bulk_wait_all();
@@ -528,25 +560,20 @@ __global__ void __launch_bounds__(352, 1)
 // ============================================================================ host side
 static int ceil_div(int64_t a, int64_t b) { return int((a + b - 1) / b); }
 
-// Pick the number of splits of the contraction for `tiles` tiles over `sms`
-// SMs: the best fraction of busy SMs in the last wave, each split keeping at
-// least min_chunks chunks.
-static int pick_splits(int tiles, int sms, int nchunks, int min_chunks, int max_splits) {
-  int best = 1;
-  double best_eff = -1.0;
-  for (int s = 1; s <= max_splits; ++s) {
-    if (s > 1 && ceil_div(nchunks, s) < min_chunks) break;
-    const int per = ceil_div(nchunks, s);
-    const int real = ceil_div(nchunks, per);
-    const int units = tiles * real;
-    const int waves = ceil_div(units, sms);
-    const double eff = double(units) / double(waves * sms);
-    if (eff > best_eff + 0.02) {
-      best_eff = eff;
-      best = real;
-    }
-  }
-  return best;
+// Stream-K grid for `total` chunks: every SM gets an equal share unless that
+// would leave a CTA fewer than `min_chunks` chunks to amortise its drain.
+static int stream_k_ctas(int64_t total, int sms, int min_chunks) {
+  int64_t g = (total + min_chunks - 1) / min_chunks;
+  if (g > sms) g = sms;
+  return g < 1 ? 1 : int(g);
+}
+
+// True when some CTA's range starts or ends inside a tile, i.e. some segment
+// covers only part of that tile's chunks.
+static bool has_partial_segment(int64_t total, int per, int ctas) {
+  for (int b = 0; b <= ctas; ++b)
+    if ((total * b / ctas) % per != 0) return true;
+  return false;
 }
 
 static SketchShape plan(int64_t n, int64_t d, int64_t k, int r, int sms) {
@@ -559,15 +586,13 @@ static SketchShape plan(int64_t n, int64_t d, int64_t k, int r, int sms) {
   P.tgroup = (r <= 256 && P.tiles > 1) ? 2 : 1;
   P.groups = ceil_div(P.tiles, P.tgroup);
   P.nchunks = ceil_div(k, kKc);
-  P.splits = pick_splits(P.groups, sms, P.nchunks, 8, 12);
-  P.chunks_per_split = ceil_div(P.nchunks, P.splits);
-  P.splits = ceil_div(P.nchunks, P.chunks_per_split);
+  const int64_t ptotal = int64_t(P.groups) * P.nchunks;
+  P.proj_ctas = stream_k_ctas(ptotal, sms, 8);
+  P.proj_partial = has_partial_segment(ptotal, P.nchunks, P.proj_ctas) ? 1 : 0;
   P.ntile_n = (P.r_pad <= 256) ? 256 : 128;
   P.dtiles = ceil_div(d, P.ntile_n);
   const int tchunks = P.n_pad / kChunk;
-  P.tsplits = pick_splits(P.dtiles, sms, tchunks, 8, 16);
-  P.tchunks_per_split = ceil_div(tchunks, P.tsplits);
-  P.tsplits = ceil_div(tchunks, P.tchunks_per_split);
+  P.acc_ctas = stream_k_ctas(int64_t(P.dtiles) * tchunks, sms, 12);
   // project: two sign-tile stages, the rest of shared memory for X tiles
   P.g_stages = 2;
   P.x_stages = (kSmemBudget - kStagingBytes - 2 * r * 128) / (P.tgroup * kTok * 128);
@@ -621,9 +646,9 @@ int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_
 
   const int proj_smem = proj_smem_bytes(P);
   LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(project_tc_kernel), proj_smem));
-  const int punits = P.groups * P.splits;
-  if (P.splits > 1) LOGRA_CUDA_TRY(cudaMemsetAsync(ppart, 0, part, s));   // the k-splits reduce-add into it
-  project_tc_kernel<<<punits < sms ? punits : sms, 512, proj_smem, s>>>(tx, tp, P, key, ctl);
+  // segments with a partial k range reduce-add into P^T, so it starts at zero
+  if (P.proj_partial) LOGRA_CUDA_TRY(cudaMemsetAsync(ppart, 0, part, s));
+  project_tc_kernel<<<P.proj_ctas, 512, proj_smem, s>>>(tx, tp, P, key, ctl);
   LOGRA_LAUNCHED();
 
   const int64_t stotal = int64_t(P.n_pad / kChunk) * P.r_pad * 4;
@@ -634,8 +659,7 @@ int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_
 
   const int acc_smem = acc_smem_bytes(P);
   LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(accumulate_tc_kernel), acc_smem));
-  const int aunits = P.dtiles * P.tsplits;
-  accumulate_tc_kernel<<<aunits < sms ? aunits : sms, 352, acc_smem, s>>>(tdy, ts, P, image, scale, ctl);
+  accumulate_tc_kernel<<<P.acc_ctas, 352, acc_smem, s>>>(tdy, ts, P, image, scale, ctl);
   LOGRA_LAUNCHED();
   return LOGRA_OK;
 }
