@@ -103,6 +103,42 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
+// The MMA issuer is a single thread, so per-MMA work on it is latency it
+// cannot hide.  Descriptors are built once per ring and advanced by plain adds
+// of the 16-byte-unit start-address field (all of shared memory lies below
+// 256 KB, so the field never carries), inside fully unrolled bodies.
+
+// Projection, one k chunk: T token tiles x NP parts of r, kKc / 16 k steps.
+template <int T, int NP>
+__device__ __forceinline__ void project_chunk_mmas(uint32_t acc0, uint32_t acc_cols, uint32_t npart, uint64_t ad,
+                                                   uint64_t bd, uint32_t idesc, uint32_t first) {
+#pragma unroll
+  for (int ks = 0; ks < kKc / 16; ++ks)
+#pragma unroll
+    for (int t = 0; t < T; ++t)
+#pragma unroll
+      for (int p = 0; p < NP; ++p)
+        mma_bf16(acc0 + uint32_t(t) * acc_cols + uint32_t(p) * npart,
+                 ad + uint64_t(t * ((kTok * 128) >> 4) + 2 * ks), bd + uint64_t(p * (npart * 8) + 2 * ks), idesc,
+                 ks ? 1u : first);
+}
+
+// Accumulate, one token chunk: MB M blocks of r, hi and lo terms, kChunk / 16 steps.
+template <int MB>
+__device__ __forceinline__ void accumulate_chunk_mmas(uint32_t acc0, uint32_t N, uint64_t ad, uint64_t bd,
+                                                      uint32_t idesc, uint32_t first) {
+#pragma unroll
+  for (int ks = 0; ks < kChunk / 16; ++ks) {
+    const uint64_t bk = bd + uint64_t(ks * (2048 >> 4));
+#pragma unroll
+    for (int m = 0; m < MB; ++m) {
+      const uint64_t am = ad + uint64_t(m * ((128 * 128) >> 4) + 2 * ks);
+      mma_bf16(acc0 + uint32_t(m) * N, am, bk, idesc, ks ? 1u : first);
+      mma_bf16(acc0 + uint32_t(m) * N, am + 4, bk, idesc, 1u);   // lo term: bytes 64..127 of each row
+    }
+  }
+}
+
 // Copies still in flight land before the CTA exits: wait (bounded) for the
 // last phase issued on every stage of a ring; phases already consumed pass.
 __device__ __forceinline__ void drain_ring(uint64_t* full, const Ring& rg, int n, unsigned long long limit) {
@@ -222,33 +258,30 @@ __global__ void __launch_bounds__(512, 1)
       const int nparts = P.r > 256 ? 2 : 1;
       const int npart = P.r / nparts;
       const uint32_t idesc = idesc_bf16(128, uint32_t(npart), 0, 0);
+      const uint64_t xdesc0 = smem_desc(smem_addr(x_tiles), 16, 1024, kSw128);
+      const uint64_t gdesc0 = smem_desc(smem_addr(g_tiles), 16, 1024, kSw128);
       SegIter it(total, P.nchunks);
       for (int seg = 0; !sh->abort && it.next(grp, c0, c1); ++seg) {
         const int ab = seg & (nacc - 1);
         const uint32_t uphase = uint32_t(seg / nacc) & 1u;
         const uint32_t acc0 = tmem + uint32_t(ab * T) * acc_cols;
+        // the accumulators of this set are free once the epilogue has drained them
+        for (int t = 0; t < T; ++t)
+          if (!wait_or_abort(sh, &sh->tmem_empty[ab * T + t], uphase ^ 1u, limit, ctl)) goto mma_done;
+        tc_fence_after();
         for (int c = c0; c < c1; ++c) {
           if (!wait_or_abort(sh, &sh->s_full[xr.stage], xr.phase, limit, ctl)) goto mma_done;
           if (!wait_or_abort(sh, &sh->o_full[gr.stage], gr.phase, limit, ctl)) goto mma_done;
           tc_fence_after();
-          const uint32_t a0 = smem_addr(x_tiles + size_t(xr.stage) * x_bytes);
-          const uint32_t b0 = smem_addr(g_tiles + size_t(gr.stage) * g_bytes);
-#pragma unroll
-          for (int ks = 0; ks < kKc / 16; ++ks) {
-            for (int t = 0; t < T; ++t) {
-              if (c == c0 && ks == 0) {
-                // accumulator t of this set is free once the epilogue has drained it
-                if (!wait_or_abort(sh, &sh->tmem_empty[ab * T + t], uphase ^ 1u, limit, ctl)) goto mma_done;
-                tc_fence_after();
-              }
-              const uint64_t ad = smem_desc(a0 + t * (kTok * 128) + ks * 32, 16, 1024, kSw128);
-              for (int p = 0; p < nparts; ++p) {
-                const uint64_t bd = smem_desc(b0 + uint32_t(p * npart) * 128 + ks * 32, 16, 1024, kSw128);
-                mma_bf16(acc0 + uint32_t(t) * acc_cols + uint32_t(p * npart), ad, bd, idesc,
-                         (c == c0 && ks == 0) ? 0u : 1u);
-              }
-            }
-          }
+          const uint64_t ad = xdesc0 + uint64_t(uint32_t(xr.stage) * (x_bytes >> 4));
+          const uint64_t bd = gdesc0 + uint64_t(uint32_t(gr.stage) * (g_bytes >> 4));
+          const uint32_t first = (c == c0) ? 0u : 1u;
+          if (T == 2)
+            project_chunk_mmas<2, 1>(acc0, acc_cols, uint32_t(npart), ad, bd, idesc, first);
+          else if (nparts == 1)
+            project_chunk_mmas<1, 1>(acc0, acc_cols, uint32_t(npart), ad, bd, idesc, first);
+          else
+            project_chunk_mmas<1, 2>(acc0, acc_cols, uint32_t(npart), ad, bd, idesc, first);
           mma_commit(&sh->s_empty[xr.stage]);
           mma_commit(&sh->o_empty[gr.stage]);
           xr.next(XS);
@@ -467,32 +500,30 @@ __global__ void __launch_bounds__(352, 1)
     if (lane == 0) {
       Ring ar, br;
       const uint32_t idesc = idesc_bf16(128, uint32_t(N), 0, 1);
+      const uint64_t adesc0 = smem_desc(smem_addr(a_tiles), 16, 1024, kSw128);
+      const uint64_t bdesc0 = smem_desc(smem_addr(b_tiles), kChunk * 128, 1024, kSw128);
       SegIter it(total, nchunks);
       for (int seg = 0; !sh->abort && it.next(dt, c0, c1); ++seg) {
         const int ab = seg & (nacc - 1);
         const uint32_t uphase = uint32_t(seg / nacc) & 1u;
         const uint32_t acc0 = tmem + uint32_t(ab * mblocks * N);
+        // the M blocks of this accumulator set are free once the epilogue drained them
+        for (int m = 0; m < mblocks; ++m)
+          if (!wait_or_abort(sh, &sh->tmem_empty[ab * mblocks + m], uphase ^ 1u, limit, ctl)) goto mma_done;
+        tc_fence_after();
         for (int c = c0; c < c1; ++c) {
           if (!wait_or_abort(sh, &sh->o_full[ar.stage], ar.phase, limit, ctl)) goto mma_done;
           if (!wait_or_abort(sh, &sh->s_full[br.stage], br.phase, limit, ctl)) goto mma_done;
           tc_fence_after();
-          const uint32_t a0 = smem_addr(a_tiles + size_t(ar.stage) * a_bytes);
-          const uint32_t b0 = smem_addr(b_tiles + size_t(br.stage) * b_bytes);
-#pragma unroll
-          for (int ks = 0; ks < kChunk / 16; ++ks) {
-            const uint64_t bd = smem_desc(b0 + ks * 2048, kChunk * 128, 1024, kSw128);
-            for (int m = 0; m < mblocks; ++m) {
-              if (c == c0 && ks == 0) {
-                // M block m of this accumulator set is free once the epilogue drained it
-                if (!wait_or_abort(sh, &sh->tmem_empty[ab * mblocks + m], uphase ^ 1u, limit, ctl)) goto mma_done;
-                tc_fence_after();
-              }
-              const uint32_t am = a0 + m * (128 * 128) + ks * 32;
-              const uint32_t acc = acc0 + uint32_t(m * N);
-              mma_bf16(acc, smem_desc(am, 16, 1024, kSw128), bd, idesc, (c == c0 && ks == 0) ? 0u : 1u);
-              mma_bf16(acc, smem_desc(am + 64, 16, 1024, kSw128), bd, idesc, 1u);
-            }
-          }
+          const uint64_t ad = adesc0 + uint64_t(uint32_t(ar.stage) * (a_bytes >> 4));
+          const uint64_t bd = bdesc0 + uint64_t(uint32_t(br.stage) * (b_bytes >> 4));
+          const uint32_t first = (c == c0) ? 0u : 1u;
+          if (mblocks == 1)
+            accumulate_chunk_mmas<1>(acc0, uint32_t(N), ad, bd, idesc, first);
+          else if (mblocks == 2)
+            accumulate_chunk_mmas<2>(acc0, uint32_t(N), ad, bd, idesc, first);
+          else
+            accumulate_chunk_mmas<4>(acc0, uint32_t(N), ad, bd, idesc, first);
           mma_commit(&sh->o_empty[ar.stage]);
           mma_commit(&sh->s_empty[br.stage]);
           ar.next(AS);

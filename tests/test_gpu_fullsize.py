@@ -75,7 +75,9 @@ def test_fullsize_sampled_sketch_and_apply(L, label, d, k, r, mbs, mask):
     assert rel(Wr, dW_or) <= TOL_ROW
     # properties at any size: ||S||^2 is the norm of the kernel's S; the bf16 copy is RN(W)
     nr = norms.cpu().numpy()
-    assert abs(nr[0] - float(np.sum(Sg * Sg))) <= 1e-9 * nr[0]
+    # the kernel sums squares of S in fp32 over 32-column blocks, then in fp64:
+    # worst-case relative error 32 * 2^-24 (~1.9e-6), inside the 1e-5 norm tolerance
+    assert abs(nr[0] - float(np.sum(Sg * Sg))) <= 2e-6 * nr[0]
     assert torch.equal(Wb, W.to(torch.bfloat16))
     # ||dW||^2 identity: (lr c)^2 sum_i k m_i / (v_i + eps), with m_i from the kernel's v
     vg = v.double().cpu().numpy()
