@@ -624,9 +624,12 @@ static SketchShape plan(int64_t n, int64_t d, int64_t k, int r, int sms) {
   P.dtiles = ceil_div(d, P.ntile_n);
   const int tchunks = P.n_pad / kChunk;
   P.acc_ctas = stream_k_ctas(int64_t(P.dtiles) * tchunks, sms, 12);
-  // project: two sign-tile stages, the rest of shared memory for X tiles
-  P.g_stages = 2;
-  P.x_stages = (kSmemBudget - kStagingBytes - 2 * r * 128) / (P.tgroup * kTok * 128);
+  // project: three sign-tile stages when three X stages still fit beside
+  // them (the generators then have a whole chunk of MMA time of slack), else
+  // two; the rest of shared memory for X tiles
+  const int x_bytes = P.tgroup * kTok * 128;
+  P.g_stages = (kSmemBudget - kStagingBytes - 3 * r * 128) / x_bytes >= 3 ? 3 : 2;
+  P.x_stages = (kSmemBudget - kStagingBytes - P.g_stages * r * 128) / x_bytes;
   if (P.x_stages > kMaxStages) P.x_stages = kMaxStages;
   // accumulate: P^T chunks come from L2 (three stages), dY from HBM (the rest)
   const int a_bytes = P.r_pad * 128, b_bytes = P.ntile_n * kChunk * 2;
