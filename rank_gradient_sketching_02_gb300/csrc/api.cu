@@ -54,6 +54,7 @@ int g_sm_count[kMaxDevices] = {};
 struct Buffer {
   void* ptr = nullptr;
   size_t bytes = 0;
+  unsigned* counters = nullptr;   // 64 zero-initialised words, never freed while the stream's entry lives
 };
 std::map<std::pair<int, cudaStream_t>, Buffer> g_ws;
 
@@ -120,6 +121,26 @@ void* workspace(cudaStream_t stream, size_t bytes, int* status) {
     b.bytes = want;
   }
   return b.ptr;
+}
+
+unsigned* stream_counter(cudaStream_t stream, int* status) {
+  *status = LOGRA_OK;
+  int dev;
+  if ((*status = current_device(&dev))) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  Buffer& b = g_ws[std::make_pair(dev, stream)];
+  if (!b.counters) {
+    void* p = nullptr;
+    cudaError_t e = cudaMalloc(&p, 64 * sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, 64 * sizeof(unsigned), stream);   // ordered before its first user
+    if (e != cudaSuccess) {
+      if (p) cudaFree(p);
+      *status = cuda_fail(e);
+      return nullptr;
+    }
+    b.counters = static_cast<unsigned*>(p);
+  }
+  return b.counters;
 }
 
 int make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, uint32_t elem_bytes, uint64_t inner,

@@ -116,6 +116,10 @@ struct ApplyArgs {
   float* inv;                 // d values 1/sqrt(v_i + eps)
   float* sync_out;
   double* part;               // one per CTA
+  double* norms;              // modes 0, 1 (nullable): {||S||^2, ||dW||^2} from the last CTA
+  const double* ssq;          // mode 4's ||S||^2 partials
+  int nssq;
+  unsigned* counter;          // CTAs finished, wrapping to 0 after the last one
 };
 
 template <int MODE>
@@ -415,6 +419,30 @@ __global__ void __launch_bounds__(352, 1)
     epi_sync();
     if (et == 0 && (MODE == 0 || MODE == 1 || MODE == 4))
       A.part[blockIdx.x] = sh->red[0] + sh->red[1] + sh->red[2] + sh->red[3];
+    if ((MODE == 0 || MODE == 1) && A.norms && warp == 2) {
+      // The last CTA to finish sums every CTA's partial (and mode 4's) in a
+      // fixed order: deterministic, and no separate reduction launch.
+      unsigned prev = 0;
+      if (lane == 0) {
+        __threadfence();
+        prev = atomicInc(A.counter, gridDim.x - 1);
+      }
+      prev = __shfl_sync(0xffffffffu, prev, 0);
+      if (prev == gridDim.x - 1) {
+        __threadfence();
+        double a = 0.0, b = 0.0;
+        for (int i = lane; i < A.nssq; i += 32) a += __ldcg(A.ssq + i);
+        for (int i = lane; i < int(gridDim.x); i += 32) b += __ldcg(A.part + i);
+        for (int o = 16; o; o >>= 1) {
+          a += __shfl_xor_sync(0xffffffffu, a, o);
+          b += __shfl_xor_sync(0xffffffffu, b, o);
+        }
+        if (lane == 0) {
+          A.norms[0] = a;
+          A.norms[1] = b;
+        }
+      }
+    }
   } else if (warp < 10) {
     // ------------------------------------------------------------------ sign-tile generators (MN-major)
     if (!kNorm) {
@@ -455,36 +483,51 @@ __global__ void __launch_bounds__(352, 1)
 }
 
 // S image for the A operand: rows split into bf16 hi + lo, 64-rank chunks of
-// 128-byte rows, 16-byte chunk q of row i stored at q ^ (i & 7).
-__global__ void s_image_kernel(const float* __restrict__ S, int64_t d, int r, uint8_t* __restrict__ img) {
+// 128-byte rows, 16-byte chunk q of row i stored at q ^ (i & 7).  Element e
+// is one (row, chunk, 8-rank group).
+__device__ __forceinline__ void s_image_elem(const float* __restrict__ S, int64_t d, int r, int nchunks,
+                                             uint8_t* __restrict__ img, int64_t e) {
+  const int q = int(e & 7);
+  const int c = int((e >> 3) % nchunks);
+  const int64_t row = (e >> 3) / nchunks;
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int a = c * kRc + q * 8 + i;
+    v[i] = (row < d && a < r) ? S[row * r + a] : 0.f;
+  }
+  uint32_t hi[4], lo[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * i]), h1 = __float2bfloat16_rn(v[2 * i + 1]);
+    const __nv_bfloat16 l0 = __float2bfloat16_rn(v[2 * i] - __bfloat162float(h0));
+    const __nv_bfloat16 l1 = __float2bfloat16_rn(v[2 * i + 1] - __bfloat162float(h1));
+    hi[i] = uint32_t(__bfloat16_as_ushort(h0)) | (uint32_t(__bfloat16_as_ushort(h1)) << 16);
+    lo[i] = uint32_t(__bfloat16_as_ushort(l0)) | (uint32_t(__bfloat16_as_ushort(l1)) << 16);
+  }
+  const int64_t rb = row / kRows;
+  const int rl = int(row % kRows);
+  uint8_t* chunk = img + (size_t(rb) * nchunks + c) * kABytes;
+  const int off = rl * 128 + ((q ^ (rl & 7)) << 4);
+  *reinterpret_cast<uint4*>(chunk + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+  *reinterpret_cast<uint4*>(chunk + kRows * 128 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+}
+
+// The apply's preparation in one launch: sign words of A (words[i][w], w <
+// nw = ceil(k / 64); skipped when words is null) for the Gram matrix, then
+// the S image.  One grid-stride loop over both index ranges.
+__global__ void apply_prep_kernel(uint64_t key, int r, int nw, uint64_t* __restrict__ words,
+                                  const float* __restrict__ S, int64_t d, uint8_t* __restrict__ img) {
   const int nchunks = (r + kRc - 1) / kRc;
-  const int64_t rows_pad = ((d + kRows - 1) / kRows) * kRows;
-  const int64_t total = rows_pad * nchunks * 8;   // one thread per (row, chunk, 8-rank group)
+  const int64_t nwords = words ? int64_t(r) * nw : 0;
+  const int64_t total = nwords + ((d + kRows - 1) / kRows) * kRows * nchunks * 8;
   for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total; e += int64_t(gridDim.x) * blockDim.x) {
-    const int q = int(e & 7);
-    const int c = int((e >> 3) % nchunks);
-    const int64_t row = (e >> 3) / nchunks;
-    float v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int a = c * kRc + q * 8 + i;
-      v[i] = (row < d && a < r) ? S[row * r + a] : 0.f;
+    if (e < nwords) {
+      const int i = int(e / nw), w = int(e - int64_t(i) * nw);
+      words[e] = sign_word(key, uint32_t(i), uint32_t(w));
+    } else {
+      s_image_elem(S, d, r, nchunks, img, e - nwords);
     }
-    uint32_t hi[4], lo[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * i]), h1 = __float2bfloat16_rn(v[2 * i + 1]);
-      const __nv_bfloat16 l0 = __float2bfloat16_rn(v[2 * i] - __bfloat162float(h0));
-      const __nv_bfloat16 l1 = __float2bfloat16_rn(v[2 * i + 1] - __bfloat162float(h1));
-      hi[i] = uint32_t(__bfloat16_as_ushort(h0)) | (uint32_t(__bfloat16_as_ushort(h1)) << 16);
-      lo[i] = uint32_t(__bfloat16_as_ushort(l0)) | (uint32_t(__bfloat16_as_ushort(l1)) << 16);
-    }
-    const int64_t rb = row / kRows;
-    const int rl = int(row % kRows);
-    uint8_t* chunk = img + (size_t(rb) * nchunks + c) * kABytes;
-    const int off = rl * 128 + ((q ^ (rl & 7)) << 4);
-    *reinterpret_cast<uint4*>(chunk + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    *reinterpret_cast<uint4*>(chunk + kRows * 128 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
   }
 }
 
@@ -494,12 +537,14 @@ size_t s_image_bytes(int64_t d, int r) {
   return size_t(rb) * nchunks * kABytes;
 }
 
-int launch_s_image(const float* S, int64_t d, int r, uint8_t* img, cudaStream_t s) {
+int launch_apply_prep(uint64_t key, int r, int64_t k, uint64_t* words, const float* S, int64_t d, uint8_t* img,
+                      cudaStream_t s) {
   const int nchunks = (r + kRc - 1) / kRc;
-  const int64_t total = ((d + kRows - 1) / kRows) * kRows * nchunks * 8;
+  const int nw = int((k + 63) / 64);
+  const int64_t total = (words ? int64_t(r) * nw : 0) + ((d + kRows - 1) / kRows) * kRows * nchunks * 8;
   int64_t blocks = (total + 255) / 256;
   if (blocks > int64_t(sm_count()) * 8) blocks = int64_t(sm_count()) * 8;
-  s_image_kernel<<<unsigned(blocks), 256, 0, s>>>(S, d, r, img);
+  apply_prep_kernel<<<unsigned(blocks), 256, 0, s>>>(key, r, nw, words, S, d, img);
   LOGRA_LAUNCHED();
   return LOGRA_OK;
 }
@@ -530,6 +575,10 @@ int launch_apply_tc(const ApplyLaunch& L, int* grid_out, Control* ctl, cudaStrea
   A.write_bf16 = (mode == 0 && L.Wb) ? 1 : 0;
   A.s_image = L.s_img;
   A.m_image = L.m_img;
+  A.norms = (mode == 0 || mode == 1) ? L.norms : nullptr;
+  A.ssq = L.ssq;
+  A.nssq = L.nssq;
+  A.counter = L.counter;
   A.S = L.S;
   A.v_in = L.v_in;
   A.v_out = L.v_out;

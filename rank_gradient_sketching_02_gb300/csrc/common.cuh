@@ -53,6 +53,9 @@ __device__ __forceinline__ void record_status(Control* ctl, int code) {
 
 Control* control_block(int* status);                     // current device
 void* workspace(cudaStream_t stream, size_t bytes, int* status);
+// A few zero-initialised counters per (device, stream) for in-kernel
+// last-CTA detection; every user leaves them at zero.
+unsigned* stream_counter(cudaStream_t stream, int* status);
 int sm_count();
 int cuda_fail(cudaError_t e);
 void count_launch();

@@ -11,14 +11,15 @@ namespace logra {
 struct Control;
 
 struct ApplyWorkspace {
-  size_t words_off, counts_off, gram_off, inv_off, ssq_off, dw2_off, img_off, bytes;
+  size_t words_off, gram_off, inv_off, ssq_off, dw2_off, img_off, bytes;
 };
 
 ApplyWorkspace apply_workspace_layout(int64_t d, int64_t k, int r);
 
 int launch_sign_matrix(uint64_t key, int r, int64_t k, float scale, float* A, cudaStream_t s);
 size_t gram_image_bytes(int r);
-int launch_gram(uint64_t key, int r, int64_t k, uint64_t* words, int* counts, uint8_t* img, cudaStream_t s);
+// M = Sigma Sigma^T image from the packed sign words (written by launch_apply_prep).
+int launch_gram(const uint64_t* words, int r, int64_t k, uint8_t* img, cudaStream_t s);
 
 int launch_sketch_simt(const void* X, const void* dY, int dtype, int64_t n, int64_t d, int64_t k, int r,
                        uint64_t key, float scale, float* S, float* P, cudaStream_t s);
@@ -28,7 +29,10 @@ int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_
                      float scale, float* S, void* ws, Control* ctl, cudaStream_t s);
 
 size_t s_image_bytes(int64_t d, int r);
-int launch_s_image(const float* S, int64_t d, int r, uint8_t* img, cudaStream_t s);
+// One launch: the S image (A operand of the apply) and, when `words` is not
+// null, the packed sign words of A for the Gram matrix.
+int launch_apply_prep(uint64_t key, int r, int64_t k, uint64_t* words, const float* S, int64_t d, uint8_t* img,
+                      cudaStream_t s);
 // The tensor-core kernel behind the apply: mode 0 apply, 1 predict (dW^2 only),
 // 2 rebuild fp32, 3 rebuild bf16, 4 row norms (v, 1/sqrt(v+eps), sync sketch,
 // ||S||^2 partials) from the Gram image.
@@ -51,6 +55,11 @@ struct ApplyLaunch {
   float* sync_out;          // mode 4 (nullable)
   float beta2, eps;
   double* part;             // per-CTA partials: dW^2 (modes 0, 1) or ||S||^2 (mode 4)
+  // modes 0, 1: the last CTA to finish sums the partials into norms[0..1]
+  double* norms;            // nullable
+  const double* ssq;        // mode 4's ||S||^2 partials
+  int nssq;
+  unsigned* counter;        // per-stream, zero between launches
 };
 int launch_apply_tc(const ApplyLaunch& L, int* grid_out, Control* ctl, cudaStream_t s);
 

@@ -1,44 +1,22 @@
-// One RowAdam apply (or predict, or reconstruct) as a sequence of launches,
-// and the fixed-order fp64 reduction of its norms.
+// One RowAdam apply (or predict, or reconstruct) as a short sequence of
+// launches.
 //
 // apply / predict (theclarity.today write-up, "What happened": running
 // estimates of squared row magnitudes, no first moment):
-//   1. sign words of A for this (seed, step); M = Sigma Sigma^T from popcounts,
-//      stored as an exact bf16 hi + lo image                     (sign.cu)
-//   2. S split into bf16 hi + lo, pre-swizzled                    (apply_tc.cu)
+//   1. sign words of A for this (seed, step) and S split into bf16 hi + lo,
+//      pre-swizzled, in one launch                                (apply_tc.cu)
+//   2. M = Sigma Sigma^T from popcounts, stored as an exact bf16 hi + lo
+//      image                                                      (sign.cu)
 //   3. row norms on the tensor cores: q_i = S_i M S_i^T = r ||(S A)_i||^2,
 //      v_i <- beta2 v_i + (1 - beta2) q_i / (r k), 1/sqrt(v_i + eps),
 //      optional sync sketch, ||S||^2 partials                     (mode 4)
-//   4. W += -lr c (S A) / (sqrt(r) sqrt(v + eps)), tile by tile   (mode 0; 1 = dW^2 only)
-//   5. norms = {||S||^2, ||dW||^2}                                 (norms_kernel)
-// reconstruct: steps 2 and 4 with a plain (or accumulating) store epilogue.
+//   4. W += -lr c (S A) / (sqrt(r) sqrt(v + eps)), tile by tile   (mode 0; 1 = dW^2 only);
+//      its last CTA sums the partials into {||S||^2, ||dW||^2} in a fixed order
+// reconstruct: steps 1 (S image only) and 4 with a plain (or accumulating) store epilogue.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace logra {
-
-// norms[0] = sum ssq_part, norms[1] = sum dw2_part (fixed order, one block).
-__global__ void norms_kernel(const double* __restrict__ ssq, int nssq, const double* __restrict__ dw2, int ndw2,
-                             double* __restrict__ norms) {
-  __shared__ double red[2][256];
-  double a = 0.0, b = 0.0;
-  for (int e = threadIdx.x; e < nssq; e += 256) a += ssq[e];
-  for (int e = threadIdx.x; e < ndw2; e += 256) b += dw2[e];
-  red[0][threadIdx.x] = a;
-  red[1][threadIdx.x] = b;
-  __syncthreads();
-  for (int o = 128; o; o >>= 1) {
-    if (threadIdx.x < o) {
-      red[0][threadIdx.x] += red[0][threadIdx.x + o];
-      red[1][threadIdx.x] += red[1][threadIdx.x + o];
-    }
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    norms[0] = red[0][0];
-    norms[1] = red[1][0];
-  }
-}
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -47,7 +25,6 @@ ApplyWorkspace apply_workspace_layout(int64_t d, int64_t k, int r) {
   const int64_t nw = (k + 63) / 64;
   size_t off = 0;
   w.words_off = off;   off += align256(size_t(r) * nw * 8);
-  w.counts_off = off;  off += align256(size_t(r) * r * 4);
   w.gram_off = off;    off += align256(gram_image_bytes(r));
   w.inv_off = off;     off += align256(size_t(d) * 4);
   w.ssq_off = off;     off += align256(size_t(1024) * 8);
@@ -66,16 +43,22 @@ int launch_rowadam(int mode, float* W, __nv_bfloat16* Wb, void* out, int accumul
   double* dw2 = reinterpret_cast<double*>(ws + WL.dw2_off);
   uint8_t* img = reinterpret_cast<uint8_t*>(ws + WL.img_off);
   uint8_t* mimg = reinterpret_cast<uint8_t*>(ws + WL.gram_off);
-  if (int st = launch_s_image(S, d, r, img, s)) return st;
+  const bool rownorms = (mode == 0 || mode == 1);
+  uint64_t* words = rownorms ? reinterpret_cast<uint64_t*>(ws + WL.words_off) : nullptr;
+  unsigned* counter = nullptr;
+  if (rownorms && norms) {
+    int st = 0;
+    counter = stream_counter(s, &st);
+    if (st) return st;
+  }
+  if (int st = launch_apply_prep(key, r, k, words, S, d, img, s)) return st;
 
   ApplyLaunch L{};
   L.d = d; L.k = k; L.r = r; L.key = key; L.neg_lrc = -lrc;
   L.s_img = img; L.m_img = mimg; L.S = S; L.inv = inv; L.beta2 = beta2; L.eps = eps;
   int grid_norm = 0, grid_upd = 0;
-  if (mode == 0 || mode == 1) {
-    uint64_t* words = reinterpret_cast<uint64_t*>(ws + WL.words_off);
-    int* counts = reinterpret_cast<int*>(ws + WL.counts_off);
-    if (int st = launch_gram(key, r, k, words, counts, mimg, s)) return st;
+  if (rownorms) {
+    if (int st = launch_gram(words, r, k, mimg, s)) return st;
     L.mode = 4;
     L.v_in = v_in;
     L.v_out = v_out;
@@ -87,11 +70,11 @@ int launch_rowadam(int mode, float* W, __nv_bfloat16* Wb, void* out, int accumul
   L.W = W; L.Wb = Wb; L.out = out; L.accumulate = accumulate;
   L.v_in = nullptr; L.v_out = nullptr; L.sync_out = nullptr;
   L.part = dw2;
+  L.norms = norms;
+  L.ssq = ssq;
+  L.nssq = grid_norm;
+  L.counter = counter;
   if (int st = launch_apply_tc(L, &grid_upd, ctl, s)) return st;
-  if ((mode == 0 || mode == 1) && norms) {
-    norms_kernel<<<1, 256, 0, s>>>(ssq, grid_norm, dw2, grid_upd, norms);
-    LOGRA_LAUNCHED();
-  }
   return LOGRA_OK;
 }
 
