@@ -54,7 +54,7 @@ int g_sm_count[kMaxDevices] = {};
 struct Buffer {
   void* ptr = nullptr;
   size_t bytes = 0;
-  unsigned* counters = nullptr;   // 64 zero-initialised words, never freed while the stream's entry lives
+  unsigned* counters = nullptr;   // kCounterWords zero-initialised words, never freed while the stream's entry lives
 };
 std::map<std::pair<int, cudaStream_t>, Buffer> g_ws;
 
@@ -131,8 +131,8 @@ unsigned* stream_counter(cudaStream_t stream, int* status) {
   Buffer& b = g_ws[std::make_pair(dev, stream)];
   if (!b.counters) {
     void* p = nullptr;
-    cudaError_t e = cudaMalloc(&p, 64 * sizeof(unsigned));
-    if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, 64 * sizeof(unsigned), stream);   // ordered before its first user
+    cudaError_t e = cudaMalloc(&p, kCounterWords * sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, kCounterWords * sizeof(unsigned), stream);   // ordered before its first user
     if (e != cudaSuccess) {
       if (p) cudaFree(p);
       *status = cuda_fail(e);

@@ -23,9 +23,10 @@
 // Operands: A = the row block of S, pre-split into bf16 hi/lo and pre-swizzled
 // (one bulk copy per 64-wide rank chunk); B = Sigma rows of that chunk for the
 // super-tile's 256 columns, MN-major, generated in shared memory from the sign
-// hash (mode 4: the M image by bulk copy).  W (and its bf16 copy) move by TMA
-// in 128 x 32 sub-tiles; one store group stays in flight while the next
-// sub-tile is computed.
+// hash (mode 4: the M image by bulk copy).  W moves in by TMA in 128 x 32
+// sub-tiles; each epilogue warp updates its 32-row slice in place and stores
+// it (and its bf16 copy) by TMA on its own, keeping one store group in flight
+// while it computes the next slice, so the four warps never wait on each other.
 //
 // Roles: warp 0 = A (and mode-4 B) producer, warp 1 = TMEM owner + MMA issuer,
 // warps 2..5 = epilogue (TMEM lane quadrant = warp % 4), warps 6..9 = sign-tile
@@ -73,20 +74,6 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// Wait taken by the whole 128-thread epilogue group with one verdict: one
-// thread waits (bounded), the group synchronises, every thread then observes
-// the completed phase itself.  Uniform verdicts keep the group's named
-// barriers matched even when a wait gives up.
-__device__ __forceinline__ bool group_wait(ApplyShared* sh, uint64_t* bar, uint32_t parity,
-                                           unsigned long long limit, Control* ctl, int et) {
-  if (et == 0) sh->flag = wait_or_abort(sh, bar, parity, limit, ctl) ? 1 : 0;
-  epi_sync();
-  const int ok = *reinterpret_cast<volatile int*>(&sh->flag);
-  epi_sync();
-  if (ok) (void)mbar_try_wait(bar, parity);
-  return ok != 0;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
          (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
@@ -125,6 +112,7 @@ struct ApplyArgs {
 template <int MODE>
 __global__ void __launch_bounds__(352, 1)
     apply_tc_kernel(const __grid_constant__ CUtensorMap tmap_f32, const __grid_constant__ CUtensorMap tmap_b16,
+                    const __grid_constant__ CUtensorMap tmap_f32s, const __grid_constant__ CUtensorMap tmap_b16s,
                     ApplyArgs A, Control* ctl) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
@@ -146,7 +134,7 @@ __global__ void __launch_bounds__(352, 1)
     }
     for (int s = 0; s < kWStages; ++s) {
       mbar_init(&sh->w_full[s], 1);
-      mbar_init(&sh->w_empty[s], 1);
+      mbar_init(&sh->w_empty[s], 4);   // one release per epilogue warp
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh->tmem_full[b], 1);
@@ -155,8 +143,14 @@ __global__ void __launch_bounds__(352, 1)
     mbar_init(&sh->drain, 1);
     sh->abort = 0;
     fence_mbar_init();
-    if (MODE == 0 || MODE == 2) prefetch_tmap(&tmap_f32);
-    if ((MODE == 0 && A.write_bf16) || MODE == 3) prefetch_tmap(&tmap_b16);
+    if (MODE == 0 || MODE == 2) {
+      prefetch_tmap(&tmap_f32);
+      prefetch_tmap(&tmap_f32s);
+    }
+    if ((MODE == 0 && A.write_bf16) || MODE == 3) {
+      prefetch_tmap(&tmap_b16);
+      prefetch_tmap(&tmap_b16s);
+    }
   }
   if (warp == 1) {
     tmem_alloc(&sh->tmem_base, 512);
@@ -276,7 +270,7 @@ __global__ void __launch_bounds__(352, 1)
       double q = 0.0;                                    // mode 4: S_i M S_i^T over the row
       for (int t = 0; t < A.inner && !aborted; ++t) {
         const int st = kNorm ? t : u % A.nsuper;
-        if (!group_wait(sh, &sh->tmem_full[buf], tph[buf], limit, ctl, et)) { aborted = true; break; }
+        if (!warp_wait(sh, &sh->tmem_full[buf], tph[buf], limit, ctl)) { aborted = true; break; }
         tph[buf] ^= 1u;
         tc_fence_after();
         float f = 0.f;
@@ -323,34 +317,45 @@ __global__ void __launch_bounds__(352, 1)
           uint8_t* wt = wr + wstage * kWBytes;
           uint8_t* ht = hb + (sub & 1) * kHBytes;
           if (load_in) {
-            if (!group_wait(sh, &sh->w_full[wstage], wphase, limit, ctl, et)) { aborted = true; break; }
+            if (!warp_wait(sh, &sh->w_full[wstage], wphase, limit, ctl)) { aborted = true; break; }
           }
           if (MODE == 0 || MODE == 2) {
             // fp32 sub-tile, 128-byte rows, 16-byte chunk q at q ^ (row & 7)
-            float acc = 0.f;
+            // all eight 16-byte loads first, then the arithmetic, then the
+            // stores: in-place stores would otherwise keep the compiler from
+            // issuing the next load early, and one warp per scheduler cannot
+            // hide a shared-memory round trip per step
             uint8_t* rowp = wt + row_l * 128;
+            float4 w[8];
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+              w[q4] = load_in ? *reinterpret_cast<const float4*>(rowp + ((q4 ^ (row_l & 7)) << 4))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
-              float4* p = reinterpret_cast<float4*>(rowp + ((q4 ^ (row_l & 7)) << 4));
-              float4 w = load_in ? *p : make_float4(0.f, 0.f, 0.f, 0.f);
               const float d0 = f * __uint_as_float(g[4 * q4 + 0]), d1 = f * __uint_as_float(g[4 * q4 + 1]);
               const float d2 = f * __uint_as_float(g[4 * q4 + 2]), d3 = f * __uint_as_float(g[4 * q4 + 3]);
               if (MODE == 0) {
-                if (4 * q4 + 0 < ncol) acc = fmaf(d0, d0, acc);
-                if (4 * q4 + 1 < ncol) acc = fmaf(d1, d1, acc);
-                if (4 * q4 + 2 < ncol) acc = fmaf(d2, d2, acc);
-                if (4 * q4 + 3 < ncol) acc = fmaf(d3, d3, acc);
+                if (4 * q4 + 0 < ncol) acc[0] = fmaf(d0, d0, acc[0]);
+                if (4 * q4 + 1 < ncol) acc[1] = fmaf(d1, d1, acc[1]);
+                if (4 * q4 + 2 < ncol) acc[2] = fmaf(d2, d2, acc[2]);
+                if (4 * q4 + 3 < ncol) acc[3] = fmaf(d3, d3, acc[3]);
               }
-              w.x += d0; w.y += d1; w.z += d2; w.w += d3;
-              *p = w;
-              if (MODE == 0 && A.write_bf16) {
-                // bf16 staging: 64-byte rows, 16-byte chunk h at h ^ ((row >> 1) & 3)
-                const int h = q4 >> 1;
-                *reinterpret_cast<uint2*>(ht + row_l * 64 + ((h ^ ((row_l >> 1) & 3)) << 4) + (q4 & 1) * 8) =
-                    make_uint2(pack_bf16x2(w.x, w.y), pack_bf16x2(w.z, w.w));
-              }
+              w[q4].x += d0; w[q4].y += d1; w[q4].z += d2; w[q4].w += d3;
             }
-            if (MODE == 0 && row_ok) acc_cta += double(acc);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+              *reinterpret_cast<float4*>(rowp + ((q4 ^ (row_l & 7)) << 4)) = w[q4];
+            if (MODE == 0 && A.write_bf16) {
+              // bf16 staging: 64-byte rows, 16-byte chunk h at h ^ ((row >> 1) & 3)
+#pragma unroll
+              for (int h = 0; h < 4; ++h)
+                *reinterpret_cast<uint4*>(ht + row_l * 64 + ((h ^ ((row_l >> 1) & 3)) << 4)) =
+                    make_uint4(pack_bf16x2(w[2 * h].x, w[2 * h].y), pack_bf16x2(w[2 * h].z, w[2 * h].w),
+                               pack_bf16x2(w[2 * h + 1].x, w[2 * h + 1].y), pack_bf16x2(w[2 * h + 1].z, w[2 * h + 1].w));
+            }
+            if (MODE == 0 && row_ok) acc_cta += double((acc[0] + acc[1]) + (acc[2] + acc[3]));
           } else {
             // MODE 3: bf16 output sub-tile (64-byte rows) in the staging buffer
             const uint8_t* src = wt + row_l * 64;
@@ -369,18 +374,21 @@ __global__ void __launch_bounds__(352, 1)
               *reinterpret_cast<uint4*>(ht + row_l * 64 + off) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
             }
           }
+          // each warp stores its own 32-row slice, so the four epilogue warps
+          // run decoupled and a slice's store overlaps the warp's next sub-tile
           fence_proxy_async_smem();
-          epi_sync();
-          if (et == 0) {
-            if (MODE == 0 || MODE == 2) tma_store_2d(&tmap_f32, wt, int32_t(col0), rb * kRows);
-            if ((MODE == 0 && A.write_bf16) || MODE == 3) tma_store_2d(&tmap_b16, ht, int32_t(col0), rb * kRows);
+          __syncwarp();
+          if (lane == 0) {
+            const int32_t r0 = rb * kRows + quad * 32;
+            if (MODE == 0 || MODE == 2) tma_store_2d(&tmap_f32s, wt + quad * (32 * 128), int32_t(col0), r0);
+            if ((MODE == 0 && A.write_bf16) || MODE == 3) tma_store_2d(&tmap_b16s, ht + quad * (32 * 64), int32_t(col0), r0);
             bulk_commit();
-            // keep this sub-tile's stores in flight; once at most one group is
-            // outstanding, the previous sub-tile's stores have read their smem
+            // keep this slice's stores in flight; once at most one group is
+            // outstanding, the previous slice's stores have read their smem
             asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
             if (load_in && prev_stage >= 0) mbar_arrive(&sh->w_empty[prev_stage]);
           }
-          epi_sync();
+          __syncwarp();
           prev_stage = load_in ? wstage : -1;
           ++sub;
           if (load_in || MODE == 2) {
@@ -409,10 +417,11 @@ __global__ void __launch_bounds__(352, 1)
         }
       }
     }
-    if (et == 0) {
+    if (lane == 0) {
       bulk_wait_all();
       if (load_in && prev_stage >= 0 && !aborted) mbar_arrive(&sh->w_empty[prev_stage]);
     }
+    __syncwarp();
     // per-CTA partial sum, fixed order
     for (int o = 16; o; o >>= 1) acc_cta += __shfl_xor_sync(0xffffffffu, acc_cta, o);
     if (lane == 0) sh->red[quad] = acc_cta;
@@ -514,19 +523,22 @@ __device__ __forceinline__ void s_image_elem(const float* __restrict__ S, int64_
 }
 
 // The apply's preparation in one launch: sign words of A (words[i][w], w <
-// nw = ceil(k / 64); skipped when words is null) for the Gram matrix, then
-// the S image.  One grid-stride loop over both index ranges.
-__global__ void apply_prep_kernel(uint64_t key, int r, int nw, uint64_t* __restrict__ words,
+// nw = ceil(k / 64)) and zeroed Gram counts (both skipped when words is
+// null), then the S image.  One grid-stride loop over the three index ranges.
+__global__ void apply_prep_kernel(uint64_t key, int r, int nw, uint64_t* __restrict__ words, int* __restrict__ counts,
                                   const float* __restrict__ S, int64_t d, uint8_t* __restrict__ img) {
   const int nchunks = (r + kRc - 1) / kRc;
   const int64_t nwords = words ? int64_t(r) * nw : 0;
-  const int64_t total = nwords + ((d + kRows - 1) / kRows) * kRows * nchunks * 8;
+  const int64_t ncounts = words ? int64_t(r) * r : 0;
+  const int64_t total = nwords + ncounts + ((d + kRows - 1) / kRows) * kRows * nchunks * 8;
   for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total; e += int64_t(gridDim.x) * blockDim.x) {
     if (e < nwords) {
       const int i = int(e / nw), w = int(e - int64_t(i) * nw);
       words[e] = sign_word(key, uint32_t(i), uint32_t(w));
+    } else if (e < nwords + ncounts) {
+      counts[e - nwords] = 0;
     } else {
-      s_image_elem(S, d, r, nchunks, img, e - nwords);
+      s_image_elem(S, d, r, nchunks, img, e - nwords - ncounts);
     }
   }
 }
@@ -537,14 +549,14 @@ size_t s_image_bytes(int64_t d, int r) {
   return size_t(rb) * nchunks * kABytes;
 }
 
-int launch_apply_prep(uint64_t key, int r, int64_t k, uint64_t* words, const float* S, int64_t d, uint8_t* img,
-                      cudaStream_t s) {
+int launch_apply_prep(uint64_t key, int r, int64_t k, uint64_t* words, int* counts, const float* S, int64_t d,
+                      uint8_t* img, cudaStream_t s) {
   const int nchunks = (r + kRc - 1) / kRc;
   const int nw = int((k + 63) / 64);
-  const int64_t total = (words ? int64_t(r) * nw : 0) + ((d + kRows - 1) / kRows) * kRows * nchunks * 8;
+  const int64_t total = (words ? int64_t(r) * nw + int64_t(r) * r : 0) + ((d + kRows - 1) / kRows) * kRows * nchunks * 8;
   int64_t blocks = (total + 255) / 256;
   if (blocks > int64_t(sm_count()) * 8) blocks = int64_t(sm_count()) * 8;
-  apply_prep_kernel<<<unsigned(blocks), 256, 0, s>>>(key, r, nw, words, S, d, img);
+  apply_prep_kernel<<<unsigned(blocks), 256, 0, s>>>(key, r, nw, words, counts, S, d, img);
   LOGRA_LAUNCHED();
   return LOGRA_OK;
 }
@@ -585,11 +597,15 @@ int launch_apply_tc(const ApplyLaunch& L, int* grid_out, Control* ctl, cudaStrea
   A.inv = L.inv;
   A.sync_out = L.sync_out;
   A.part = L.part;
-  CUtensorMap t32{}, t16{};
+  // loads move 128-row sub-tiles; each epilogue warp stores its own 32-row slice
+  CUtensorMap t32{}, t16{}, t32s{}, t16s{};
   if (mode == 0 || mode == 2) {
     const void* p = mode == 0 ? static_cast<const void*>(L.W) : L.out;
     if (int st = make_tmap_2d(&t32, p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(L.k), uint64_t(L.d),
                               uint64_t(L.k) * 4, kSub, kRows, CU_TENSOR_MAP_SWIZZLE_128B))
+      return st;
+    if (int st = make_tmap_2d(&t32s, p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(L.k), uint64_t(L.d),
+                              uint64_t(L.k) * 4, kSub, 32, CU_TENSOR_MAP_SWIZZLE_128B))
       return st;
   }
   if ((mode == 0 && L.Wb) || mode == 3) {
@@ -597,12 +613,15 @@ int launch_apply_tc(const ApplyLaunch& L, int* grid_out, Control* ctl, cudaStrea
     if (int st = make_tmap_2d(&t16, p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, uint64_t(L.k), uint64_t(L.d),
                               uint64_t(L.k) * 2, kSub, kRows, CU_TENSOR_MAP_SWIZZLE_64B))
       return st;
+    if (int st = make_tmap_2d(&t16s, p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, uint64_t(L.k), uint64_t(L.d),
+                              uint64_t(L.k) * 2, kSub, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+      return st;
   }
   const int grid = A.units < sms ? A.units : sms;
   *grid_out = grid;
   auto run = [&](auto kern) -> int {
     LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(kern), int(kApplySmem)));
-    kern<<<grid, 352, kApplySmem, s>>>(t32, t16, A, ctl);
+    kern<<<grid, 352, kApplySmem, s>>>(t32, t16, t32s, t16s, A, ctl);
     LOGRA_LAUNCHED();
     return LOGRA_OK;
   };

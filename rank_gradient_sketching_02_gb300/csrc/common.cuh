@@ -55,6 +55,7 @@ Control* control_block(int* status);                     // current device
 void* workspace(cudaStream_t stream, size_t bytes, int* status);
 // A few zero-initialised counters per (device, stream) for in-kernel
 // last-CTA detection; every user leaves them at zero.
+constexpr int kCounterWords = 1024;
 unsigned* stream_counter(cudaStream_t stream, int* status);
 int sm_count();
 int cuda_fail(cudaError_t e);

@@ -5,8 +5,8 @@
 // estimates of squared row magnitudes, no first moment):
 //   1. sign words of A for this (seed, step) and S split into bf16 hi + lo,
 //      pre-swizzled, in one launch                                (apply_tc.cu)
-//   2. M = Sigma Sigma^T from popcounts, stored as an exact bf16 hi + lo
-//      image                                                      (sign.cu)
+//   2. M = Sigma Sigma^T from popcounts (word ranges split over blocks, exact
+//      integer atomics), stored as an exact bf16 hi + lo image   (sign.cu)
 //   3. row norms on the tensor cores: q_i = S_i M S_i^T = r ||(S A)_i||^2,
 //      v_i <- beta2 v_i + (1 - beta2) q_i / (r k), 1/sqrt(v_i + eps),
 //      optional sync sketch, ||S||^2 partials                     (mode 4)
@@ -25,6 +25,7 @@ ApplyWorkspace apply_workspace_layout(int64_t d, int64_t k, int r) {
   const int64_t nw = (k + 63) / 64;
   size_t off = 0;
   w.words_off = off;   off += align256(size_t(r) * nw * 8);
+  w.counts_off = off;  off += align256(size_t(r) * r * 4);
   w.gram_off = off;    off += align256(gram_image_bytes(r));
   w.inv_off = off;     off += align256(size_t(d) * 4);
   w.ssq_off = off;     off += align256(size_t(1024) * 8);
@@ -45,20 +46,22 @@ int launch_rowadam(int mode, float* W, __nv_bfloat16* Wb, void* out, int accumul
   uint8_t* mimg = reinterpret_cast<uint8_t*>(ws + WL.gram_off);
   const bool rownorms = (mode == 0 || mode == 1);
   uint64_t* words = rownorms ? reinterpret_cast<uint64_t*>(ws + WL.words_off) : nullptr;
-  unsigned* counter = nullptr;
-  if (rownorms && norms) {
+  // per-stream zeroed counters: [0] the update pass's finished CTAs, [64..) the Gram tiles' arrivals
+  unsigned* counters = nullptr;
+  if (rownorms) {
     int st = 0;
-    counter = stream_counter(s, &st);
+    counters = stream_counter(s, &st);
     if (st) return st;
   }
-  if (int st = launch_apply_prep(key, r, k, words, S, d, img, s)) return st;
+  int* counts = rownorms ? reinterpret_cast<int*>(ws + WL.counts_off) : nullptr;
+  if (int st = launch_apply_prep(key, r, k, words, counts, S, d, img, s)) return st;
 
   ApplyLaunch L{};
   L.d = d; L.k = k; L.r = r; L.key = key; L.neg_lrc = -lrc;
   L.s_img = img; L.m_img = mimg; L.S = S; L.inv = inv; L.beta2 = beta2; L.eps = eps;
   int grid_norm = 0, grid_upd = 0;
   if (rownorms) {
-    if (int st = launch_gram(words, r, k, mimg, s)) return st;
+    if (int st = launch_gram(words, r, k, counts, counters + 64, mimg, s)) return st;
     L.mode = 4;
     L.v_in = v_in;
     L.v_out = v_out;
@@ -70,10 +73,10 @@ int launch_rowadam(int mode, float* W, __nv_bfloat16* Wb, void* out, int accumul
   L.W = W; L.Wb = Wb; L.out = out; L.accumulate = accumulate;
   L.v_in = nullptr; L.v_out = nullptr; L.sync_out = nullptr;
   L.part = dw2;
-  L.norms = norms;
+  L.norms = norms;   // null for predict without norms: no last-CTA sum
   L.ssq = ssq;
   L.nssq = grid_norm;
-  L.counter = counter;
+  L.counter = counters;
   if (int st = launch_apply_tc(L, &grid_upd, ctl, s)) return st;
   return LOGRA_OK;
 }
