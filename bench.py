@@ -37,11 +37,14 @@ if ROOT not in sys.path:
 
 METRIC = "sketch TFLOP/s + fused RowAdam-apply GB/s per GB300; % of roofline"
 
-# DRAM bytes (read + write) of one logra_sketch_accumulate call on the largest
-# matrix of the workload, summed over its launches, from one ncu capture of
-# the kernels as they stand (see profiles/).  None until taken for the
-# current kernels.
-SKETCH_TRAFFIC_PER_CALL = {}
+# DRAM bytes (read + write) of one logra_sketch_accumulate call, summed over
+# its three launches, from one ncu capture of the kernels as they stand
+# (profiles/sketch_kernels_gate27b.md): key (n, d, k, r).  Shapes without an
+# entry report null.
+SKETCH_TRAFFIC_PER_CALL = {
+    # project 92.57 + 3.47 MB, split 8.40 + 0 MB, accumulate 512.66 + 26.90 MB
+    (8192, 27648, 5120, 256): 644.0e6,
+}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
