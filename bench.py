@@ -14,7 +14,10 @@ Default workload: 4 decoder layers of 27B-class shapes (q/o 5120x5120, k/v
 GPU's memory.  The metric is sketch TFLOP/s over the whole step (algorithmic
 sketch FLOPs 2 n r (k + d) per matrix-microbatch, divided by the step time
 including the apply), with the apply's GB/s and both kernels' roofline
-fractions alongside.
+fractions alongside.  The matrices are independent, so the step issues them
+round robin on --streams CUDA streams (default 3); per-call durations (the
+components and the dominant call's roofline) come from one extra step on a
+single stream right after the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun (N > 1) every rank sketches its own microbatches (weak
@@ -57,6 +60,8 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="layers27b")
     p.add_argument("--rank", type=int, default=256)
     p.add_argument("--layers", type=int, default=None, help="override the workload's layer count")
+    p.add_argument("--streams", type=int, default=3,
+                   help="CUDA streams the matrices are issued on, round robin (each keeps its own workspace)")
     p.add_argument("--e2e-steps", type=int, default=2)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -101,8 +106,15 @@ class Clocks:
             os.close(fd)
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.out, stderr=subprocess.DEVNULL)
+            # start timing only once the sampler is producing rows (nvidia-smi takes a moment to start)
+            deadline = time.time() + 5.0
+            while time.time() < deadline and os.path.getsize(self.path) == 0 and self.proc.poll() is None:
+                time.sleep(0.02)
+            self.skip = 0
+            with open(self.path) as f:
+                self.skip = sum(1 for _ in f)        # rows taken before the timed region
         except Exception:
             self.proc = None
 
@@ -117,7 +129,9 @@ class Clocks:
         self.out.close()
         rows = []
         with open(self.path) as f:
-            for line in f:
+            for i, line in enumerate(f):
+                if i < getattr(self, "skip", 0):
+                    continue
                 parts = [x.strip() for x in line.split(",")]
                 if len(parts) >= 9:
                     rows.append(parts)
@@ -252,30 +266,43 @@ def run_ours(args):
     # pre-size the per-stream workspace so no allocation happens while timing
     ws = max(max(L.lib().logra_sketch_workspace_bytes(n, m["d"], m["k"], r, 1 if dt == torch.bfloat16 else 0),
                  L.lib().logra_apply_workspace_bytes(m["d"], m["k"], r)) for m in mats)
-    L.logra_reserve_workspace(ws)
+    # The matrices are independent, so they are issued round robin on `--streams` CUDA streams (each
+    # with its own library workspace): one matrix's launches fill the SMs that another's leave idle
+    # in its tails and launch gaps.  Each matrix's own calls stay in order on one stream.
+    streams = [stream] + [torch.cuda.Stream(device=dev) for _ in range(max(1, args.streams) - 1)]
+    for st in streams:
+        with torch.cuda.stream(st):
+            L.logra_reserve_workspace(ws)
 
-    def one_step(step_idx, ev=None):
-        for m in mats:
-            m["S"].zero_()
-            for mb in range(nmb):
+    def one_step(step_idx, ev=None, sts=None):
+        sts = sts or streams
+        for st in sts[1:]:
+            st.wait_stream(stream)
+        for i, m in enumerate(mats):
+            st = sts[i % len(sts)]
+            with torch.cuda.stream(st):
+                m["S"].zero_()
+                for mb in range(nmb):
+                    if ev is not None:
+                        a = torch.cuda.Event(enable_timing=True)
+                        b = torch.cuda.Event(enable_timing=True)
+                        a.record(st)
+                    L.logra_sketch_accumulate(m["X"][mb], m["dY"][mb], m["S"], m["seed"], step_idx)
+                    if ev is not None:
+                        b.record(st)
+                        ev["sketch"].append((a, b, m["d"], m["k"]))
+                dp.allreduce_sketch(m["S"])
                 if ev is not None:
                     a = torch.cuda.Event(enable_timing=True)
                     b = torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                L.logra_sketch_accumulate(m["X"][mb], m["dY"][mb], m["S"], m["seed"], step_idx)
+                    a.record(st)
+                L.logra_rowadam_apply_ex(m["W"], m["S"], m["v"], m["seed"], step_idx, beta2, eps, lr, c,
+                                         m["norms"], m["Wb"], None)
                 if ev is not None:
-                    b.record(stream)
-                    ev["sketch"].append((a, b, m["d"], m["k"]))
-            dp.allreduce_sketch(m["S"])
-            if ev is not None:
-                a = torch.cuda.Event(enable_timing=True)
-                b = torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-            L.logra_rowadam_apply_ex(m["W"], m["S"], m["v"], m["seed"], step_idx, beta2, eps, lr, c, m["norms"],
-                                     m["Wb"], None)
-            if ev is not None:
-                b.record(stream)
-                ev["apply"].append((a, b, m["d"], m["k"]))
+                    b.record(st)
+                    ev["apply"].append((a, b, m["d"], m["k"]))
+        for st in sts[1:]:
+            stream.wait_stream(st)
 
     def barrier():
         if world > 1:
@@ -289,7 +316,6 @@ def run_ours(args):
     barrier()
     torch.cuda.synchronize()
 
-    ev = {"sketch": [], "apply": []}
     clocks = Clocks(local)
     launches0 = L.logra_launch_count()
     clocks.start()
@@ -297,13 +323,20 @@ def run_ours(args):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for s in range(args.steps):
-        one_step(args.warmup + s, ev)
+        one_step(args.warmup + s)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
     clk = clocks.stop()
     launches = L.logra_launch_count() - launches0
+
+    # Per-call durations come from one more step issued on a single stream right after the
+    # timed region, with CUDA events around every call on that stream: inside the multi-stream
+    # step a call's event span would also cover the other streams' kernels.
+    ev = {"sketch": [], "apply": []}
+    one_step(args.warmup + args.steps, ev, [stream])
+    torch.cuda.synchronize()
     elapsed_ms = t_start.elapsed_time(t_end)
     if world > 1:
         t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
@@ -321,8 +354,8 @@ def run_ours(args):
         f, b = apply_work(m["d"], m["k"], r)
         ap_f += f
         ap_b += b
-    sk_ms = sum(a.elapsed_time(b) for a, b, _, _ in ev["sketch"]) / args.steps
-    ap_ms = sum(a.elapsed_time(b) for a, b, _, _ in ev["apply"]) / args.steps
+    sk_ms = sum(a.elapsed_time(b) for a, b, _, _ in ev["sketch"])
+    ap_ms = sum(a.elapsed_time(b) for a, b, _, _ in ev["apply"])
     peaks, peak_kind = load_peaks()
     hbm, tc = float(peaks["hbm_gbs"]), float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
     value = world * sk_f / (ms_step * 1e-3) / 1e12
@@ -359,7 +392,9 @@ def run_ours(args):
         "config": {"workload": w.name, "layers": layers, "matrices": [list(x) for x in w.matrices],
                    "microbatches": nmb, "tokens": n, "r": r, "mask_frac": w.mask_frac,
                    "input_bytes_resident": input_bytes, "l2": "inputs larger than L2, no flush",
-                   "parallelism": f"dp{world}"},
+                   "parallelism": f"dp{world}", "streams": len(streams),
+                   "component_timing": "components and roofline: CUDA events around each call in one "
+                   "extra step issued on a single stream right after the timed region"},
         "components": {
             "sketch": {"ms_per_step": sk_ms, "tflops": sk_tflops, "gbs": sk_gbs,
                        "frac_of_roofline": sk_roof_ms / sk_ms, "roofline_ms": sk_roof_ms},
