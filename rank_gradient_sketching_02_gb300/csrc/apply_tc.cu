@@ -24,9 +24,10 @@
 // (one bulk copy per 64-wide rank chunk); B = Sigma rows of that chunk for the
 // super-tile's 256 columns, MN-major, generated in shared memory from the sign
 // hash (mode 4: the M image by bulk copy).  W moves in by TMA in 128 x 32
-// sub-tiles; each epilogue warp updates its 32-row slice in place and stores
-// it (and its bf16 copy) by TMA on its own, keeping one store group in flight
-// while it computes the next slice, so the four warps never wait on each other.
+// sub-tiles through a 3-stage ring whose stages are released as soon as the
+// epilogue warps have read them; each warp writes its updated 32-row slice (and
+// its bf16 copy) to double-buffered staging and stores it by TMA on its own,
+// keeping one store group in flight while it computes the next slice.
 //
 // Roles: warp 0 = A (and mode-4 B) producer, warp 1 = TMEM owner + MMA issuer,
 // warps 2..5 = epilogue (TMEM lane quadrant = warp % 4), warps 6..9 = sign-tile
@@ -49,7 +50,7 @@ constexpr int kCols = 256;        // MMA N: columns per super-tile
 constexpr int kRc = 64;           // ranks per K chunk
 constexpr int kSub = 32;          // epilogue sub-tile width (columns)
 constexpr int kAbStages = 2;
-constexpr int kWStages = 4;
+constexpr int kWStages = 3;
 constexpr uint32_t kABytes = 2 * kRows * 128;   // hi + lo: 32 KB
 constexpr uint32_t kBBytes = kRc * kCols * 2;   // 64 ranks x 256 columns bf16: 32 KB
 constexpr uint32_t kWBytes = kRows * kSub * 4;  // fp32 sub-tile: 16 KB
@@ -65,7 +66,7 @@ struct ApplyShared {
   double red[4];
 };
 
-constexpr size_t kApplySmem = 1024 + kAbStages * (kABytes + kBBytes) + kWStages * kWBytes + 2 * kHBytes +
+constexpr size_t kApplySmem = 1024 + kAbStages * (kABytes + kBBytes) + kWStages * kWBytes + 2 * kWBytes + 2 * kHBytes +
                               sizeof(ApplyShared) + 64;
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -117,8 +118,9 @@ __global__ void __launch_bounds__(352, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   uint8_t* ab = base;                                              // [stage][A 32 KB | B 32 KB]
-  uint8_t* wr = ab + kAbStages * (kABytes + kBBytes);              // [stage][16 KB]
-  uint8_t* hb = wr + kWStages * kWBytes;                           // 2 x 8 KB bf16 staging
+  uint8_t* wr = ab + kAbStages * (kABytes + kBBytes);              // [stage][16 KB] W sub-tiles in
+  uint8_t* sb32 = wr + kWStages * kWBytes;                         // 2 x 16 KB fp32 staging out
+  uint8_t* hb = sb32 + 2 * kWBytes;                                // 2 x 8 KB bf16 staging out
   ApplyShared* sh = reinterpret_cast<ApplyShared*>(hb + 2 * kHBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned long long limit = ctl->wait_limit;
@@ -259,7 +261,7 @@ __global__ void __launch_bounds__(352, 1)
     const int et = threadIdx.x - 64;                     // 0..127
     uint32_t tph[2] = {0, 0};
     int buf = 0;
-    int wstage = 0, prev_stage = -1, sub = 0;
+    int wstage = 0, sub = 0;
     uint32_t wphase = 0;
     double acc_cta = 0.0;                                // dW^2 (modes 0, 1) or ||S||^2 (mode 4)
     bool aborted = false;
@@ -314,23 +316,36 @@ __global__ void __launch_bounds__(352, 1)
             acc_cta += double(acc);
             continue;
           }
-          uint8_t* wt = wr + wstage * kWBytes;
+          const uint8_t* wt = wr + wstage * kWBytes;
+          uint8_t* st = sb32 + (sub & 1) * kWBytes;
           uint8_t* ht = hb + (sub & 1) * kHBytes;
+          // W comes in through the ring and leaves through separate staging, so
+          // a ring stage is released as soon as the warps have read it and the
+          // whole ring stays available for loads in flight
+          float4 w[8];
+          uint4 wb[4];
           if (load_in) {
             if (!warp_wait(sh, &sh->w_full[wstage], wphase, limit, ctl)) { aborted = true; break; }
+            if (MODE == 0 || MODE == 2) {
+              // fp32 sub-tile, 128-byte rows, 16-byte chunk q at q ^ (row & 7)
+#pragma unroll
+              for (int q4 = 0; q4 < 8; ++q4)
+                w[q4] = *reinterpret_cast<const float4*>(wt + row_l * 128 + ((q4 ^ (row_l & 7)) << 4));
+            } else {
+              // bf16 sub-tile, 64-byte rows, 16-byte chunk h at h ^ ((row >> 1) & 3)
+#pragma unroll
+              for (int h = 0; h < 4; ++h)
+                wb[h] = *reinterpret_cast<const uint4*>(wt + row_l * 64 + ((h ^ ((row_l >> 1) & 3)) << 4));
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh->w_empty[wstage]);
+          } else {
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) w[q4] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) wb[h] = make_uint4(0, 0, 0, 0);
           }
           if (MODE == 0 || MODE == 2) {
-            // fp32 sub-tile, 128-byte rows, 16-byte chunk q at q ^ (row & 7)
-            // all eight 16-byte loads first, then the arithmetic, then the
-            // stores: in-place stores would otherwise keep the compiler from
-            // issuing the next load early, and one warp per scheduler cannot
-            // hide a shared-memory round trip per step
-            uint8_t* rowp = wt + row_l * 128;
-            float4 w[8];
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-              w[q4] = load_in ? *reinterpret_cast<const float4*>(rowp + ((q4 ^ (row_l & 7)) << 4))
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
@@ -346,7 +361,7 @@ __global__ void __launch_bounds__(352, 1)
             }
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4)
-              *reinterpret_cast<float4*>(rowp + ((q4 ^ (row_l & 7)) << 4)) = w[q4];
+              *reinterpret_cast<float4*>(st + row_l * 128 + ((q4 ^ (row_l & 7)) << 4)) = w[q4];
             if (MODE == 0 && A.write_bf16) {
               // bf16 staging: 64-byte rows, 16-byte chunk h at h ^ ((row >> 1) & 3)
 #pragma unroll
@@ -358,12 +373,10 @@ __global__ void __launch_bounds__(352, 1)
             if (MODE == 0 && row_ok) acc_cta += double((acc[0] + acc[1]) + (acc[2] + acc[3]));
           } else {
             // MODE 3: bf16 output sub-tile (64-byte rows) in the staging buffer
-            const uint8_t* src = wt + row_l * 64;
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
               const int off = (h ^ ((row_l >> 1) & 3)) << 4;
-              uint4 in = load_in ? *reinterpret_cast<const uint4*>(src + off) : make_uint4(0, 0, 0, 0);
-              const uint32_t iw[4] = {in.x, in.y, in.z, in.w};
+              const uint32_t iw[4] = {wb[h].x, wb[h].y, wb[h].z, wb[h].w};
               uint32_t ow[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
@@ -380,18 +393,16 @@ __global__ void __launch_bounds__(352, 1)
           __syncwarp();
           if (lane == 0) {
             const int32_t r0 = rb * kRows + quad * 32;
-            if (MODE == 0 || MODE == 2) tma_store_2d(&tmap_f32s, wt + quad * (32 * 128), int32_t(col0), r0);
+            if (MODE == 0 || MODE == 2) tma_store_2d(&tmap_f32s, st + quad * (32 * 128), int32_t(col0), r0);
             if ((MODE == 0 && A.write_bf16) || MODE == 3) tma_store_2d(&tmap_b16s, ht + quad * (32 * 64), int32_t(col0), r0);
             bulk_commit();
             // keep this slice's stores in flight; once at most one group is
-            // outstanding, the previous slice's stores have read their smem
+            // outstanding, the other staging buffers have been read
             asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-            if (load_in && prev_stage >= 0) mbar_arrive(&sh->w_empty[prev_stage]);
           }
           __syncwarp();
-          prev_stage = load_in ? wstage : -1;
           ++sub;
-          if (load_in || MODE == 2) {
+          if (load_in) {
             if (++wstage == kWStages) { wstage = 0; wphase ^= 1u; }
           }
         }
@@ -417,10 +428,7 @@ __global__ void __launch_bounds__(352, 1)
         }
       }
     }
-    if (lane == 0) {
-      bulk_wait_all();
-      if (load_in && prev_stage >= 0 && !aborted) mbar_arrive(&sh->w_empty[prev_stage]);
-    }
+    if (lane == 0) bulk_wait_all();
     __syncwarp();
     // per-CTA partial sum, fixed order
     for (int o = 16; o; o >>= 1) acc_cta += __shfl_xor_sync(0xffffffffu, acc_cta, o);
