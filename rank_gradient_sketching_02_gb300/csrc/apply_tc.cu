@@ -49,7 +49,8 @@ constexpr int kRows = 128;        // MMA M: rows of W per block
 constexpr int kCols = 256;        // MMA N: columns per super-tile
 constexpr int kRc = 64;           // ranks per K chunk
 constexpr int kSub = 32;          // epilogue sub-tile width (columns)
-constexpr int kAbStages = 2;
+constexpr int kAbStages = 2;      // A/B stages of the update and rebuild passes
+constexpr int kAbStagesNorm = 3;  // row norms: the W ring and staging space holds a third
 constexpr int kWStages = 3;
 constexpr uint32_t kABytes = 2 * kRows * 128;   // hi + lo: 32 KB
 constexpr uint32_t kBBytes = kRc * kCols * 2;   // 64 ranks x 256 columns bf16: 32 KB
@@ -57,7 +58,7 @@ constexpr uint32_t kWBytes = kRows * kSub * 4;  // fp32 sub-tile: 16 KB
 constexpr uint32_t kHBytes = kRows * kSub * 2;  // bf16 sub-tile: 8 KB
 
 struct ApplyShared {
-  uint64_t ab_full[kAbStages], gen_full[kAbStages], ab_empty[kAbStages];
+  uint64_t ab_full[kAbStagesNorm], gen_full[kAbStagesNorm], ab_empty[kAbStagesNorm];
   uint64_t w_full[kWStages], w_empty[kWStages];
   uint64_t tmem_full[2], tmem_empty[2], drain;
   uint32_t tmem_base;
@@ -125,11 +126,12 @@ __global__ void __launch_bounds__(352, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned long long limit = ctl->wait_limit;
   constexpr bool kNorm = (MODE == 4);
+  constexpr int AS = kNorm ? kAbStagesNorm : kAbStages;   // mode 4 uses no W ring or staging
   const int nchunks = kNorm ? 2 * A.nck : A.nck;      // mode 4: M_hi chunks, then M_lo chunks
   const bool load_in = (MODE == 0) || ((MODE == 2 || MODE == 3) && A.accumulate);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kAbStages; ++s) {
+    for (int s = 0; s < AS; ++s) {
       mbar_init(&sh->ab_full[s], 1);
       mbar_init(&sh->gen_full[s], 4);
       mbar_init(&sh->ab_empty[s], 1);
@@ -188,12 +190,12 @@ __global__ void __launch_bounds__(352, 1)
                           &sh->ab_full[stage]);
               }
             }
-            if (++stage == kAbStages) { stage = 0; phase ^= 1u; }
+            if (++stage == AS) { stage = 0; phase ^= 1u; }
           }
         }
       }
     a_done:
-      for (int s = 0; s < kAbStages; ++s) mbar_wait(&sh->ab_full[s], (s < stage) ? phase : (phase ^ 1u), limit);
+      for (int s = 0; s < AS; ++s) mbar_wait(&sh->ab_full[s], (s < stage) ? phase : (phase ^ 1u), limit);
     }
   } else if (warp == 10) {
     // ------------------------------------------------------------------ W tile producer
@@ -243,7 +245,7 @@ __global__ void __launch_bounds__(352, 1)
               mma_bf16(dt, smem_desc(a0 + kRows * 128 + ks * 32, 16, 1024, kSw128), bd, idesc, 1u);
             }
             mma_commit(&sh->ab_empty[stage]);
-            if (++stage == kAbStages) { stage = 0; phase ^= 1u; }
+            if (++stage == AS) { stage = 0; phase ^= 1u; }
           }
           mma_commit(&sh->tmem_full[buf]);
           tph[buf] ^= 1u;
@@ -272,6 +274,13 @@ __global__ void __launch_bounds__(352, 1)
       double q = 0.0;                                    // mode 4: S_i M S_i^T over the row
       for (int t = 0; t < A.inner && !aborted; ++t) {
         const int st = kNorm ? t : u % A.nsuper;
+        // row norms: the first S slice is fetched while the MMAs still run
+        float4 snext[8];
+        if (MODE == 4 && row_ok) {
+          const float4* sp = reinterpret_cast<const float4*>(A.S + row * A.r + int64_t(st) * kCols);
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) snext[q4] = sp[q4];
+        }
         if (!warp_wait(sh, &sh->tmem_full[buf], tph[buf], limit, ctl)) { aborted = true; break; }
         tph[buf] ^= 1u;
         tc_fence_after();
@@ -288,11 +297,19 @@ __global__ void __launch_bounds__(352, 1)
           const int ncol = int(ncols_total - col0 < kSub ? ncols_total - col0 : kSub);
           if (MODE == 4) {
             if (row_ok) {
-              const float4* sp = reinterpret_cast<const float4*>(A.S + row * A.r + col0);
+              // this slice of S was fetched one sub-tile ahead; fetch the next one
+              float4 scur[8];
+#pragma unroll
+              for (int q4 = 0; q4 < 8; ++q4) scur[q4] = snext[q4];
+              if (col0 + kSub < ncols_total && s + 1 < kCols / kSub) {
+                const float4* sp = reinterpret_cast<const float4*>(A.S + row * A.r + col0 + kSub);
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) snext[q4] = sp[q4];
+              }
               float dot = 0.f, ss = 0.f;
 #pragma unroll
               for (int q4 = 0; q4 < 8; ++q4) {
-                const float4 sv = sp[q4];
+                const float4 sv = scur[q4];
                 dot = fmaf(__uint_as_float(g[4 * q4 + 0]), sv.x, dot);
                 dot = fmaf(__uint_as_float(g[4 * q4 + 1]), sv.y, dot);
                 dot = fmaf(__uint_as_float(g[4 * q4 + 2]), sv.z, dot);
@@ -484,7 +501,7 @@ __global__ void __launch_bounds__(352, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh->gen_full[stage]);
-          if (++stage == kAbStages) { stage = 0; phase ^= 1u; }
+          if (++stage == AS) { stage = 0; phase ^= 1u; }
         }
       }
     gen_done:;

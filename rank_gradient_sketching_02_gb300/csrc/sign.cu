@@ -21,7 +21,8 @@ __global__ void sign_matrix_kernel(uint64_t key, int r, int64_t k, float scale, 
 }
 
 // M = Sigma Sigma^T, the B operand of the row-norm GEMM.  Blocks split the
-// sign words of each 32 x 32 tile into ranges of at most kGramWords words and
+// sign words of each 32 x 32 tile into ranges of at most kGramWords words (many
+// small blocks: the pass is latency-bound) and
 // add, with exact integer atomics, the number of bit positions where rows a and
 // b differ into counts (zeroed by the prep launch).  The last block of a tile
 // (a wrapping arrival counter, left at zero) writes its part of the image:
@@ -30,7 +31,7 @@ __global__ void sign_matrix_kernel(uint64_t key, int r, int64_t k, float scale, 
 // super-tile st, 64-rank chunk c, term): a 32 KB MN-major tile of 4 groups of
 // 64 columns x 64 rows of 128 bytes, 16-byte chunk q of row a stored at
 // q ^ (a & 7).  Entries outside r x r are zero.
-constexpr int kGramWords = 64;
+constexpr int kGramWords = 16;
 
 __global__ void __launch_bounds__(256) gram_kernel(const uint64_t* __restrict__ words, int r, int nw, int64_t k,
                                                    int* __restrict__ counts, unsigned* __restrict__ arrivals,
@@ -45,6 +46,7 @@ __global__ void __launch_bounds__(256) gram_kernel(const uint64_t* __restrict__ 
     const int wbeg = blockIdx.z * kGramWords, wend = min(nw, wbeg + kGramWords);
     int diff[4] = {0, 0, 0, 0};
     for (int w0 = wbeg; w0 < wend; w0 += 32) {
+      const int nwr = min(32, wend - w0);
       for (int rr = ty; rr < 32; rr += 8) {
         const int w = w0 + tx;
         uint64_t va = 0, vb = 0;
@@ -60,7 +62,7 @@ __global__ void __launch_bounds__(256) gram_kernel(const uint64_t* __restrict__ 
       }
       __syncthreads();
 #pragma unroll 4
-      for (int w = 0; w < 32; ++w) {
+      for (int w = 0; w < nwr; ++w) {
         const uint64_t x = wb[tx][w];
 #pragma unroll
         for (int q = 0; q < 4; ++q) diff[q] += __popcll(wa[ty + 8 * q][w] ^ x);
