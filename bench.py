@@ -492,6 +492,7 @@ def run_e2e(args, L, dp, mats, w, r, dt, dev, stream, sk_f, world):
     ms = t0.elapsed_time(t1) / steps
     return {"value": world * sk_f / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d // steps, "d2h_bytes_per_step": d2h // steps,
+            "h2d_gbs": (h2d / steps) / (ms * 1e-3) / 1e9,
             "host_inputs": "pinned host copy of one microbatch per matrix shape, re-sent for every microbatch"}
 
 
