@@ -82,7 +82,7 @@ def test_sketch_tiny_fp32(L):
 
 
 @pytest.mark.parametrize("n,d,k,r", [(4096, 1536, 1536, 256), (300, 264, 520, 96), (1, 8, 8, 32),
-                                     (777, 1024, 200, 512), (129, 4104, 136, 128)])
+                                     (777, 1024, 200, 512), (129, 4104, 136, 128), (640, 392, 1032, 384)])
 def test_sketch_bf16(L, n, d, k, r):
     mbs = [synth.host_microbatch(n, d, k, dy_kind="lognormal", mask_frac=0.25, key=(1, n, d, k, r, mb))[:2]
            for mb in range(2)]
@@ -132,7 +132,7 @@ def _sketch_like(d, r, seed, scale=1e-3):
 
 
 @pytest.mark.parametrize("d,k,r", [(256, 512, 32), (1536, 1536, 256), (40, 1000, 64), (520, 264, 512),
-                                   (8, 8, 32)])
+                                   (8, 8, 32), (392, 1032, 384)])
 def test_apply_stagewise_zero_w0(L, d, k, r):
     import torch
     S32 = _sketch_like(d, r, d + k)
