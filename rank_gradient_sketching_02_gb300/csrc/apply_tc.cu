@@ -50,7 +50,7 @@ constexpr int kCols = 256;        // MMA N: columns per super-tile
 constexpr int kRc = 64;           // ranks per K chunk
 constexpr int kSub = 32;          // epilogue sub-tile width (columns)
 constexpr int kAbStages = 2;      // A/B stages of the update and rebuild passes
-constexpr int kAbStagesNorm = 3;  // row norms: the W ring and staging space holds a third
+constexpr int kAbStagesNorm = 2;  // row norms: two 96 KB stages (S chunk + M hi + M lo) in the A/B, W ring and staging space
 constexpr int kWStages = 3;
 constexpr uint32_t kABytes = 2 * kRows * 128;   // hi + lo: 32 KB
 constexpr uint32_t kBBytes = kRc * kCols * 2;   // 64 ranks x 256 columns bf16: 32 KB
@@ -127,7 +127,10 @@ __global__ void __launch_bounds__(352, 1)
   const unsigned long long limit = ctl->wait_limit;
   constexpr bool kNorm = (MODE == 4);
   constexpr int AS = kNorm ? kAbStagesNorm : kAbStages;   // mode 4 uses no W ring or staging
-  const int nchunks = kNorm ? 2 * A.nck : A.nck;      // mode 4: M_hi chunks, then M_lo chunks
+  // a stage holds one 64-rank chunk of the S image and its B operand: the sign
+  // tile, or (mode 4) both terms of the Gram image, so each S chunk loads once
+  constexpr uint32_t kStageB = kNorm ? kABytes + 2 * kBBytes : kABytes + kBBytes;
+  const int nchunks = A.nck;
   const bool load_in = (MODE == 0) || ((MODE == 2 || MODE == 3) && A.accumulate);
 
   if (threadIdx.x == 0) {
@@ -175,20 +178,17 @@ __global__ void __launch_bounds__(352, 1)
         for (int t = 0; t < A.inner; ++t) {
           const int rb = kNorm ? u : u / A.nsuper;
           const int st = kNorm ? t : u % A.nsuper;
-          for (int cc = 0; cc < nchunks; ++cc) {
-            const int c = kNorm ? cc % A.nck : cc;
+          for (int c = 0; c < nchunks; ++c) {
             if (!wait_or_abort(sh, &sh->ab_empty[stage], phase ^ 1u, limit, ctl)) goto a_done;
-            uint8_t* dst = ab + stage * (kABytes + kBBytes);
-            if (inject && cc == 0) {
+            uint8_t* dst = ab + stage * kStageB;
+            if (inject && c == 0) {
               inject = 0;
             } else {
-              mbar_arrive_expect_tx(&sh->ab_full[stage], kNorm ? kABytes + kBBytes : kABytes);
+              mbar_arrive_expect_tx(&sh->ab_full[stage], kNorm ? kStageB : kABytes);
               bulk_load(dst, A.s_image + (size_t(rb) * A.nck + c) * kABytes, kABytes, &sh->ab_full[stage]);
-              if (kNorm) {
-                const int term = cc / A.nck;
-                bulk_load(dst + kABytes, A.m_image + ((size_t(st) * A.nck + c) * 2 + term) * kBBytes, kBBytes,
+              if (kNorm)   // M_hi and M_lo of this chunk are adjacent in the image
+                bulk_load(dst + kABytes, A.m_image + (size_t(st) * A.nck + c) * 2 * kBBytes, 2 * kBBytes,
                           &sh->ab_full[stage]);
-              }
             }
             if (++stage == AS) { stage = 0; phase ^= 1u; }
           }
@@ -226,23 +226,31 @@ __global__ void __launch_bounds__(352, 1)
       uint32_t tph[2] = {0, 0};
       int buf = 0;
       const uint32_t idesc = idesc_bf16(kRows, kCols, 0, 1);
+      // stage-0 descriptors, advanced by adds of the 16-byte-unit address field
+      const uint64_t adesc0 = smem_desc(smem_addr(ab), 16, 1024, kSw128);
+      const uint64_t bdesc0 = smem_desc(smem_addr(ab + kABytes), kRc * 128, 1024, kSw128);
       for (int u = blockIdx.x; u < A.units && !sh->abort; u += gridDim.x) {
         for (int t = 0; t < A.inner; ++t) {
           if (!wait_or_abort(sh, &sh->tmem_empty[buf], tph[buf] ^ 1u, limit, ctl)) goto mma_done;
           tc_fence_after();
           const uint32_t dt = tmem + uint32_t(buf * kCols);
-          for (int cc = 0; cc < nchunks; ++cc) {
-            const int c = kNorm ? cc % A.nck : cc;
+          for (int c = 0; c < nchunks; ++c) {
             if (!wait_or_abort(sh, &sh->ab_full[stage], phase, limit, ctl)) goto mma_done;
             if (!kNorm && !wait_or_abort(sh, &sh->gen_full[stage], phase, limit, ctl)) goto mma_done;
             tc_fence_after();
-            const uint32_t a0 = smem_addr(ab + stage * (kABytes + kBBytes));
-            const uint32_t b0 = a0 + kABytes;
+            const uint64_t ad = adesc0 + uint64_t(uint32_t(stage) * (kStageB >> 4));
+            const uint64_t bd = bdesc0 + uint64_t(uint32_t(stage) * (kStageB >> 4));
             const int ksteps = min(kRc, A.r - c * kRc) / 16;
             for (int ks = 0; ks < ksteps; ++ks) {
-              const uint64_t bd = smem_desc(b0 + ks * 2048, kRc * 128, 1024, kSw128);
-              mma_bf16(dt, smem_desc(a0 + ks * 32, 16, 1024, kSw128), bd, idesc, (cc | ks) ? 1u : 0u);
-              mma_bf16(dt, smem_desc(a0 + kRows * 128 + ks * 32, 16, 1024, kSw128), bd, idesc, 1u);
+              const uint64_t a_hi = ad + uint64_t(2 * ks), a_lo = a_hi + uint64_t((kRows * 128) >> 4);
+              const uint64_t b = bd + uint64_t(ks * (2048 >> 4));
+              mma_bf16(dt, a_hi, b, idesc, (c | ks) ? 1u : 0u);
+              mma_bf16(dt, a_lo, b, idesc, 1u);
+              if (kNorm) {                                   // the M_lo term
+                const uint64_t bl = b + uint64_t(kBBytes >> 4);
+                mma_bf16(dt, a_hi, bl, idesc, 1u);
+                mma_bf16(dt, a_lo, bl, idesc, 1u);
+              }
             }
             mma_commit(&sh->ab_empty[stage]);
             if (++stage == AS) { stage = 0; phase ^= 1u; }
@@ -487,7 +495,7 @@ __global__ void __launch_bounds__(352, 1)
         const int st = u % A.nsuper;
         for (int c = 0; c < nchunks; ++c) {
           if (!warp_wait(sh, &sh->ab_empty[stage], phase ^ 1u, limit, ctl)) goto gen_done;
-          uint8_t* bt = ab + stage * (kABytes + kBBytes) + kABytes;
+          uint8_t* bt = ab + stage * kStageB + kABytes;
           // 4 groups of 64 columns x 64 rank rows; row = one sign word (64 columns)
           for (int e = gtid; e < 4 * kRc; e += 128) {
             const int grp = e / kRc, a_l = e % kRc;
