@@ -208,7 +208,9 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": w.name, "r": r, "tokens": w.tokens, "microbatches": w.microbatches},
+            "config": {"workload": w.name, "layers": args.layers or w.layers,
+                       "matrices": [list(x) for x in w.matrices], "microbatches": w.microbatches,
+                       "tokens": w.tokens, "r": r, "mask_frac": w.mask_frac, "parallelism": "dp1"},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": res["cores"], "kind": "oracle",
                              "sample": res["sample"]},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
