@@ -25,13 +25,14 @@
 // super-tile's 256 columns, MN-major, generated in shared memory from the sign
 // hash (mode 4: the M image by bulk copy).  W moves in by TMA in 128 x 32
 // sub-tiles through a 3-stage ring whose stages are released as soon as the
-// epilogue warps have read them; each warp writes its updated 32-row slice (and
-// its bf16 copy) to double-buffered staging and stores it by TMA on its own,
-// keeping one store group in flight while it computes the next slice.
+// epilogue warps have read them; two epilogue groups take alternate sub-tiles
+// and each warp writes its updated 32-row slice (and its bf16 copy) to its
+// group's staging and stores it by TMA on its own, the store draining while the
+// other group works on the next sub-tile.
 //
 // Roles: warp 0 = A (and mode-4 B) producer, warp 1 = TMEM owner + MMA issuer,
-// warps 2..5 = epilogue (TMEM lane quadrant = warp % 4), warps 6..9 = sign-tile
-// generators, warp 10 = W tile producer.  TMEM holds two 256-column
+// warps 2..5 and 11..14 = two epilogue groups (TMEM lane quadrant = warp % 4),
+// warps 6..9 = sign-tile generators, warp 10 = W tile producer.  TMEM holds two 256-column
 // accumulators so the epilogue of one super-tile overlaps the MMAs of the next.
 #include <cuda.h>
 
@@ -64,7 +65,7 @@ struct ApplyShared {
   uint32_t tmem_base;
   int abort;
   int flag;
-  double red[4];
+  double red[8];
 };
 
 constexpr size_t kApplySmem = 1024 + kAbStages * (kABytes + kBBytes) + kWStages * kWBytes + 2 * kWBytes + 2 * kHBytes +
@@ -74,7 +75,7 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
@@ -112,7 +113,7 @@ struct ApplyArgs {
 };
 
 template <int MODE>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(480, 1)
     apply_tc_kernel(const __grid_constant__ CUtensorMap tmap_f32, const __grid_constant__ CUtensorMap tmap_b16,
                     const __grid_constant__ CUtensorMap tmap_f32s, const __grid_constant__ CUtensorMap tmap_b16s,
                     ApplyArgs A, Control* ctl) {
@@ -145,7 +146,7 @@ __global__ void __launch_bounds__(352, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh->tmem_full[b], 1);
-      mbar_init(&sh->tmem_empty[b], 4);
+      mbar_init(&sh->tmem_empty[b], kNorm ? 4 : 8);   // every active epilogue warp
     }
     mbar_init(&sh->drain, 1);
     sh->abort = 0;
@@ -264,18 +265,24 @@ __global__ void __launch_bounds__(352, 1)
       mma_commit(&sh->drain);
       mbar_wait(&sh->drain, 0, limit);
     }
-  } else if (warp < 6) {
+  } else if (warp < 6 || warp >= 11) {
     // ------------------------------------------------------------------ epilogue
+    // Two groups of four warps (2..5 and 11..14), each covering the four TMEM
+    // lane quadrants, take alternate 32-column sub-tiles (row norms: group 0
+    // only), so two warps per scheduler share the per-sub-tile work.
+    const int grp = warp >= 11 ? 1 : 0;
+    const int ngrp = kNorm ? 1 : 2;
     const int quad = warp & 3;
     const int row_l = quad * 32 + lane;                  // row within the block = TMEM lane
-    const int et = threadIdx.x - 64;                     // 0..127
+    const int eidx = grp * 4 + (grp ? warp - 11 : warp - 2);
+    const int et = eidx * 32 + lane;                     // 0..255
     uint32_t tph[2] = {0, 0};
     int buf = 0;
-    int wstage = 0, sub = 0;
+    int wstage = 0;
     uint32_t wphase = 0;
     double acc_cta = 0.0;                                // dW^2 (modes 0, 1) or ||S||^2 (mode 4)
     bool aborted = false;
-    for (int u = blockIdx.x; u < A.units && !aborted; u += gridDim.x) {
+    for (int u = blockIdx.x; u < A.units && !aborted && grp < ngrp; u += gridDim.x) {
       const int rb = kNorm ? u : u / A.nsuper;
       const int64_t row = int64_t(rb) * kRows + row_l;
       const bool row_ok = row < A.d;
@@ -299,6 +306,13 @@ __global__ void __launch_bounds__(352, 1)
         for (int s = 0; s < kCols / kSub; ++s) {
           const int64_t col0 = int64_t(st) * kCols + s * kSub;
           if (col0 >= ncols_total) break;
+          if ((s & (ngrp - 1)) != grp) {
+            // the other group's sub-tile: keep this warp's place in the W ring
+            if (load_in) {
+              if (++wstage == kWStages) { wstage = 0; wphase ^= 1u; }
+            }
+            continue;
+          }
           uint32_t g[32];
           tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + uint32_t(buf * kCols + s * kSub), g);
           tmem_ld_wait();
@@ -342,8 +356,8 @@ __global__ void __launch_bounds__(352, 1)
             continue;
           }
           const uint8_t* wt = wr + wstage * kWBytes;
-          uint8_t* st = sb32 + (sub & 1) * kWBytes;
-          uint8_t* ht = hb + (sub & 1) * kHBytes;
+          uint8_t* st = sb32 + grp * kWBytes;                   // one staging buffer per group
+          uint8_t* ht = hb + grp * kHBytes;
           // W comes in through the ring and leaves through separate staging, so
           // a ring stage is released as soon as the warps have read it and the
           // whole ring stays available for loads in flight
@@ -370,6 +384,10 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
             for (int h = 0; h < 4; ++h) wb[h] = make_uint4(0, 0, 0, 0);
           }
+          // the group's previous stores have read the staging buffers (they had
+          // the other group's sub-tile worth of time; usually no wait)
+          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+          __syncwarp();
           if (MODE == 0 || MODE == 2) {
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -420,13 +438,9 @@ __global__ void __launch_bounds__(352, 1)
             const int32_t r0 = rb * kRows + quad * 32;
             if (MODE == 0 || MODE == 2) tma_store_2d(&tmap_f32s, st + quad * (32 * 128), int32_t(col0), r0);
             if ((MODE == 0 && A.write_bf16) || MODE == 3) tma_store_2d(&tmap_b16s, ht + quad * (32 * 64), int32_t(col0), r0);
-            bulk_commit();
-            // keep this slice's stores in flight; once at most one group is
-            // outstanding, the other staging buffers have been read
-            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+            bulk_commit();          // in flight until the group's next sub-tile
           }
           __syncwarp();
-          ++sub;
           if (load_in) {
             if (++wstage == kWStages) { wstage = 0; wphase ^= 1u; }
           }
@@ -457,10 +471,11 @@ __global__ void __launch_bounds__(352, 1)
     __syncwarp();
     // per-CTA partial sum, fixed order
     for (int o = 16; o; o >>= 1) acc_cta += __shfl_xor_sync(0xffffffffu, acc_cta, o);
-    if (lane == 0) sh->red[quad] = acc_cta;
+    if (lane == 0) sh->red[eidx] = acc_cta;
     epi_sync();
     if (et == 0 && (MODE == 0 || MODE == 1 || MODE == 4))
-      A.part[blockIdx.x] = sh->red[0] + sh->red[1] + sh->red[2] + sh->red[3];
+      A.part[blockIdx.x] = ((sh->red[0] + sh->red[1]) + (sh->red[2] + sh->red[3])) +
+                           ((sh->red[4] + sh->red[5]) + (sh->red[6] + sh->red[7]));
     if ((MODE == 0 || MODE == 1) && A.norms && warp == 2) {
       // The last CTA to finish sums every CTA's partial (and mode 4's) in a
       // fixed order: deterministic, and no separate reduction launch.
@@ -654,7 +669,7 @@ int launch_apply_tc(const ApplyLaunch& L, int* grid_out, Control* ctl, cudaStrea
   *grid_out = grid;
   auto run = [&](auto kern) -> int {
     LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(kern), int(kApplySmem)));
-    kern<<<grid, 352, kApplySmem, s>>>(t32, t16, t32s, t16s, A, ctl);
+    kern<<<grid, 480, kApplySmem, s>>>(t32, t16, t32s, t16s, A, ctl);
     LOGRA_LAUNCHED();
     return LOGRA_OK;
   };
