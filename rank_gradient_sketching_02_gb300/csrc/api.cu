@@ -55,6 +55,7 @@ struct Buffer {
   void* ptr = nullptr;
   size_t bytes = 0;
   unsigned* counters = nullptr;   // kCounterWords zero-initialised words, never freed while the stream's entry lives
+  int* gram = nullptr;            // 512 x 512 Gram counts, zero between applies
 };
 std::map<std::pair<int, cudaStream_t>, Buffer> g_ws;
 
@@ -121,6 +122,27 @@ void* workspace(cudaStream_t stream, size_t bytes, int* status) {
     b.bytes = want;
   }
   return b.ptr;
+}
+
+int* gram_counts(cudaStream_t stream, int* status) {
+  *status = LOGRA_OK;
+  int dev;
+  if ((*status = current_device(&dev))) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  Buffer& b = g_ws[std::make_pair(dev, stream)];
+  if (!b.gram) {
+    void* p = nullptr;
+    const size_t bytes = size_t(512) * 512 * sizeof(int);
+    cudaError_t e = cudaMalloc(&p, bytes);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, bytes, stream);   // ordered before its first user
+    if (e != cudaSuccess) {
+      if (p) cudaFree(p);
+      *status = cuda_fail(e);
+      return nullptr;
+    }
+    b.gram = static_cast<int*>(p);
+  }
+  return b.gram;
 }
 
 unsigned* stream_counter(cudaStream_t stream, int* status) {

@@ -570,25 +570,111 @@ __device__ __forceinline__ void s_image_elem(const float* __restrict__ S, int64_
   *reinterpret_cast<uint4*>(chunk + kRows * 128 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
 }
 
-// The apply's preparation in one launch: sign words of A (words[i][w], w <
-// nw = ceil(k / 64)) and zeroed Gram counts (both skipped when words is
-// null), then the S image.  One grid-stride loop over the three index ranges.
-__global__ void apply_prep_kernel(uint64_t key, int r, int nw, uint64_t* __restrict__ words, int* __restrict__ counts,
-                                  const float* __restrict__ S, int64_t d, uint8_t* __restrict__ img) {
-  const int nchunks = (r + kRc - 1) / kRc;
-  const int64_t nwords = words ? int64_t(r) * nw : 0;
-  const int64_t ncounts = words ? int64_t(r) * r : 0;
-  const int64_t total = nwords + ncounts + ((d + kRows - 1) / kRows) * kRows * nchunks * 8;
-  for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total; e += int64_t(gridDim.x) * blockDim.x) {
-    if (e < nwords) {
-      const int i = int(e / nw), w = int(e - int64_t(i) * nw);
-      words[e] = sign_word(key, uint32_t(i), uint32_t(w));
-    } else if (e < nwords + ncounts) {
-      counts[e - nwords] = 0;
-    } else {
-      s_image_elem(S, d, r, nchunks, img, e - nwords - ncounts);
+// One block of the Gram pass: M = Sigma Sigma^T, the B operand of the
+// row-norm GEMM.  Block (bx, by, bz) takes the 32 x 32 tile (rows a0 = 32 by,
+// columns b0 = 32 bx) and sign words [16 bz, 16 bz + 16): it hashes the words of
+// its 64 rows itself and adds, with exact integer atomics, the number of bit
+// positions where rows a and b differ into counts.  The last block of a tile
+// (a wrapping arrival counter, left at zero) writes its part of the image,
+// M[a][b] = k - 2 * count exactly, split into bf16 hi + lo (|M| <= k < 2^15, so
+// lo is an integer below 2^7 in magnitude), and sets the tile's counts back to
+// zero for the next apply.  Image layout per (256-column super-tile st, 64-rank
+// chunk c, term): a 32 KB MN-major tile of 4 groups of 64 columns x 64 rows of
+// 128 bytes, 16-byte chunk q of row a stored at q ^ (a & 7).  Entries outside
+// r x r are zero.
+constexpr int kGramWords = 16;
+
+__device__ __forceinline__ void gram_block(uint64_t key, int r, int nw, int64_t k, int* __restrict__ counts,
+                                           unsigned* __restrict__ arrivals, uint8_t* __restrict__ mimg, int bx,
+                                           int by, int bz, int gx, int gz) {
+  __shared__ uint64_t wa[32][kGramWords + 1];
+  __shared__ uint64_t wb[32][kGramWords + 1];
+  __shared__ unsigned last;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8 threads
+  const int a0 = by * 32, b0 = bx * 32;
+  const bool live = a0 < r && b0 < r;                         // block-uniform
+  if (live) {
+    const int wbeg = bz * kGramWords, nwr = min(kGramWords, nw - wbeg);
+    for (int e = threadIdx.x; e < 2 * 32 * kGramWords; e += blockDim.x) {
+      const int side = e / (32 * kGramWords), rr = (e / kGramWords) % 32, w = e % kGramWords;
+      const int row = (side ? b0 : a0) + rr;
+      uint64_t v = 0;
+      if (w < nwr && row < r) {
+        v = sign_word(key, uint32_t(row), uint32_t(wbeg + w));
+        const int64_t rem = k - int64_t(wbeg + w) * 64;
+        if (rem < 64) v &= (1ull << rem) - 1ull;
+      }
+      (side ? wb : wa)[rr][w] = v;
     }
+    __syncthreads();
+    int diff[4] = {0, 0, 0, 0};
+    for (int w = 0; w < nwr; ++w) {
+      const uint64_t x = wb[tx][w];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) diff[q] += __popcll(wa[ty + 8 * q][w] ^ x);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int a = a0 + ty + 8 * q, b = b0 + tx;
+      if (a < r && b < r && diff[q]) atomicAdd(&counts[a * r + b], diff[q]);
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = (atomicInc(&arrivals[by * gx + bx], gz - 1) == gz - 1) ? 1u : 0u;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+  } else if (bz != 0) {
+    return;                                                   // padding tiles: block z = 0 writes the zeros
   }
+  // the tile's image: 32 rows x 4 sixteen-byte chunks x 2 terms, one whole
+  // chunk (8 consecutive columns of one row, one term) per thread
+  const int nck = (r + 63) / 64;
+  const int term = threadIdx.x >> 7, a = a0 + ((threadIdx.x >> 2) & 31), bq = b0 + (threadIdx.x & 3) * 8;
+  uint32_t packed[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t two = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int b = bq + 2 * i + h;
+      const float m = (a < r && b < r) ? float(k - 2 * int64_t(__ldcg(counts + a * r + b))) : 0.f;
+      const __nv_bfloat16 hi = __float2bfloat16_rn(m);
+      const __nv_bfloat16 v = term ? __float2bfloat16_rn(m - __bfloat162float(hi)) : hi;
+      two |= uint32_t(__bfloat16_as_ushort(v)) << (16 * h);
+    }
+    packed[i] = two;
+  }
+  const int st = bq >> 8, grp = (bq >> 6) & 3, q = (bq >> 3) & 7;
+  const int c = a >> 6, a_l = a & 63;
+  uint8_t* tile = mimg + ((size_t(st) * nck + c) * 2 + term) * 32768;
+  *reinterpret_cast<uint4*>(tile + grp * 8192 + a_l * 128 + ((q ^ (a_l & 7)) << 4)) =
+      make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  if (live) {
+    __syncthreads();                                          // both terms have read the counts
+    if (term == 0 && a < r)
+      for (int b = bq; b < bq + 8 && b < r; ++b) counts[a * r + b] = 0;
+  }
+}
+
+// The apply's preparation in one launch: the first ngram blocks run the Gram
+// pass (when asked), the rest build the S image with a grid-stride loop.
+__global__ void __launch_bounds__(256) apply_prep_kernel(uint64_t key, int r, int nw, int64_t k, int gx, int gy,
+                                                         int gz, int* __restrict__ counts,
+                                                         unsigned* __restrict__ arrivals, uint8_t* __restrict__ mimg,
+                                                         const float* __restrict__ S, int64_t d,
+                                                         uint8_t* __restrict__ img) {
+  const int ngram = gx * gy * gz;
+  if (int(blockIdx.x) < ngram) {
+    const int b = blockIdx.x;
+    gram_block(key, r, nw, k, counts, arrivals, mimg, b % gx, (b / gx) % gy, b / (gx * gy), gx, gz);
+    return;
+  }
+  const int nchunks = (r + kRc - 1) / kRc;
+  const int64_t total = ((d + kRows - 1) / kRows) * kRows * nchunks * 8;
+  const int64_t nb = int64_t(gridDim.x) - ngram;
+  for (int64_t e = (int64_t(blockIdx.x) - ngram) * blockDim.x + threadIdx.x; e < total; e += nb * blockDim.x)
+    s_image_elem(S, d, r, nchunks, img, e);
 }
 
 size_t s_image_bytes(int64_t d, int r) {
@@ -597,14 +683,18 @@ size_t s_image_bytes(int64_t d, int r) {
   return size_t(rb) * nchunks * kABytes;
 }
 
-int launch_apply_prep(uint64_t key, int r, int64_t k, uint64_t* words, int* counts, const float* S, int64_t d,
-                      uint8_t* img, cudaStream_t s) {
+int launch_apply_prep(uint64_t key, int r, int64_t k, bool gram, int* counts, unsigned* arrivals, uint8_t* mimg,
+                      const float* S, int64_t d, uint8_t* img, cudaStream_t s) {
   const int nchunks = (r + kRc - 1) / kRc;
   const int nw = int((k + 63) / 64);
-  const int64_t total = (words ? int64_t(r) * nw + int64_t(r) * r : 0) + ((d + kRows - 1) / kRows) * kRows * nchunks * 8;
+  const int gx = gram ? ((r + 255) / 256) * 8 : 0, gy = gram ? ((r + 63) / 64) * 2 : 0;
+  const int gz = gram ? (nw + kGramWords - 1) / kGramWords : 0;
+  const int64_t total = ((d + kRows - 1) / kRows) * kRows * nchunks * 8;
   int64_t blocks = (total + 255) / 256;
   if (blocks > int64_t(sm_count()) * 8) blocks = int64_t(sm_count()) * 8;
-  apply_prep_kernel<<<unsigned(blocks), 256, 0, s>>>(key, r, nw, words, counts, S, d, img);
+  if (blocks < 1) blocks = 1;
+  apply_prep_kernel<<<unsigned(blocks + int64_t(gx) * gy * gz), 256, 0, s>>>(key, r, nw, k, gx, gy, gz, counts,
+                                                                             arrivals, mimg, S, d, img);
   LOGRA_LAUNCHED();
   return LOGRA_OK;
 }

@@ -56,6 +56,9 @@ void* workspace(cudaStream_t stream, size_t bytes, int* status);
 // A few zero-initialised counters per (device, stream) for in-kernel
 // last-CTA detection; every user leaves them at zero.
 constexpr int kCounterWords = 1024;
+// r x r (r <= 512) Gram counts per (device, stream), zero when allocated and
+// left zero by every apply.
+int* gram_counts(cudaStream_t stream, int* status);
 unsigned* stream_counter(cudaStream_t stream, int* status);
 int sm_count();
 int cuda_fail(cudaError_t e);

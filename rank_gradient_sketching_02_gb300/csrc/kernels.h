@@ -11,17 +11,14 @@ namespace logra {
 struct Control;
 
 struct ApplyWorkspace {
-  size_t words_off, counts_off, gram_off, inv_off, ssq_off, dw2_off, img_off, bytes;
+  size_t gram_off, inv_off, ssq_off, dw2_off, img_off, bytes;
 };
 
 ApplyWorkspace apply_workspace_layout(int64_t d, int64_t k, int r);
 
 int launch_sign_matrix(uint64_t key, int r, int64_t k, float scale, float* A, cudaStream_t s);
 size_t gram_image_bytes(int r);
-// M = Sigma Sigma^T image from the packed sign words; counts (r x r) zeroed and
-// words written by launch_apply_prep; arrivals: (nst*8) x (nck*2) zero words.
-int launch_gram(const uint64_t* words, int r, int64_t k, int* counts, unsigned* arrivals, uint8_t* img,
-                cudaStream_t s);
+
 
 int launch_sketch_simt(const void* X, const void* dY, int dtype, int64_t n, int64_t d, int64_t k, int r,
                        uint64_t key, float scale, float* S, float* P, cudaStream_t s);
@@ -31,10 +28,11 @@ int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_
                      float scale, float* S, void* ws, Control* ctl, cudaStream_t s);
 
 size_t s_image_bytes(int64_t d, int r);
-// One launch: the S image (A operand of the apply) and, when `words` is not
-// null, the packed sign words of A and zeroed r x r counts for the Gram matrix.
-int launch_apply_prep(uint64_t key, int r, int64_t k, uint64_t* words, int* counts, const float* S, int64_t d,
-                      uint8_t* img, cudaStream_t s);
+// One launch: the S image (A operand of the apply) and, when `gram` is set,
+// the Gram image M = Sigma Sigma^T.  counts: r x r ints and arrivals: one word
+// per 32 x 32 tile of M, both zero on entry and left zero.
+int launch_apply_prep(uint64_t key, int r, int64_t k, bool gram, int* counts, unsigned* arrivals, uint8_t* mimg,
+                      const float* S, int64_t d, uint8_t* img, cudaStream_t s);
 // The tensor-core kernel behind the apply: mode 0 apply, 1 predict (dW^2 only),
 // 2 rebuild fp32, 3 rebuild bf16, 4 row norms (v, 1/sqrt(v+eps), sync sketch,
 // ||S||^2 partials) from the Gram image.

@@ -3,10 +3,10 @@
 //
 // apply / predict (theclarity.today write-up, "What happened": running
 // estimates of squared row magnitudes, no first moment):
-//   1. sign words of A for this (seed, step) and S split into bf16 hi + lo,
-//      pre-swizzled, in one launch                                (apply_tc.cu)
-//   2. M = Sigma Sigma^T from popcounts (word ranges split over blocks, exact
-//      integer atomics), stored as an exact bf16 hi + lo image   (sign.cu)
+//   1+2. one launch: S split into bf16 hi + lo, pre-swizzled; and M = Sigma
+//      Sigma^T from popcounts of sign words hashed in place (word ranges split
+//      over blocks, exact integer atomics), stored as an exact bf16 hi + lo
+//      image                                                      (apply_tc.cu)
 //   3. row norms on the tensor cores: q_i = S_i M S_i^T = r ||(S A)_i||^2,
 //      v_i <- beta2 v_i + (1 - beta2) q_i / (r k), 1/sqrt(v_i + eps),
 //      optional sync sketch, ||S||^2 partials                     (mode 4)
@@ -22,10 +22,7 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 ApplyWorkspace apply_workspace_layout(int64_t d, int64_t k, int r) {
   ApplyWorkspace w{};
-  const int64_t nw = (k + 63) / 64;
   size_t off = 0;
-  w.words_off = off;   off += align256(size_t(r) * nw * 8);
-  w.counts_off = off;  off += align256(size_t(r) * r * 4);
   w.gram_off = off;    off += align256(gram_image_bytes(r));
   w.inv_off = off;     off += align256(size_t(d) * 4);
   w.ssq_off = off;     off += align256(size_t(1024) * 8);
@@ -45,23 +42,24 @@ int launch_rowadam(int mode, float* W, __nv_bfloat16* Wb, void* out, int accumul
   uint8_t* img = reinterpret_cast<uint8_t*>(ws + WL.img_off);
   uint8_t* mimg = reinterpret_cast<uint8_t*>(ws + WL.gram_off);
   const bool rownorms = (mode == 0 || mode == 1);
-  uint64_t* words = rownorms ? reinterpret_cast<uint64_t*>(ws + WL.words_off) : nullptr;
-  // per-stream zeroed counters: [0] the update pass's finished CTAs, [64..) the Gram tiles' arrivals
+  // per-stream zeroed scratch: counters [0] the update pass's finished CTAs,
+  // [64..) the Gram tiles' arrivals; the Gram counts
   unsigned* counters = nullptr;
+  int* counts = nullptr;
   if (rownorms) {
     int st = 0;
     counters = stream_counter(s, &st);
+    if (!st) counts = gram_counts(s, &st);
     if (st) return st;
   }
-  int* counts = rownorms ? reinterpret_cast<int*>(ws + WL.counts_off) : nullptr;
-  if (int st = launch_apply_prep(key, r, k, words, counts, S, d, img, s)) return st;
+  if (int st = launch_apply_prep(key, r, k, rownorms, counts, counters ? counters + 64 : nullptr, mimg, S, d, img, s))
+    return st;
 
   ApplyLaunch L{};
   L.d = d; L.k = k; L.r = r; L.key = key; L.neg_lrc = -lrc;
   L.s_img = img; L.m_img = mimg; L.S = S; L.inv = inv; L.beta2 = beta2; L.eps = eps;
   int grid_norm = 0, grid_upd = 0;
   if (rownorms) {
-    if (int st = launch_gram(words, r, k, counts, counters + 64, mimg, s)) return st;
     L.mode = 4;
     L.v_in = v_in;
     L.v_out = v_out;
