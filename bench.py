@@ -17,7 +17,8 @@ including the apply), with the apply's GB/s and both kernels' roofline
 fractions alongside.  The matrices are independent, so the step issues them
 round robin on --streams CUDA streams (default 3); per-call durations (the
 components and the dominant call's roofline) come from one extra step on a
-single stream right after the timed region.
+single stream right after the timed region; the apply component also reports all of a
+step's applies issued at once on --apply-streams streams (default 7).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun (N > 1) every rank sketches its own microbatches (weak
@@ -62,6 +63,8 @@ def parse_args(argv=None):
     p.add_argument("--layers", type=int, default=None, help="override the workload's layer count")
     p.add_argument("--streams", type=int, default=3,
                    help="CUDA streams the matrices are issued on, round robin (each keeps its own workspace)")
+    p.add_argument("--apply-streams", type=int, default=7,
+                   help="streams for the all-applies-at-once measurement (each with its own workspace)")
     p.add_argument("--e2e-steps", type=int, default=2)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -339,6 +342,36 @@ def run_ours(args):
     ev = {"sketch": [], "apply": []}
     one_step(args.warmup + args.steps, ev, [stream])
     torch.cuda.synchronize()
+
+    # The applies of a step are independent too: one more measurement issues all of them at
+    # once on the same streams (fork/join on the main stream, CUDA events there), so one
+    # matrix's short prep / row-norm launches overlap another's update pass.
+    ap_streams = [stream] + [torch.cuda.Stream(device=dev) for _ in range(max(1, args.apply_streams) - 1)]
+    for st in ap_streams[1:]:
+        with torch.cuda.stream(st):
+            L.logra_reserve_workspace(ws)
+
+    def apply_phase(step_idx):
+        for st in ap_streams[1:]:
+            st.wait_stream(stream)
+        for i, m in enumerate(mats):
+            with torch.cuda.stream(ap_streams[i % len(ap_streams)]):
+                L.logra_rowadam_apply_ex(m["W"], m["S"], m["v"], m["seed"], step_idx, beta2, eps, lr, c,
+                                         m["norms"], m["Wb"], None)
+        for st in ap_streams[1:]:
+            stream.wait_stream(st)
+
+    apply_phase(args.warmup + args.steps)
+    ap_runs = []
+    for rep_i in range(3):
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        apply_phase(args.warmup + args.steps + 1 + rep_i)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        ap_runs.append(a0.elapsed_time(a1))
+    ap_conc_ms = statistics.median(ap_runs)
     elapsed_ms = t_start.elapsed_time(t_end)
     if world > 1:
         t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
@@ -401,7 +434,13 @@ def run_ours(args):
             "sketch": {"ms_per_step": sk_ms, "tflops": sk_tflops, "gbs": sk_gbs,
                        "frac_of_roofline": sk_roof_ms / sk_ms, "roofline_ms": sk_roof_ms},
             "apply": {"ms_per_step": ap_ms, "gbs": ap_gbs, "frac_hbm": ap_gbs / hbm,
-                      "frac_of_roofline": ap_roof_ms / ap_ms, "roofline_ms": ap_roof_ms},
+                      "frac_of_roofline": ap_roof_ms / ap_ms, "roofline_ms": ap_roof_ms,
+                      "all_applies_on_streams": {"streams": len(ap_streams), "ms_per_step": ap_conc_ms,
+                                                 "gbs": ap_b / (ap_conc_ms * 1e-3) / 1e9,
+                                                 "frac_hbm": ap_b / (ap_conc_ms * 1e-3) / 1e9 / hbm,
+                                                 "timing": "median of 3; every apply of a step issued "
+                                                           "round robin on the streams, events on the "
+                                                           "main stream around fork and join"}},
         },
         "roofline": roof,
         "gpu_launches": launches,
