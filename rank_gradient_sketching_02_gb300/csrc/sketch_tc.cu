@@ -1,16 +1,21 @@
 // Tensor-core sketch for bf16 inputs (tcgen05 + TMEM + TMA), three launches:
 //
-//   project   P_s^T = Sigma X_s^T for a k-range s  (D[128 tokens x r] in TMEM;
-//             A = X tile by TMA, B = Sigma tile generated in shared memory
-//             from the sign hash; k split over s for occupancy)
-//   split     P^T (partial k ranges summed by fp32 reductions into one buffer)
-//             stored as a two-term bf16 expansion
-//             P^T = hi + lo, written pre-swizzled in 32-token chunks so the
-//             next kernel loads one chunk with a single bulk copy
+//   project   P^T partial sums = Sigma X^T over a k-chunk range per segment
+//             (D[128 tokens x r] in TMEM per token tile, two token tiles per
+//             generated sign tile; A = X tile by TMA, B = Sigma tile generated
+//             in shared memory from the sign hash); segments covering a whole
+//             k range store, the others reduce-add into the zeroed P^T buffer
+//   split     P^T stored as a two-term bf16 expansion P^T = hi + lo, written
+//             pre-swizzled in 32-token chunks so the next kernel loads one
+//             chunk with a single bulk copy
 //   accumulate S += (P^T dY)^T / sqrt(r): D[r x N d-columns] in TMEM with
 //             A = P^T chunk (hi and lo, two MMAs into one accumulator),
-//             B = dY tile (MN-major, TMA), tokens split over units; each unit
-//             adds its tile into S with TMA tensor reduce-adds (fp32).
+//             B = dY tile (MN-major, TMA); each segment adds its tile into S
+//             with TMA tensor reduce-adds (fp32).
+//
+// Both tensor-core kernels split their work stream-K style: every CTA takes an
+// equal contiguous range of the flattened (tile, chunk) space (SegIter), which
+// falls into segments at tile boundaries; every segment ends in one drain.
 //
 // (theclarity.today write-up, "Why it matters": S = G A^T is accumulated during
 // backpropagation and G is never formed; academy.dair.ai summary: the random-
@@ -21,9 +26,11 @@
 // rings, so the HBM stream gets the deep ring its latency needs.
 //
 // Roles per CTA: warp 0 = producer of the first ring, warp 1 = TMEM owner +
-// MMA issuer, warps 2..5 = epilogue (TMEM lane quadrant = warp % 4), warps
-// 6..15 except 9 and 13 = sign-tile generators (project; the two skipped warps
-// share the MMA warp's scheduler) / warp 6 = dY producer (accumulate).
+// MMA issuer (one thread; its descriptors are built once per ring and advanced
+// by adds), warps 2..5 = epilogue (TMEM lane quadrant = warp % 4; the
+// accumulate adds a second group, warps 7..10), warps 6..15 except 9 and 13 =
+// sign-tile generators (project; the two skipped warps share the MMA warp's
+// scheduler) / warp 6 = dY producer (accumulate).
 // Every wait is bounded; a wait that runs out records LOGRA_ERR_TIMEOUT in the
 // control block and the CTA drains and exits.
 #include <cuda.h>
