@@ -15,7 +15,7 @@ GPU's memory.  The metric is sketch TFLOP/s over the whole step (algorithmic
 sketch FLOPs 2 n r (k + d) per matrix-microbatch, divided by the step time
 including the apply), with the apply's GB/s and both kernels' roofline
 fractions alongside.  The matrices are independent, so the step issues them
-round robin on --streams CUDA streams (default 3); per-call durations (the
+round robin on --streams CUDA streams (default 4); per-call durations (the
 components and the dominant call's roofline) come from one extra step on a
 single stream right after the timed region; the apply component also reports all of a
 step's applies issued at once on --apply-streams streams (default 7).
@@ -61,7 +61,7 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="layers27b")
     p.add_argument("--rank", type=int, default=256)
     p.add_argument("--layers", type=int, default=None, help="override the workload's layer count")
-    p.add_argument("--streams", type=int, default=3,
+    p.add_argument("--streams", type=int, default=4,
                    help="CUDA streams the matrices are issued on, round robin (each keeps its own workspace)")
     p.add_argument("--apply-streams", type=int, default=7,
                    help="streams for the all-applies-at-once measurement (each with its own workspace)")
