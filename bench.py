@@ -3,8 +3,10 @@
 every compressed matrix, then apply RowAdam from the sketch.
 
 A step covers, for each layer and each projection matrix (q, k, v, o, gate,
-up, down): zero S, one logra_sketch_accumulate per microbatch, then one
-logra_rowadam_apply_ex (fp32 master W, bf16 working copy, v, norms).  Inputs
+up, down): zero S and one logra_sketch_accumulate per microbatch; then, per
+layer, one logra_rowadam_apply_group call over the layer's seven matrices
+(fp32 master W, bf16 working copy, v, norms; --apply-mode single: one
+logra_rowadam_apply_ex per matrix instead).  Inputs
 (bf16 X and dY for every microbatch) are resident in HBM before timing; they
 are far larger than L2, so no L2 flush is needed between steps.
 
@@ -18,7 +20,7 @@ fractions alongside.  The matrices are independent, so the step issues them
 round robin on --streams CUDA streams (default 4); per-call durations (the
 components and the dominant call's roofline) come from one extra step on a
 single stream right after the timed region; the apply component also reports all of a
-step's applies issued at once on --apply-streams streams (default 7).
+step's apply calls issued at once on up to --apply-streams streams (default 7).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun (N > 1) every rank sketches its own microbatches (weak
@@ -61,10 +63,15 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="layers27b")
     p.add_argument("--rank", type=int, default=256)
     p.add_argument("--layers", type=int, default=None, help="override the workload's layer count")
+    p.add_argument("--microbatches", type=int, default=None,
+                   help="override the workload's microbatches per step (small profiling cases)")
     p.add_argument("--streams", type=int, default=4,
                    help="CUDA streams the matrices are issued on, round robin (each keeps its own workspace)")
     p.add_argument("--apply-streams", type=int, default=7,
                    help="streams for the all-applies-at-once measurement (each with its own workspace)")
+    p.add_argument("--apply-mode", choices=("group", "single"), default="group",
+                   help="group: one logra_rowadam_apply_group call per layer (its matrices in shared launches); "
+                        "single: one logra_rowadam_apply_ex call per matrix")
     p.add_argument("--e2e-steps", type=int, default=2)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -241,7 +248,7 @@ def run_ours(args):
     w = synth.WORKLOADS[args.workload]
     r = args.rank
     layers = args.layers or w.layers
-    n, nmb = w.tokens, w.microbatches
+    n, nmb = w.tokens, args.microbatches or w.microbatches
     dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     dev = torch.device("cuda", local)
     beta2, eps, lr, c = synth.BETA2, synth.EPS, synth.LR, synth.C
@@ -265,12 +272,18 @@ def run_ours(args):
                                         out_X=m["X"][mb], out_dY=m["dY"][mb])
             mats.append(m)
     torch.cuda.synchronize()
+    layer_mats = [[m for m in mats if m["layer"] == li] for li in range(layers)]
+
+    def group_items(ms):
+        return [{"W": m["W"], "S": m["S"], "v": m["v"], "seed": m["seed"], "lr": lr, "c": c,
+                 "norms_out": m["norms"], "W_bf16_out": m["Wb"]} for m in ms]
     input_bytes = sum(m["X"].numel() * m["X"].element_size() + m["dY"].numel() * m["dY"].element_size() for m in mats)
 
     stream = torch.cuda.current_stream()
     # pre-size the per-stream workspace so no allocation happens while timing
     ws = max(max(L.lib().logra_sketch_workspace_bytes(n, m["d"], m["k"], r, 1 if dt == torch.bfloat16 else 0),
                  L.lib().logra_apply_workspace_bytes(m["d"], m["k"], r)) for m in mats)
+    ws = max([ws] + [L.logra_apply_group_workspace_bytes(group_items(lm)) for lm in layer_mats])
     # The matrices are independent, so they are issued round robin on `--streams` CUDA streams (each
     # with its own library workspace): one matrix's launches fill the SMs that another's leave idle
     # in its tails and launch gaps.  Each matrix's own calls stay in order on one stream.
@@ -279,33 +292,48 @@ def run_ours(args):
         with torch.cuda.stream(st):
             L.logra_reserve_workspace(ws)
 
+    def timed(ev, kind, st, fn, *tag):
+        if ev is None:
+            fn()
+            return
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        fn()
+        b.record(st)
+        ev[kind].append((a, b) + tag)
+
     def one_step(step_idx, ev=None, sts=None):
         sts = sts or streams
         for st in sts[1:]:
             st.wait_stream(stream)
-        for i, m in enumerate(mats):
-            st = sts[i % len(sts)]
-            with torch.cuda.stream(st):
-                m["S"].zero_()
-                for mb in range(nmb):
-                    if ev is not None:
-                        a = torch.cuda.Event(enable_timing=True)
-                        b = torch.cuda.Event(enable_timing=True)
-                        a.record(st)
-                    L.logra_sketch_accumulate(m["X"][mb], m["dY"][mb], m["S"], m["seed"], step_idx)
-                    if ev is not None:
-                        b.record(st)
-                        ev["sketch"].append((a, b, m["d"], m["k"]))
-                dp.allreduce_sketch(m["S"])
-                if ev is not None:
-                    a = torch.cuda.Event(enable_timing=True)
-                    b = torch.cuda.Event(enable_timing=True)
-                    a.record(st)
-                L.logra_rowadam_apply_ex(m["W"], m["S"], m["v"], m["seed"], step_idx, beta2, eps, lr, c,
-                                         m["norms"], m["Wb"], None)
-                if ev is not None:
-                    b.record(st)
-                    ev["apply"].append((a, b, m["d"], m["k"]))
+        i = 0
+        for li, lm in enumerate(layer_mats):
+            used = []
+            for m in lm:
+                st = sts[i % len(sts)]
+                i += 1
+                used.append(st)
+                with torch.cuda.stream(st):
+                    m["S"].zero_()
+                    for mb in range(nmb):
+                        timed(ev, "sketch", st, lambda: L.logra_sketch_accumulate(
+                            m["X"][mb], m["dY"][mb], m["S"], m["seed"], step_idx), m["d"], m["k"])
+                    dp.allreduce_sketch(m["S"])
+                    if args.apply_mode == "single":
+                        timed(ev, "apply", st, lambda: L.logra_rowadam_apply_ex(
+                            m["W"], m["S"], m["v"], m["seed"], step_idx, beta2, eps, lr, c, m["norms"], m["Wb"],
+                            None), m["d"], m["k"])
+            if args.apply_mode == "group":
+                # the layer's applies as one call, on the stream of its last matrix, once all of the
+                # layer's sketches (on the other streams) are done
+                ast = used[-1]
+                for st in set(used):
+                    if st is not ast:
+                        ast.wait_stream(st)
+                with torch.cuda.stream(ast):
+                    timed(ev, "apply", ast, lambda: L.logra_rowadam_apply_group(
+                        group_items(lm), step_idx, beta2, eps), li, len(lm))
         for st in sts[1:]:
             stream.wait_stream(st)
 
@@ -354,10 +382,15 @@ def run_ours(args):
     def apply_phase(step_idx):
         for st in ap_streams[1:]:
             st.wait_stream(stream)
-        for i, m in enumerate(mats):
-            with torch.cuda.stream(ap_streams[i % len(ap_streams)]):
-                L.logra_rowadam_apply_ex(m["W"], m["S"], m["v"], m["seed"], step_idx, beta2, eps, lr, c,
-                                         m["norms"], m["Wb"], None)
+        if args.apply_mode == "group":
+            for li, lm in enumerate(layer_mats):
+                with torch.cuda.stream(ap_streams[li % len(ap_streams)]):
+                    L.logra_rowadam_apply_group(group_items(lm), step_idx, beta2, eps)
+        else:
+            for i, m in enumerate(mats):
+                with torch.cuda.stream(ap_streams[i % len(ap_streams)]):
+                    L.logra_rowadam_apply_ex(m["W"], m["S"], m["v"], m["seed"], step_idx, beta2, eps, lr, c,
+                                             m["norms"], m["Wb"], None)
         for st in ap_streams[1:]:
             stream.wait_stream(st)
 
@@ -427,7 +460,7 @@ def run_ours(args):
         "config": {"workload": w.name, "layers": layers, "matrices": [list(x) for x in w.matrices],
                    "microbatches": nmb, "tokens": n, "r": r, "mask_frac": w.mask_frac,
                    "input_bytes_resident": input_bytes, "l2": "inputs larger than L2, no flush",
-                   "parallelism": f"dp{world}", "streams": len(streams),
+                   "parallelism": f"dp{world}", "streams": len(streams), "apply_mode": args.apply_mode,
                    "component_timing": "components and roofline: CUDA events around each call in one "
                    "extra step issued on a single stream right after the timed region"},
         "components": {
@@ -435,10 +468,12 @@ def run_ours(args):
                        "frac_of_roofline": sk_roof_ms / sk_ms, "roofline_ms": sk_roof_ms},
             "apply": {"ms_per_step": ap_ms, "gbs": ap_gbs, "frac_hbm": ap_gbs / hbm,
                       "frac_of_roofline": ap_roof_ms / ap_ms, "roofline_ms": ap_roof_ms,
-                      "all_applies_on_streams": {"streams": len(ap_streams), "ms_per_step": ap_conc_ms,
+                      "calls_per_step": len(ev["apply"]),
+                      "all_applies_on_streams": {"streams": min(len(ap_streams), len(ev["apply"])),
+                                                 "ms_per_step": ap_conc_ms,
                                                  "gbs": ap_b / (ap_conc_ms * 1e-3) / 1e9,
                                                  "frac_hbm": ap_b / (ap_conc_ms * 1e-3) / 1e9 / hbm,
-                                                 "timing": "median of 3; every apply of a step issued "
+                                                 "timing": "median of 3; every apply call of a step issued "
                                                            "round robin on the streams, events on the "
                                                            "main stream around fork and join"}},
         },
@@ -450,7 +485,7 @@ def run_ours(args):
 
     # ---- end to end through the public API from pinned host memory
     if not args.no_e2e:
-        line["e2e"] = run_e2e(args, L, dp, mats, w, r, dt, dev, stream, sk_f, world)
+        line["e2e"] = run_e2e(args, L, dp, mats, w, r, dt, dev, stream, sk_f, world, layer_mats, group_items)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = time_oracle(w, r, args.cpu_seconds)
@@ -461,13 +496,13 @@ def run_ours(args):
     return 0
 
 
-def run_e2e(args, L, dp, mats, w, r, dt, dev, stream, sk_f, world):
+def run_e2e(args, L, dp, mats, w, r, dt, dev, stream, sk_f, world, layer_mats, group_items):
     """Same step, but every microbatch's X and dY come from pinned host memory
     (copied on a side stream, double-buffered) and the norms go back to the host."""
     import torch
     from rank_gradient_sketching_02_gb300 import synth
     beta2, eps, lr, c = synth.BETA2, synth.EPS, synth.LR, synth.C
-    n, nmb = w.tokens, w.microbatches
+    n, nmb = w.tokens, args.microbatches or w.microbatches
     host = {}
     for m in mats:
         key = (m["d"], m["k"])
@@ -487,6 +522,7 @@ def run_e2e(args, L, dp, mats, w, r, dt, dev, stream, sk_f, world):
         done = [None, None]
         i = 0
         for mi, m in enumerate(mats):
+            lm = layer_mats[m["layer"]]
             Xh, Yh = host[(m["d"], m["k"])]
             m["S"].zero_()
             for mb in range(nmb):
@@ -513,10 +549,15 @@ def run_e2e(args, L, dp, mats, w, r, dt, dev, stream, sk_f, world):
                 done[slot] = ev
                 i += 1
             dp.allreduce_sketch(m["S"])
-            L.logra_rowadam_apply_ex(m["W"], m["S"], m["v"], m["seed"], step_idx, beta2, eps, lr, c,
-                                     m["norms"], m["Wb"], None)
-            norms_h[mi].copy_(m["norms"], non_blocking=True)
-            d2h += 16
+            if args.apply_mode == "single":
+                L.logra_rowadam_apply_ex(m["W"], m["S"], m["v"], m["seed"], step_idx, beta2, eps, lr, c,
+                                         m["norms"], m["Wb"], None)
+            elif m is lm[-1]:
+                L.logra_rowadam_apply_group(group_items(lm), step_idx, beta2, eps)
+            if args.apply_mode == "single" or m is lm[-1]:
+                for mm in ([m] if args.apply_mode == "single" else lm):
+                    norms_h[mats.index(mm)].copy_(mm["norms"], non_blocking=True)
+                    d2h += 16
         return norms_h
 
     e2e_step(10_000)

@@ -150,6 +150,48 @@ int logra_rowadam_apply_ex(float* W, const float* S, float* v, int64_t d,
                            float* sync_sketch_out, logra_stream_t stream);
 
 /*
+ * logra_apply_item -- one matrix of logra_rowadam_apply_group: the arguments of
+ * logra_rowadam_apply_ex that differ between matrices.  Device pointers as
+ * there; norms_out, W_bf16_out and sync_sketch_out may be NULL.
+ */
+typedef struct logra_apply_item {
+  float* W;                 /* d x k fp32 master weight, updated in place */
+  const float* S;           /* d x r fp32 sketch (read only)              */
+  float* v;                 /* d fp32 second moment, updated in place     */
+  int64_t d, k;
+  uint64_t seed;            /* this matrix's seed (A is drawn per matrix) */
+  float lr, c;
+  double* norms_out;        /* 2 doubles: {||S||_F^2, ||dW||_F^2}         */
+  uint16_t* W_bf16_out;     /* d x k bf16 copy of the updated W           */
+  float* sync_sketch_out;   /* d x r, S'_i = -lr c S_i / sqrt(v_i + eps)  */
+} logra_apply_item;
+
+/*
+ * logra_rowadam_apply_group -- logra_rowadam_apply_ex for `count` matrices of
+ * one rank r and one step: every output equals what `count` separate
+ * logra_rowadam_apply_ex calls write (W, v, the bf16 copy and the sync sketch
+ * bit for bit; the norms up to the order of their fp64 partial sums).
+ *   items   HOST array of `count` items, read during the call only.  The
+ *           matrices must not overlap in memory.
+ * The matrices are processed in launch groups of up to 8: each group is one
+ * preparation launch, one row-norm launch and one update launch whose work
+ * units span all of the group's matrices, so small matrices (attention
+ * projections of a layer) share the GPU with large ones instead of each
+ * paying its own pipeline fill and tail (the update is the fused
+ * reconstruct-and-update pass of the theclarity.today write-up, "What
+ * happened").  Workspace: logra_apply_group_workspace_bytes(items, count, r)
+ * bytes of the stream's scratch.  count == 0 is a no-op.
+ */
+int logra_rowadam_apply_group(const logra_apply_item* items, int count, int r,
+                              uint64_t step, float beta2, float eps,
+                              logra_stream_t stream);
+
+/* Workspace bytes logra_rowadam_apply_group needs for these items (0 if an
+ * item's shape is invalid). */
+size_t logra_apply_group_workspace_bytes(const logra_apply_item* items,
+                                         int count, int r);
+
+/*
  * logra_rowadam_predict -- the norms logra_rowadam_apply would report with
  * c = 1, writing nothing else (W and v untouched).  Because dW is linear in c,
  * ||dW(c)||^2 = c^2 * norms_out[1]; a controller can pick c from this before

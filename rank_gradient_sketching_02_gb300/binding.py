@@ -39,6 +39,17 @@ SIGNATURES = {
     "logra_noalloc_scratch_bytes": (_SZ, []),
 }
 
+
+
+class logra_apply_item(C.Structure):
+    """One matrix of logra_rowadam_apply_group (the C struct of the same name)."""
+    _fields_ = [("W", _VP), ("S", _VP), ("v", _VP), ("d", _I64), ("k", _I64), ("seed", _U64),
+                ("lr", _F), ("c", _F), ("norms_out", _VP), ("W_bf16_out", _VP), ("sync_sketch_out", _VP)]
+
+
+SIGNATURES["logra_rowadam_apply_group"] = (_I, [C.POINTER(logra_apply_item), _I, _I, _U64, _F, _F, _VP])
+SIGNATURES["logra_apply_group_workspace_bytes"] = (_SZ, [C.POINTER(logra_apply_item), _I, _I])
+
 _lib = None
 _lock = threading.Lock()
 
@@ -153,6 +164,42 @@ def logra_rowadam_apply_ex(W, S, v, seed: int, step: int, beta2: float, eps: flo
     _check(lib().logra_rowadam_apply_ex(pw, ps, pv, d, k, r, seed, step, beta2, eps, lr, c, pn, pb, pq,
                                         _stream(stream)), "logra_rowadam_apply_ex")
     return W
+
+
+def _apply_items(items):
+    """items: sequence of dicts with W, S, v, seed, lr, c and optional norms_out, W_bf16_out,
+    sync_sketch_out (CUDA tensors as for logra_rowadam_apply_ex).  Returns (ctypes array, r)."""
+    import torch
+    f32 = (torch.float32,)
+    arr = (logra_apply_item * max(1, len(items)))()
+    r = None
+    for i, m in enumerate(items):
+        W, S, v = m["W"], m["S"], m["v"]
+        d, k = W.shape
+        if r is None:
+            r = S.shape[1]
+        elif S.shape[1] != r:
+            raise ValueError("every matrix of a group has the same rank r")
+        nm, wb, sq = m.get("norms_out"), m.get("W_bf16_out"), m.get("sync_sketch_out")
+        arr[i] = logra_apply_item(
+            _dev(W, "W", f32), _dev(S, "S", f32, (d, r)), _dev(v, "v", f32, (d,)), d, k, int(m["seed"]),
+            float(m["lr"]), float(m["c"]),
+            _dev(nm, "norms_out", (torch.float64,), (2,)) if nm is not None else None,
+            _dev(wb, "W_bf16_out", (torch.bfloat16,), (d, k)) if wb is not None else None,
+            _dev(sq, "sync_sketch_out", f32, (d, r)) if sq is not None else None)
+    return arr, (r if r is not None else 32)
+
+
+def logra_rowadam_apply_group(items, step: int, beta2: float, eps: float, stream=None):
+    """logra_rowadam_apply_ex over several matrices of one rank in grouped launches."""
+    arr, r = _apply_items(items)
+    _check(lib().logra_rowadam_apply_group(arr, len(items), r, step, beta2, eps, _stream(stream)),
+           "logra_rowadam_apply_group")
+
+
+def logra_apply_group_workspace_bytes(items) -> int:
+    arr, r = _apply_items(items)
+    return int(lib().logra_apply_group_workspace_bytes(arr, len(items), r))
 
 
 def logra_rowadam_predict(S, v, k: int, seed: int, step: int, beta2: float, eps: float, lr: float,

@@ -55,7 +55,7 @@ struct Buffer {
   void* ptr = nullptr;
   size_t bytes = 0;
   unsigned* counters = nullptr;   // kCounterWords zero-initialised words, never freed while the stream's entry lives
-  int* gram = nullptr;            // 512 x 512 Gram counts, zero between applies
+  int* gram = nullptr;            // kGramCountInts Gram counts, zero between applies
 };
 std::map<std::pair<int, cudaStream_t>, Buffer> g_ws;
 
@@ -132,7 +132,7 @@ int* gram_counts(cudaStream_t stream, int* status) {
   Buffer& b = g_ws[std::make_pair(dev, stream)];
   if (!b.gram) {
     void* p = nullptr;
-    const size_t bytes = size_t(512) * 512 * sizeof(int);
+    const size_t bytes = kGramCountInts * sizeof(int);
     cudaError_t e = cudaMalloc(&p, bytes);
     if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, bytes, stream);   // ordered before its first user
     if (e != cudaSuccess) {
@@ -288,9 +288,35 @@ static int rowadam_common(int mode, float* W, const float* S, float* v, int64_t 
   if (st) return st;
   Control* ctl = control_block(&st);
   if (!ctl) return st;
-  return launch_rowadam(mode, W, reinterpret_cast<__nv_bfloat16*>(W_bf16_out), nullptr, 0, S, v,
-                        mode == 0 ? v : nullptr, mode == 0 ? sync_out : nullptr, d, k, r, step_key(seed, step), beta2,
-                        eps, lr * c, norms_out, ws, ctl, stream);
+  RowAdamItem it{};
+  it.W = W;
+  it.Wb = reinterpret_cast<__nv_bfloat16*>(W_bf16_out);
+  it.S = S;
+  it.v_in = v;
+  it.v_out = mode == 0 ? v : nullptr;
+  it.sync_out = mode == 0 ? sync_out : nullptr;
+  it.d = d;
+  it.k = k;
+  it.key = step_key(seed, step);
+  it.lrc = lr * c;
+  it.norms = norms_out;
+  it.ws = ws;
+  return launch_rowadam(mode, &it, 1, r, beta2, eps, 0, ctl, stream);
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Workspace of the largest run of up to kMaxGroup consecutive items (the
+// items of one launch group lie side by side, each 256-byte aligned).
+static size_t group_workspace_bytes(const logra_apply_item* items, int count, int r) {
+  size_t best = 0;
+  for (int g = 0; g < count; g += kMaxGroup) {
+    size_t sum = 0;
+    for (int i = g; i < count && i < g + kMaxGroup; ++i)
+      sum += align256(apply_workspace_layout(items[i].d, items[i].k, r).bytes);
+    if (sum > best) best = sum;
+  }
+  return best;
 }
 
 int logra_rowadam_apply(float* W, const float* S, float* v, int64_t d, int64_t k, int r, uint64_t seed,
@@ -327,8 +353,64 @@ int logra_reconstruct(const float* S, int64_t d, int64_t k, int r, uint64_t seed
   if (st) return st;
   Control* ctl = control_block(&st);
   if (!ctl) return st;
-  return launch_rowadam(out_dtype == LOGRA_F32 ? 2 : 3, nullptr, nullptr, dW_out, accumulate, S, nullptr, nullptr,
-                        nullptr, d, k, r, step_key(seed, step), 0.f, 0.f, 0.f, nullptr, ws, ctl, stream);
+  RowAdamItem it{};
+  it.out = dW_out;
+  it.S = S;
+  it.d = d;
+  it.k = k;
+  it.key = step_key(seed, step);
+  it.ws = ws;
+  return launch_rowadam(out_dtype == LOGRA_F32 ? 2 : 3, &it, 1, r, 0.f, 0.f, accumulate, ctl, stream);
+}
+
+size_t logra_apply_group_workspace_bytes(const logra_apply_item* items, int count, int r) {
+  if (!items || count <= 0 || check_rank(r)) return 0;
+  for (int i = 0; i < count; ++i)
+    if (items[i].d <= 0 || items[i].k <= 0) return 0;
+  return group_workspace_bytes(items, count, r);
+}
+
+int logra_rowadam_apply_group(const logra_apply_item* items, int count, int r, uint64_t step, float beta2, float eps,
+                              logra_stream_t stream) {
+  if (count < 0 || (count > 0 && !items)) return LOGRA_ERR_INVALID_ARG;
+  if (check_rank(r)) return LOGRA_ERR_UNSUPPORTED;
+  for (int i = 0; i < count; ++i) {
+    const logra_apply_item& m = items[i];
+    if (!m.W || !m.S || !m.v) return LOGRA_ERR_INVALID_ARG;
+    if (int st = check_mat(m.d, m.k)) return st;
+    if (!aligned16(m.W) || !aligned16(m.S) || !aligned16(m.v) || (m.W_bf16_out && !aligned16(m.W_bf16_out)) ||
+        (m.sync_sketch_out && !aligned16(m.sync_sketch_out)) || (m.norms_out && !aligned16(m.norms_out)))
+      return LOGRA_ERR_UNSUPPORTED;
+  }
+  if (count == 0) return LOGRA_OK;
+  int st;
+  char* ws = static_cast<char*>(workspace(stream, group_workspace_bytes(items, count, r), &st));
+  if (st) return st;
+  Control* ctl = control_block(&st);
+  if (!ctl) return st;
+  for (int g = 0; g < count; g += kMaxGroup) {
+    const int n = count - g < kMaxGroup ? count - g : kMaxGroup;
+    RowAdamItem it[kMaxGroup] = {};
+    size_t off = 0;
+    for (int i = 0; i < n; ++i) {
+      const logra_apply_item& m = items[g + i];
+      it[i].W = m.W;
+      it[i].Wb = reinterpret_cast<__nv_bfloat16*>(m.W_bf16_out);
+      it[i].S = m.S;
+      it[i].v_in = m.v;
+      it[i].v_out = m.v;
+      it[i].sync_out = m.sync_sketch_out;
+      it[i].d = m.d;
+      it[i].k = m.k;
+      it[i].key = step_key(m.seed, step);
+      it[i].lrc = m.lr * m.c;
+      it[i].norms = m.norms_out;
+      it[i].ws = ws + off;
+      off += align256(apply_workspace_layout(m.d, m.k, r).bytes);
+    }
+    if (int e = launch_rowadam(0, it, n, r, beta2, eps, 0, ctl, stream)) return e;
+  }
+  return LOGRA_OK;
 }
 
 int logra_get_status(logra_stream_t stream) {

@@ -65,7 +65,7 @@ struct ApplyShared {
   uint32_t tmem_base;
   int abort;
   int flag;
-  double red[8];
+  double red[kMaxGroup][8];   // per matrix, per epilogue warp: this CTA's partial sum
 };
 
 constexpr size_t kApplySmem = 1024 + kAbStages * (kABytes + kBBytes) + kWStages * kWBytes + 2 * kWBytes + 2 * kHBytes +
@@ -84,19 +84,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 
 }  // namespace
 
-struct ApplyArgs {
+// One matrix of a launch.
+struct ApplyMat {
   int64_t d, k;
-  int r;
   int nsuper;                 // super-tiles per row block (columns of W; mode 4: of M)
   int units;                  // modes 0-3: row blocks x super-tiles; mode 4: row blocks
-  int inner;                  // super-tiles per unit: 1, or nsuper in mode 4
-  int nck;                    // 64-rank chunks
   uint64_t key;
   float neg_lrc_scale;        // -lr c / sqrt(r)   (apply, predict)
-  float scale;                // 1 / sqrt(r)       (rebuild)
   float neg_lrc;              // -lr c             (mode 4 sync sketch)
-  float beta2, eps;
-  int accumulate;             // rebuild: add into the output
   int write_bf16;             // apply: also store the bf16 copy
   const uint8_t* s_image;     // [row block][rank chunk][hi | lo][128 rows][128 B]
   const uint8_t* m_image;     // [super-tile][rank chunk][hi, lo][32 KB]
@@ -108,15 +103,38 @@ struct ApplyArgs {
   double* part;               // one per CTA
   double* norms;              // modes 0, 1 (nullable): {||S||^2, ||dW||^2} from the last CTA
   const double* ssq;          // mode 4's ||S||^2 partials
-  int nssq;
-  unsigned* counter;          // CTAs finished, wrapping to 0 after the last one
 };
+
+// A launch over up to kMaxGroup matrices of the same rank: their work units
+// (row block x super-tile; mode 4: row block) are numbered one matrix after
+// another and dealt round robin to the persistent CTAs, so small matrices
+// share the machine with large ones instead of each paying its own fill and
+// tail.  Passed as one __grid_constant__ parameter block (about 5 KB).
+struct ApplyArgs {
+  CUtensorMap tm[kMaxGroup][4];   // fp32 load (128 rows), bf16 load, fp32 store (32 rows), bf16 store
+  ApplyMat m[kMaxGroup];
+  int ustart[kMaxGroup + 1];      // first unit of each matrix; ustart[nm] = all units
+  int nm;
+  int r;
+  int inner;                  // super-tiles per unit: 1, or nsuper in mode 4
+  int nck;                    // 64-rank chunks
+  float scale;                // 1 / sqrt(r)       (rebuild)
+  float beta2, eps;
+  int accumulate;             // rebuild: add into the output
+  int nssq;                   // mode 4's grid: partials per matrix in ssq
+  unsigned* counter;          // CTAs finished, wrapping to 0 after the last one (null: no norms)
+};
+
+// Matrix of unit u (units are numbered matrix by matrix).
+__device__ __forceinline__ int mat_of(const ApplyArgs& A, int u) {
+  int m = 0;
+  while (m + 1 < A.nm && u >= A.ustart[m + 1]) ++m;
+  return m;
+}
 
 template <int MODE>
 __global__ void __launch_bounds__(480, 1)
-    apply_tc_kernel(const __grid_constant__ CUtensorMap tmap_f32, const __grid_constant__ CUtensorMap tmap_b16,
-                    const __grid_constant__ CUtensorMap tmap_f32s, const __grid_constant__ CUtensorMap tmap_b16s,
-                    ApplyArgs A, Control* ctl) {
+    apply_tc_kernel(const __grid_constant__ ApplyArgs A, Control* ctl) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   uint8_t* ab = base;                                              // [stage][A 32 KB | B 32 KB]
@@ -132,6 +150,7 @@ __global__ void __launch_bounds__(480, 1)
   // tile, or (mode 4) both terms of the Gram image, so each S chunk loads once
   constexpr uint32_t kStageB = kNorm ? kABytes + 2 * kBBytes : kABytes + kBBytes;
   const int nchunks = A.nck;
+  const int units = A.ustart[A.nm];
   const bool load_in = (MODE == 0) || ((MODE == 2 || MODE == 3) && A.accumulate);
 
   if (threadIdx.x == 0) {
@@ -150,14 +169,17 @@ __global__ void __launch_bounds__(480, 1)
     }
     mbar_init(&sh->drain, 1);
     sh->abort = 0;
+    for (int i = 0; i < kMaxGroup * 8; ++i) sh->red[i / 8][i % 8] = 0.0;
     fence_mbar_init();
-    if (MODE == 0 || MODE == 2) {
-      prefetch_tmap(&tmap_f32);
-      prefetch_tmap(&tmap_f32s);
-    }
-    if ((MODE == 0 && A.write_bf16) || MODE == 3) {
-      prefetch_tmap(&tmap_b16);
-      prefetch_tmap(&tmap_b16s);
+    for (int mi = 0; mi < A.nm; ++mi) {
+      if (MODE == 0 || MODE == 2) {
+        prefetch_tmap(&A.tm[mi][0]);
+        prefetch_tmap(&A.tm[mi][2]);
+      }
+      if ((MODE == 0 && A.m[mi].write_bf16) || MODE == 3) {
+        prefetch_tmap(&A.tm[mi][1]);
+        prefetch_tmap(&A.tm[mi][3]);
+      }
     }
   }
   if (warp == 1) {
@@ -175,10 +197,12 @@ __global__ void __launch_bounds__(480, 1)
       int stage = 0;
       uint32_t phase = 0;
       int inject = ctl->inject_fault && blockIdx.x == 0;
-      for (int u = blockIdx.x; u < A.units; u += gridDim.x) {
+      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const int mi = mat_of(A, u), lu = u - A.ustart[mi];
+        const ApplyMat& M = A.m[mi];
         for (int t = 0; t < A.inner; ++t) {
-          const int rb = kNorm ? u : u / A.nsuper;
-          const int st = kNorm ? t : u % A.nsuper;
+          const int rb = kNorm ? lu : lu / M.nsuper;
+          const int st = kNorm ? t : lu % M.nsuper;
           for (int c = 0; c < nchunks; ++c) {
             if (!wait_or_abort(sh, &sh->ab_empty[stage], phase ^ 1u, limit, ctl)) goto a_done;
             uint8_t* dst = ab + stage * kStageB;
@@ -186,9 +210,9 @@ __global__ void __launch_bounds__(480, 1)
               inject = 0;
             } else {
               mbar_arrive_expect_tx(&sh->ab_full[stage], kNorm ? kStageB : kABytes);
-              bulk_load(dst, A.s_image + (size_t(rb) * A.nck + c) * kABytes, kABytes, &sh->ab_full[stage]);
+              bulk_load(dst, M.s_image + (size_t(rb) * A.nck + c) * kABytes, kABytes, &sh->ab_full[stage]);
               if (kNorm)   // M_hi and M_lo of this chunk are adjacent in the image
-                bulk_load(dst + kABytes, A.m_image + (size_t(st) * A.nck + c) * 2 * kBBytes, 2 * kBBytes,
+                bulk_load(dst + kABytes, M.m_image + (size_t(st) * A.nck + c) * 2 * kBBytes, 2 * kBBytes,
                           &sh->ab_full[stage]);
             }
             if (++stage == AS) { stage = 0; phase ^= 1u; }
@@ -204,12 +228,13 @@ __global__ void __launch_bounds__(480, 1)
       int stage = 0;
       uint32_t phase = 0;
       const uint32_t bytes = (MODE == 3) ? kHBytes : kWBytes;
-      const CUtensorMap* map = (MODE == 3) ? &tmap_b16 : &tmap_f32;
-      for (int u = blockIdx.x; u < A.units; u += gridDim.x) {
-        const int rb = u / A.nsuper, st = u % A.nsuper;
+      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const int mi = mat_of(A, u), lu = u - A.ustart[mi];
+        const CUtensorMap* map = &A.tm[mi][MODE == 3 ? 1 : 0];
+        const int rb = lu / A.m[mi].nsuper, st = lu % A.m[mi].nsuper;
         for (int s = 0; s < kCols / kSub; ++s) {
           const int64_t col0 = int64_t(st) * kCols + s * kSub;
-          if (col0 >= A.k) break;
+          if (col0 >= A.m[mi].k) break;
           if (!wait_or_abort(sh, &sh->w_empty[stage], phase ^ 1u, limit, ctl)) goto w_done;
           mbar_arrive_expect_tx(&sh->w_full[stage], bytes);
           tma_load_2d(wr + stage * kWBytes, map, &sh->w_full[stage], int32_t(col0), rb * kRows);
@@ -230,7 +255,7 @@ __global__ void __launch_bounds__(480, 1)
       // stage-0 descriptors, advanced by adds of the 16-byte-unit address field
       const uint64_t adesc0 = smem_desc(smem_addr(ab), 16, 1024, kSw128);
       const uint64_t bdesc0 = smem_desc(smem_addr(ab + kABytes), kRc * 128, 1024, kSw128);
-      for (int u = blockIdx.x; u < A.units && !sh->abort; u += gridDim.x) {
+      for (int u = blockIdx.x; u < units && !sh->abort; u += gridDim.x) {
         for (int t = 0; t < A.inner; ++t) {
           if (!wait_or_abort(sh, &sh->tmem_empty[buf], tph[buf] ^ 1u, limit, ctl)) goto mma_done;
           tc_fence_after();
@@ -280,19 +305,32 @@ __global__ void __launch_bounds__(480, 1)
     int buf = 0;
     int wstage = 0;
     uint32_t wphase = 0;
-    double acc_cta = 0.0;                                // dW^2 (modes 0, 1) or ||S||^2 (mode 4)
+    double acc_cta = 0.0;   // the current matrix's dW^2 (modes 0, 1) or ||S||^2 (mode 4)
+    int cur = -1;           // the matrix acc_cta belongs to
     bool aborted = false;
-    for (int u = blockIdx.x; u < A.units && !aborted && grp < ngrp; u += gridDim.x) {
-      const int rb = kNorm ? u : u / A.nsuper;
+    // the warp's partial of one matrix, summed over its lanes in a fixed order
+    auto flush = [&]() {
+      for (int o = 16; o; o >>= 1) acc_cta += __shfl_xor_sync(0xffffffffu, acc_cta, o);
+      if (lane == 0 && cur >= 0) sh->red[cur][eidx] = acc_cta;
+      acc_cta = 0.0;
+    };
+    for (int u = blockIdx.x; u < units && !aborted && grp < ngrp; u += gridDim.x) {
+      const int mi = mat_of(A, u), lu = u - A.ustart[mi];
+      const ApplyMat& M = A.m[mi];
+      if (mi != cur) {    // units come in increasing order, so a matrix's units are contiguous here
+        flush();
+        cur = mi;
+      }
+      const int rb = kNorm ? lu : lu / M.nsuper;
       const int64_t row = int64_t(rb) * kRows + row_l;
-      const bool row_ok = row < A.d;
+      const bool row_ok = row < M.d;
       double q = 0.0;                                    // mode 4: S_i M S_i^T over the row
       for (int t = 0; t < A.inner && !aborted; ++t) {
-        const int st = kNorm ? t : u % A.nsuper;
+        const int st = kNorm ? t : lu % M.nsuper;
         // row norms: the first S slice is fetched while the MMAs still run
         float4 snext[8];
         if (MODE == 4 && row_ok) {
-          const float4* sp = reinterpret_cast<const float4*>(A.S + row * A.r + int64_t(st) * kCols);
+          const float4* sp = reinterpret_cast<const float4*>(M.S + row * A.r + int64_t(st) * kCols);
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) snext[q4] = sp[q4];
         }
@@ -300,9 +338,9 @@ __global__ void __launch_bounds__(480, 1)
         tph[buf] ^= 1u;
         tc_fence_after();
         float f = 0.f;
-        if (MODE == 0 || MODE == 1) f = row_ok ? A.neg_lrc_scale * A.inv[row] : 0.f;
+        if (MODE == 0 || MODE == 1) f = row_ok ? M.neg_lrc_scale * M.inv[row] : 0.f;
         else f = A.scale;
-        const int64_t ncols_total = kNorm ? int64_t(A.r) : A.k;
+        const int64_t ncols_total = kNorm ? int64_t(A.r) : M.k;
         for (int s = 0; s < kCols / kSub; ++s) {
           const int64_t col0 = int64_t(st) * kCols + s * kSub;
           if (col0 >= ncols_total) break;
@@ -324,7 +362,7 @@ __global__ void __launch_bounds__(480, 1)
 #pragma unroll
               for (int q4 = 0; q4 < 8; ++q4) scur[q4] = snext[q4];
               if (col0 + kSub < ncols_total && s + 1 < kCols / kSub) {
-                const float4* sp = reinterpret_cast<const float4*>(A.S + row * A.r + col0 + kSub);
+                const float4* sp = reinterpret_cast<const float4*>(M.S + row * A.r + col0 + kSub);
 #pragma unroll
                 for (int q4 = 0; q4 < 8; ++q4) snext[q4] = sp[q4];
               }
@@ -405,7 +443,7 @@ __global__ void __launch_bounds__(480, 1)
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4)
               *reinterpret_cast<float4*>(st + row_l * 128 + ((q4 ^ (row_l & 7)) << 4)) = w[q4];
-            if (MODE == 0 && A.write_bf16) {
+            if (MODE == 0 && M.write_bf16) {
               // bf16 staging: 64-byte rows, 16-byte chunk h at h ^ ((row >> 1) & 3)
 #pragma unroll
               for (int h = 0; h < 4; ++h)
@@ -436,8 +474,8 @@ __global__ void __launch_bounds__(480, 1)
           __syncwarp();
           if (lane == 0) {
             const int32_t r0 = rb * kRows + quad * 32;
-            if (MODE == 0 || MODE == 2) tma_store_2d(&tmap_f32s, st + quad * (32 * 128), int32_t(col0), r0);
-            if ((MODE == 0 && A.write_bf16) || MODE == 3) tma_store_2d(&tmap_b16s, ht + quad * (32 * 64), int32_t(col0), r0);
+            if (MODE == 0 || MODE == 2) tma_store_2d(&A.tm[mi][2], st + quad * (32 * 128), int32_t(col0), r0);
+            if ((MODE == 0 && M.write_bf16) || MODE == 3) tma_store_2d(&A.tm[mi][3], ht + quad * (32 * 64), int32_t(col0), r0);
             bulk_commit();          // in flight until the group's next sub-tile
           }
           __syncwarp();
@@ -451,15 +489,15 @@ __global__ void __launch_bounds__(480, 1)
         buf ^= 1;
       }
       if (MODE == 4 && !aborted && row_ok) {
-        const float mean_sq = float(q) / (float(A.r) * float(A.k));
-        const float vn = A.beta2 * A.v_in[row] + (1.f - A.beta2) * mean_sq;
-        if (A.v_out) A.v_out[row] = vn;
+        const float mean_sq = float(q) / (float(A.r) * float(M.k));
+        const float vn = A.beta2 * M.v_in[row] + (1.f - A.beta2) * mean_sq;
+        if (M.v_out) M.v_out[row] = vn;
         const float inv = 1.f / sqrtf(vn + A.eps);
-        A.inv[row] = inv;
-        if (A.sync_out) {
-          const float fs = A.neg_lrc * inv;
-          const float4* sp = reinterpret_cast<const float4*>(A.S + row * A.r);
-          float4* op = reinterpret_cast<float4*>(A.sync_out + row * A.r);
+        M.inv[row] = inv;
+        if (M.sync_out) {
+          const float fs = M.neg_lrc * inv;
+          const float4* sp = reinterpret_cast<const float4*>(M.S + row * A.r);
+          float4* op = reinterpret_cast<float4*>(M.sync_out + row * A.r);
           for (int b = 0; b < A.r / 4; ++b) {
             const float4 sv = sp[b];
             op[b] = make_float4(fs * sv.x, fs * sv.y, fs * sv.z, fs * sv.w);
@@ -469,34 +507,37 @@ __global__ void __launch_bounds__(480, 1)
     }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
-    // per-CTA partial sum, fixed order
-    for (int o = 16; o; o >>= 1) acc_cta += __shfl_xor_sync(0xffffffffu, acc_cta, o);
-    if (lane == 0) sh->red[eidx] = acc_cta;
+    flush();
     epi_sync();
-    if (et == 0 && (MODE == 0 || MODE == 1 || MODE == 4))
-      A.part[blockIdx.x] = ((sh->red[0] + sh->red[1]) + (sh->red[2] + sh->red[3])) +
-                           ((sh->red[4] + sh->red[5]) + (sh->red[6] + sh->red[7]));
-    if ((MODE == 0 || MODE == 1) && A.norms && warp == 2) {
-      // The last CTA to finish sums every CTA's partial (and mode 4's) in a
-      // fixed order: deterministic, and no separate reduction launch.
+    // this CTA's partial of each matrix (zero for one it had no unit of), fixed order
+    if ((MODE == 0 || MODE == 1 || MODE == 4) && et < A.nm) {
+      const double* rd = sh->red[et];
+      A.m[et].part[blockIdx.x] = ((rd[0] + rd[1]) + (rd[2] + rd[3])) + ((rd[4] + rd[5]) + (rd[6] + rd[7]));
+    }
+    if ((MODE == 0 || MODE == 1) && A.counter && warp == 2) {
+      // The last CTA to finish sums every CTA's partials (and mode 4's) of
+      // each matrix in a fixed order: deterministic, and no reduction launch.
+      __threadfence();    // by every lane that wrote a partial
+      __syncwarp();
       unsigned prev = 0;
-      if (lane == 0) {
-        __threadfence();
-        prev = atomicInc(A.counter, gridDim.x - 1);
-      }
+      if (lane == 0) prev = atomicInc(A.counter, gridDim.x - 1);
       prev = __shfl_sync(0xffffffffu, prev, 0);
       if (prev == gridDim.x - 1) {
         __threadfence();
-        double a = 0.0, b = 0.0;
-        for (int i = lane; i < A.nssq; i += 32) a += __ldcg(A.ssq + i);
-        for (int i = lane; i < int(gridDim.x); i += 32) b += __ldcg(A.part + i);
-        for (int o = 16; o; o >>= 1) {
-          a += __shfl_xor_sync(0xffffffffu, a, o);
-          b += __shfl_xor_sync(0xffffffffu, b, o);
-        }
-        if (lane == 0) {
-          A.norms[0] = a;
-          A.norms[1] = b;
+        for (int mi = 0; mi < A.nm; ++mi) {
+          const ApplyMat& M = A.m[mi];
+          if (!M.norms) continue;
+          double a = 0.0, b = 0.0;
+          for (int i = lane; i < A.nssq; i += 32) a += __ldcg(M.ssq + i);
+          for (int i = lane; i < int(gridDim.x); i += 32) b += __ldcg(M.part + i);
+          for (int o = 16; o; o >>= 1) {
+            a += __shfl_xor_sync(0xffffffffu, a, o);
+            b += __shfl_xor_sync(0xffffffffu, b, o);
+          }
+          if (lane == 0) {
+            M.norms[0] = a;
+            M.norms[1] = b;
+          }
         }
       }
     }
@@ -506,8 +547,10 @@ __global__ void __launch_bounds__(480, 1)
       const int gtid = threadIdx.x - 192;
       int stage = 0;
       uint32_t phase = 0;
-      for (int u = blockIdx.x; u < A.units; u += gridDim.x) {
-        const int st = u % A.nsuper;
+      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const int mi = mat_of(A, u);
+        const int st = (u - A.ustart[mi]) % A.m[mi].nsuper;
+        const uint64_t key = A.m[mi].key;
         for (int c = 0; c < nchunks; ++c) {
           if (!warp_wait(sh, &sh->ab_empty[stage], phase ^ 1u, limit, ctl)) goto gen_done;
           uint8_t* bt = ab + stage * kStageB + kABytes;
@@ -515,7 +558,7 @@ __global__ void __launch_bounds__(480, 1)
           for (int e = gtid; e < 4 * kRc; e += 128) {
             const int grp = e / kRc, a_l = e % kRc;
             const int a = c * kRc + a_l;
-            const uint64_t w = a < A.r ? sign_word(A.key, uint32_t(a), uint32_t(st * (kCols / 64) + grp)) : 0ull;
+            const uint64_t w = a < A.r ? sign_word(key, uint32_t(a), uint32_t(st * (kCols / 64) + grp)) : 0ull;
             uint8_t* rowp = bt + grp * (kRc * 128) + a_l * 128;
 #pragma unroll
             for (int q = 0; q < 8; ++q)
@@ -547,11 +590,16 @@ __device__ __forceinline__ void s_image_elem(const float* __restrict__ S, int64_
   const int q = int(e & 7);
   const int c = int((e >> 3) % nchunks);
   const int64_t row = (e >> 3) / nchunks;
+  // r is a multiple of 32: the 8 ranks of an element are all inside or all outside
   float v[8];
+  if (row < d && c * kRc + q * 8 < r) {
+    const float4* src = reinterpret_cast<const float4*>(S + row * r + c * kRc + q * 8);
+    const float4 x = __ldg(src), y = __ldg(src + 1);
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
+  } else {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int a = c * kRc + q * 8 + i;
-    v[i] = (row < d && a < r) ? S[row * r + a] : 0.f;
+    for (int i = 0; i < 8; ++i) v[i] = 0.f;
   }
   uint32_t hi[4], lo[4];
 #pragma unroll
@@ -572,27 +620,34 @@ __device__ __forceinline__ void s_image_elem(const float* __restrict__ S, int64_
 
 // One block of the Gram pass: M = Sigma Sigma^T, the B operand of the
 // row-norm GEMM.  Block (bx, by, bz) takes the 32 x 32 tile (rows a0 = 32 by,
-// columns b0 = 32 bx) and sign words [16 bz, 16 bz + 16): it hashes the words of
-// its 64 rows itself and adds, with exact integer atomics, the number of bit
-// positions where rows a and b differ into counts.  The last block of a tile
-// (a wrapping arrival counter, left at zero) writes its part of the image,
-// M[a][b] = k - 2 * count exactly, split into bf16 hi + lo (|M| <= k < 2^15, so
-// lo is an integer below 2^7 in magnitude), and sets the tile's counts back to
-// zero for the next apply.  Image layout per (256-column super-tile st, 64-rank
-// chunk c, term): a 32 KB MN-major tile of 4 groups of 64 columns x 64 rows of
-// 128 bytes, 16-byte chunk q of row a stored at q ^ (a & 7).  Entries outside
-// r x r are zero.
-constexpr int kGramWords = 16;
+// columns b0 = 32 bx) and sign words [64 bz, 64 bz + 64): it hashes the words
+// of its 64 rows itself and counts, for each (a, b), the bit positions where
+// rows a and b differ.  M is symmetric: only tiles on or above the diagonal
+// are counted, and each one above it also writes the mirrored tile's image.  When one block covers all words of the tile (k <= 4096)
+// the counts stay in shared memory; otherwise every block adds its counts,
+// with exact integer atomics, into `counts`, and the last block of the tile (a
+// wrapping arrival counter, left at zero) reads them back and sets them to
+// zero for the next apply.  That block writes its part of the image,
+// M[a][b] = k - 2 * count, split into bf16 hi + lo: exact while |M| <= k <
+// 2^17 (hi keeps 8 significant bits, so the integer M - hi is at most 2^8 in
+// magnitude and fits lo's 8 bits); for larger k, lo rounds, an error below
+// 2^-16 of the entry.  Image layout per
+// (256-column super-tile st, 64-rank chunk c, term): a 32 KB MN-major tile of
+// 4 groups of 64 columns x 64 rows of 128 bytes, 16-byte chunk q of row a
+// stored at q ^ (a & 7).  Entries outside r x r are zero.
+constexpr int kGramWords = 64;
 
 __device__ __forceinline__ void gram_block(uint64_t key, int r, int nw, int64_t k, int* __restrict__ counts,
                                            unsigned* __restrict__ arrivals, uint8_t* __restrict__ mimg, int bx,
                                            int by, int bz, int gx, int gz) {
   __shared__ uint64_t wa[32][kGramWords + 1];
   __shared__ uint64_t wb[32][kGramWords + 1];
+  __shared__ int cnt[32][33];
   __shared__ unsigned last;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8 threads
   const int a0 = by * 32, b0 = bx * 32;
   const bool live = a0 < r && b0 < r;                         // block-uniform
+  if (live && bx < by) return;                                // below the diagonal: its mirror writes it
   if (live) {
     const int wbeg = bz * kGramWords, nwr = min(kGramWords, nw - wbeg);
     for (int e = threadIdx.x; e < 2 * 32 * kGramWords; e += blockDim.x) {
@@ -613,68 +668,103 @@ __device__ __forceinline__ void gram_block(uint64_t key, int r, int nw, int64_t 
 #pragma unroll
       for (int q = 0; q < 4; ++q) diff[q] += __popcll(wa[ty + 8 * q][w] ^ x);
     }
+    if (gz == 1) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int a = a0 + ty + 8 * q, b = b0 + tx;
-      if (a < r && b < r && diff[q]) atomicAdd(&counts[a * r + b], diff[q]);
+      for (int q = 0; q < 4; ++q) cnt[ty + 8 * q][tx] = diff[q];
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int a = a0 + ty + 8 * q, b = b0 + tx;
+        if (a < r && b < r && diff[q]) atomicAdd(&counts[a * r + b], diff[q]);
+      }
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) last = (atomicInc(&arrivals[by * gx + bx], gz - 1) == gz - 1) ? 1u : 0u;
+      __syncthreads();
+      if (!last) return;
+      __threadfence();
+      // the tile's counts, read back and left at zero
+      for (int e = threadIdx.x; e < 32 * 32; e += blockDim.x) {
+        const int a = a0 + e / 32, b = b0 + e % 32;
+        int v = 0;
+        if (a < r && b < r) {
+          v = __ldcg(counts + a * r + b);
+          counts[a * r + b] = 0;
+        }
+        cnt[e / 32][e % 32] = v;
+      }
     }
-    __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) last = (atomicInc(&arrivals[by * gx + bx], gz - 1) == gz - 1) ? 1u : 0u;
-    __syncthreads();
-    if (!last) return;
-    __threadfence();
   } else if (bz != 0) {
     return;                                                   // padding tiles: block z = 0 writes the zeros
   }
-  // the tile's image: 32 rows x 4 sixteen-byte chunks x 2 terms, one whole
-  // chunk (8 consecutive columns of one row, one term) per thread
+  // the tile's image (and, above the diagonal, the mirrored tile's): 32 rows
+  // x 4 sixteen-byte chunks x 2 terms, one whole chunk (8 consecutive
+  // columns of one row, one term) per thread
   const int nck = (r + 63) / 64;
-  const int term = threadIdx.x >> 7, a = a0 + ((threadIdx.x >> 2) & 31), bq = b0 + (threadIdx.x & 3) * 8;
-  uint32_t packed[4];
+  for (int mirror = 0; mirror < ((live && bx > by) ? 2 : 1); ++mirror) {
+    const int ra = mirror ? b0 : a0, cb = mirror ? a0 : b0;  // image rows / columns of this tile
+    const int term = threadIdx.x >> 7, a = ra + ((threadIdx.x >> 2) & 31), bq = cb + (threadIdx.x & 3) * 8;
+    uint32_t packed[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t two = 0;
+    for (int i = 0; i < 4; ++i) {
+      uint32_t two = 0;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int b = bq + 2 * i + h;
-      const float m = (a < r && b < r) ? float(k - 2 * int64_t(__ldcg(counts + a * r + b))) : 0.f;
-      const __nv_bfloat16 hi = __float2bfloat16_rn(m);
-      const __nv_bfloat16 v = term ? __float2bfloat16_rn(m - __bfloat162float(hi)) : hi;
-      two |= uint32_t(__bfloat16_as_ushort(v)) << (16 * h);
+      for (int h = 0; h < 2; ++h) {
+        const int b = bq + 2 * i + h;
+        const int n = (a < r && b < r) ? (mirror ? cnt[b - a0][a - b0] : cnt[a - a0][b - b0]) : 0;
+        const float m = (a < r && b < r) ? float(k - 2 * int64_t(n)) : 0.f;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(m);
+        const __nv_bfloat16 v = term ? __float2bfloat16_rn(m - __bfloat162float(hi)) : hi;
+        two |= uint32_t(__bfloat16_as_ushort(v)) << (16 * h);
+      }
+      packed[i] = two;
     }
-    packed[i] = two;
-  }
-  const int st = bq >> 8, grp = (bq >> 6) & 3, q = (bq >> 3) & 7;
-  const int c = a >> 6, a_l = a & 63;
-  uint8_t* tile = mimg + ((size_t(st) * nck + c) * 2 + term) * 32768;
-  *reinterpret_cast<uint4*>(tile + grp * 8192 + a_l * 128 + ((q ^ (a_l & 7)) << 4)) =
-      make_uint4(packed[0], packed[1], packed[2], packed[3]);
-  if (live) {
-    __syncthreads();                                          // both terms have read the counts
-    if (term == 0 && a < r)
-      for (int b = bq; b < bq + 8 && b < r; ++b) counts[a * r + b] = 0;
+    const int st = bq >> 8, grp = (bq >> 6) & 3, q = (bq >> 3) & 7;
+    const int c = a >> 6, a_l = a & 63;
+    uint8_t* tile = mimg + ((size_t(st) * nck + c) * 2 + term) * 32768;
+    *reinterpret_cast<uint4*>(tile + grp * 8192 + a_l * 128 + ((q ^ (a_l & 7)) << 4)) =
+        make_uint4(packed[0], packed[1], packed[2], packed[3]);
   }
 }
 
-// The apply's preparation in one launch: the first ngram blocks run the Gram
-// pass (when asked), the rest build the S image with a grid-stride loop.
-__global__ void __launch_bounds__(256) apply_prep_kernel(uint64_t key, int r, int nw, int64_t k, int gx, int gy,
-                                                         int gz, int* __restrict__ counts,
-                                                         unsigned* __restrict__ arrivals, uint8_t* __restrict__ mimg,
-                                                         const float* __restrict__ S, int64_t d,
-                                                         uint8_t* __restrict__ img) {
-  const int ngram = gx * gy * gz;
-  if (int(blockIdx.x) < ngram) {
-    const int b = blockIdx.x;
-    gram_block(key, r, nw, k, counts, arrivals, mimg, b % gx, (b / gx) % gy, b / (gx * gy), gx, gz);
+// The preparation of a group of applies in one launch: the first ngram blocks
+// run the Gram passes of all matrices (when asked), the rest build their S
+// images with a grid-stride loop over each matrix in turn.
+struct PrepMat {
+  uint64_t key;
+  int64_t d, k;
+  int nw, gz;                 // sign words per row; Gram blocks along the words
+  int gram0;                  // first Gram block of this matrix
+  int* counts;                // r x r, zero on entry and left zero
+  unsigned* arrivals;         // one word per 32 x 32 tile of M, zero on entry and left zero
+  uint8_t* mimg;
+  const float* S;
+  uint8_t* img;
+};
+struct PrepArgs {
+  PrepMat m[kMaxGroup];
+  int nm, r, nck, gx, gy, ngram;
+};
+
+__global__ void __launch_bounds__(256) apply_prep_kernel(const __grid_constant__ PrepArgs P) {
+  const int b = blockIdx.x;
+  if (b < P.ngram) {
+    int mi = 0;
+    while (mi + 1 < P.nm && b >= P.m[mi + 1].gram0) ++mi;
+    const PrepMat& M = P.m[mi];
+    const int g = b - M.gram0;
+    gram_block(M.key, P.r, M.nw, M.k, M.counts, M.arrivals, M.mimg, g % P.gx, (g / P.gx) % P.gy,
+               g / (P.gx * P.gy), P.gx, M.gz);
     return;
   }
-  const int nchunks = (r + kRc - 1) / kRc;
-  const int64_t total = ((d + kRows - 1) / kRows) * kRows * nchunks * 8;
-  const int64_t nb = int64_t(gridDim.x) - ngram;
-  for (int64_t e = (int64_t(blockIdx.x) - ngram) * blockDim.x + threadIdx.x; e < total; e += nb * blockDim.x)
-    s_image_elem(S, d, r, nchunks, img, e);
+  const int64_t nb = int64_t(gridDim.x) - P.ngram;
+  for (int mi = 0; mi < P.nm; ++mi) {
+    const PrepMat& M = P.m[mi];
+    const int64_t total = ((M.d + kRows - 1) / kRows) * kRows * P.nck * 8;
+    for (int64_t e = (int64_t(b) - P.ngram) * blockDim.x + threadIdx.x; e < total; e += nb * blockDim.x)
+      s_image_elem(M.S, M.d, P.r, P.nck, M.img, e);
+  }
 }
 
 size_t s_image_bytes(int64_t d, int r) {
@@ -683,18 +773,37 @@ size_t s_image_bytes(int64_t d, int r) {
   return size_t(rb) * nchunks * kABytes;
 }
 
-int launch_apply_prep(uint64_t key, int r, int64_t k, bool gram, int* counts, unsigned* arrivals, uint8_t* mimg,
-                      const float* S, int64_t d, uint8_t* img, cudaStream_t s) {
-  const int nchunks = (r + kRc - 1) / kRc;
-  const int nw = int((k + 63) / 64);
-  const int gx = gram ? ((r + 255) / 256) * 8 : 0, gy = gram ? ((r + 63) / 64) * 2 : 0;
-  const int gz = gram ? (nw + kGramWords - 1) / kGramWords : 0;
-  const int64_t total = ((d + kRows - 1) / kRows) * kRows * nchunks * 8;
+int launch_apply_prep(const PrepMatLaunch* mats, int nm, int r, bool gram, cudaStream_t s) {
+  if (nm < 1 || nm > kMaxGroup) return LOGRA_ERR_INVALID_ARG;
+  PrepArgs P{};
+  P.nm = nm;
+  P.r = r;
+  P.nck = (r + kRc - 1) / kRc;
+  P.gx = gram ? ((r + 255) / 256) * 8 : 0;
+  P.gy = gram ? ((r + 63) / 64) * 2 : 0;
+  int64_t total = 0, ngram = 0;
+  for (int i = 0; i < nm; ++i) {
+    PrepMat& M = P.m[i];
+    M.key = mats[i].key;
+    M.d = mats[i].d;
+    M.k = mats[i].k;
+    M.nw = int((M.k + 63) / 64);
+    M.gz = gram ? (M.nw + kGramWords - 1) / kGramWords : 0;
+    M.gram0 = int(ngram);
+    M.counts = mats[i].counts;
+    M.arrivals = mats[i].arrivals;
+    M.mimg = mats[i].mimg;
+    M.S = mats[i].S;
+    M.img = mats[i].img;
+    ngram += int64_t(P.gx) * P.gy * M.gz;
+    total += ((M.d + kRows - 1) / kRows) * kRows * P.nck * 8;
+  }
+  if (ngram > (int64_t(1) << 30)) return LOGRA_ERR_UNSUPPORTED;
+  P.ngram = int(ngram);
   int64_t blocks = (total + 255) / 256;
   if (blocks > int64_t(sm_count()) * 8) blocks = int64_t(sm_count()) * 8;
   if (blocks < 1) blocks = 1;
-  apply_prep_kernel<<<unsigned(blocks + int64_t(gx) * gy * gz), 256, 0, s>>>(key, r, nw, k, gx, gy, gz, counts,
-                                                                             arrivals, mimg, S, d, img);
+  apply_prep_kernel<<<unsigned(blocks + ngram), 256, 0, s>>>(P);
   LOGRA_LAUNCHED();
   return LOGRA_OK;
 }
@@ -702,64 +811,71 @@ int launch_apply_prep(uint64_t key, int r, int64_t k, bool gram, int* counts, un
 int launch_apply_tc(const ApplyLaunch& L, int* grid_out, Control* ctl, cudaStream_t s) {
   const int sms = sm_count();
   const int mode = L.mode;
+  if (L.nm < 1 || L.nm > kMaxGroup) return LOGRA_ERR_INVALID_ARG;
   ApplyArgs A{};
-  A.d = L.d; A.k = L.k; A.r = L.r;
+  A.nm = L.nm;
+  A.r = L.r;
   A.nck = (L.r + kRc - 1) / kRc;
-  const int64_t rbs = (L.d + kRows - 1) / kRows;
-  if (mode == 4) {
-    A.nsuper = (L.r + kCols - 1) / kCols;
-    A.units = int(rbs);
-    A.inner = A.nsuper;
-  } else {
-    A.nsuper = int((L.k + kCols - 1) / kCols);
-    A.units = int(rbs * A.nsuper);
-    A.inner = 1;
-  }
-  A.key = L.key;
+  A.inner = mode == 4 ? (L.r + kCols - 1) / kCols : 1;
   A.scale = inv_sqrt_r(L.r);
-  A.neg_lrc_scale = L.neg_lrc * A.scale;
-  A.neg_lrc = L.neg_lrc;
   A.beta2 = L.beta2;
   A.eps = L.eps;
   A.accumulate = L.accumulate;
-  A.write_bf16 = (mode == 0 && L.Wb) ? 1 : 0;
-  A.s_image = L.s_img;
-  A.m_image = L.m_img;
-  A.norms = (mode == 0 || mode == 1) ? L.norms : nullptr;
-  A.ssq = L.ssq;
   A.nssq = L.nssq;
-  A.counter = L.counter;
-  A.S = L.S;
-  A.v_in = L.v_in;
-  A.v_out = L.v_out;
-  A.inv = L.inv;
-  A.sync_out = L.sync_out;
-  A.part = L.part;
-  // loads move 128-row sub-tiles; each epilogue warp stores its own 32-row slice
-  CUtensorMap t32{}, t16{}, t32s{}, t16s{};
-  if (mode == 0 || mode == 2) {
-    const void* p = mode == 0 ? static_cast<const void*>(L.W) : L.out;
-    if (int st = make_tmap_2d(&t32, p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(L.k), uint64_t(L.d),
-                              uint64_t(L.k) * 4, kSub, kRows, CU_TENSOR_MAP_SWIZZLE_128B))
-      return st;
-    if (int st = make_tmap_2d(&t32s, p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(L.k), uint64_t(L.d),
-                              uint64_t(L.k) * 4, kSub, 32, CU_TENSOR_MAP_SWIZZLE_128B))
-      return st;
+  A.counter = nullptr;
+  int64_t units = 0;
+  for (int i = 0; i < L.nm; ++i) {
+    const ApplyMatLaunch& X = L.m[i];
+    ApplyMat& M = A.m[i];
+    M.d = X.d;
+    M.k = X.k;
+    const int64_t rbs = (X.d + kRows - 1) / kRows;
+    M.nsuper = mode == 4 ? A.inner : int((X.k + kCols - 1) / kCols);
+    M.units = int(mode == 4 ? rbs : rbs * M.nsuper);
+    M.key = X.key;
+    M.neg_lrc = X.neg_lrc;
+    M.neg_lrc_scale = X.neg_lrc * A.scale;
+    M.write_bf16 = (mode == 0 && X.Wb) ? 1 : 0;
+    M.s_image = X.s_img;
+    M.m_image = X.m_img;
+    M.S = X.S;
+    M.v_in = X.v_in;
+    M.v_out = X.v_out;
+    M.inv = X.inv;
+    M.sync_out = X.sync_out;
+    M.part = X.part;
+    M.norms = (mode == 0 || mode == 1) ? X.norms : nullptr;
+    M.ssq = X.ssq;
+    if (M.norms) A.counter = L.counter;
+    A.ustart[i] = int(units);
+    units += M.units;
+    // loads move 128-row sub-tiles; each epilogue warp stores its own 32-row slice
+    if (mode == 0 || mode == 2) {
+      const void* p = mode == 0 ? static_cast<const void*>(X.W) : X.out;
+      if (int st = make_tmap_2d(&A.tm[i][0], p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(X.k), uint64_t(X.d),
+                                uint64_t(X.k) * 4, kSub, kRows, CU_TENSOR_MAP_SWIZZLE_128B))
+        return st;
+      if (int st = make_tmap_2d(&A.tm[i][2], p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(X.k), uint64_t(X.d),
+                                uint64_t(X.k) * 4, kSub, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+        return st;
+    }
+    if ((mode == 0 && X.Wb) || mode == 3) {
+      const void* p = mode == 0 ? static_cast<const void*>(X.Wb) : X.out;
+      if (int st = make_tmap_2d(&A.tm[i][1], p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, uint64_t(X.k), uint64_t(X.d),
+                                uint64_t(X.k) * 2, kSub, kRows, CU_TENSOR_MAP_SWIZZLE_64B))
+        return st;
+      if (int st = make_tmap_2d(&A.tm[i][3], p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, uint64_t(X.k), uint64_t(X.d),
+                                uint64_t(X.k) * 2, kSub, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+        return st;
+    }
   }
-  if ((mode == 0 && L.Wb) || mode == 3) {
-    const void* p = mode == 0 ? static_cast<const void*>(L.Wb) : L.out;
-    if (int st = make_tmap_2d(&t16, p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, uint64_t(L.k), uint64_t(L.d),
-                              uint64_t(L.k) * 2, kSub, kRows, CU_TENSOR_MAP_SWIZZLE_64B))
-      return st;
-    if (int st = make_tmap_2d(&t16s, p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, uint64_t(L.k), uint64_t(L.d),
-                              uint64_t(L.k) * 2, kSub, 32, CU_TENSOR_MAP_SWIZZLE_64B))
-      return st;
-  }
-  const int grid = A.units < sms ? A.units : sms;
+  if (units > (int64_t(1) << 30)) return LOGRA_ERR_UNSUPPORTED;
+  A.ustart[L.nm] = int(units);
+  const int grid = units < sms ? int(units) : sms;
   *grid_out = grid;
   auto run = [&](auto kern) -> int {
     LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(kern), int(kApplySmem)));
-    kern<<<grid, 480, kApplySmem, s>>>(t32, t16, t32s, t16s, A, ctl);
+    kern<<<grid, 480, kApplySmem, s>>>(A, ctl);
     LOGRA_LAUNCHED();
     return LOGRA_OK;
   };

@@ -53,11 +53,17 @@ __device__ __forceinline__ void record_status(Control* ctl, int code) {
 
 Control* control_block(int* status);                     // current device
 void* workspace(cudaStream_t stream, size_t bytes, int* status);
-// A few zero-initialised counters per (device, stream) for in-kernel
-// last-CTA detection; every user leaves them at zero.
-constexpr int kCounterWords = 1024;
-// r x r (r <= 512) Gram counts per (device, stream), zero when allocated and
-// left zero by every apply.
+// Zero-initialised counters per (device, stream) for in-kernel last-CTA
+// detection; every user leaves them at zero.  Word 0: the apply's update
+// pass; from kArrivalBase, kArrivalWords per matrix of a grouped apply: the
+// Gram tiles' arrivals (at most 16 x 16 tiles of 32 x 32 for r <= 512).
+constexpr int kArrivalBase = 64;
+constexpr int kArrivalWords = 256;
+constexpr int kCounterWords = 4096;
+// Gram counts per (device, stream): r x r ints (r <= 512) for each of up to
+// eight matrices of a grouped apply, zero when allocated and left zero by
+// every apply.
+constexpr size_t kGramCountInts = size_t(8) * 512 * 512;
 int* gram_counts(cudaStream_t stream, int* status);
 unsigned* stream_counter(cudaStream_t stream, int* status);
 int sm_count();

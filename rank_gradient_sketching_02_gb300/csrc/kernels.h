@@ -28,22 +28,34 @@ int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_
                      float scale, float* S, void* ws, Control* ctl, cudaStream_t s);
 
 size_t s_image_bytes(int64_t d, int r);
-// One launch: the S image (A operand of the apply) and, when `gram` is set,
-// the Gram image M = Sigma Sigma^T.  counts: r x r ints and arrivals: one word
-// per 32 x 32 tile of M, both zero on entry and left zero.
-int launch_apply_prep(uint64_t key, int r, int64_t k, bool gram, int* counts, unsigned* arrivals, uint8_t* mimg,
-                      const float* S, int64_t d, uint8_t* img, cudaStream_t s);
-// The tensor-core kernel behind the apply: mode 0 apply, 1 predict (dW^2 only),
-// 2 rebuild fp32, 3 rebuild bf16, 4 row norms (v, 1/sqrt(v+eps), sync sketch,
-// ||S||^2 partials) from the Gram image.
-struct ApplyLaunch {
-  int mode;
+
+// Matrices per grouped apply launch.
+constexpr int kMaxGroup = 8;
+
+// One matrix of the preparation launch: its S image (A operand of the apply)
+// and, when `gram` is set, its Gram image M = Sigma Sigma^T.  counts: r x r
+// ints and arrivals: one word per 32 x 32 tile of M, both zero on entry and
+// left zero.
+struct PrepMatLaunch {
+  uint64_t key;
+  int64_t d, k;
+  int* counts;
+  unsigned* arrivals;
+  uint8_t* mimg;
+  const float* S;
+  uint8_t* img;
+};
+int launch_apply_prep(const PrepMatLaunch* mats, int nm, int r, bool gram, cudaStream_t s);
+
+// The tensor-core kernel behind the apply, over 1..kMaxGroup matrices of one
+// rank: mode 0 apply, 1 predict (dW^2 only), 2 rebuild fp32, 3 rebuild bf16,
+// 4 row norms (v, 1/sqrt(v+eps), sync sketch, ||S||^2 partials) from the Gram
+// image.
+struct ApplyMatLaunch {
   float* W;
   __nv_bfloat16* Wb;
   void* out;
-  int accumulate;
   int64_t d, k;
-  int r;
   uint64_t key;
   float neg_lrc;            // -lr c
   const uint8_t* s_img;
@@ -53,19 +65,42 @@ struct ApplyLaunch {
   float* v_out;             // mode 4 (nullable: predict)
   float* inv;               // written by mode 4, read by modes 0 and 1
   float* sync_out;          // mode 4 (nullable)
-  float beta2, eps;
   double* part;             // per-CTA partials: dW^2 (modes 0, 1) or ||S||^2 (mode 4)
   // modes 0, 1: the last CTA to finish sums the partials into norms[0..1]
   double* norms;            // nullable
   const double* ssq;        // mode 4's ||S||^2 partials
-  int nssq;
+};
+struct ApplyLaunch {
+  int mode;
+  int nm;
+  int r;
+  float beta2, eps;
+  int accumulate;
+  int nssq;                 // mode 4's grid (partials per matrix in ssq)
   unsigned* counter;        // per-stream, zero between launches
+  ApplyMatLaunch m[kMaxGroup];
 };
 int launch_apply_tc(const ApplyLaunch& L, int* grid_out, Control* ctl, cudaStream_t s);
 
-// mode 0 apply, 1 predict, 2 reconstruct fp32, 3 reconstruct bf16.
-int launch_rowadam(int mode, float* W, __nv_bfloat16* Wb, void* out, int accumulate, const float* S,
-                   const float* v_in, float* v_out, float* sync_out, int64_t d, int64_t k, int r, uint64_t key,
-                   float beta2, float eps, float lrc, double* norms, char* ws, Control* ctl, cudaStream_t s);
+// One matrix of launch_rowadam; ws: its own apply_workspace_layout(d, k, r) bytes.
+struct RowAdamItem {
+  float* W;
+  __nv_bfloat16* Wb;
+  void* out;
+  const float* S;
+  const float* v_in;
+  float* v_out;
+  float* sync_out;
+  int64_t d, k;
+  uint64_t key;
+  float lrc;                // lr c
+  double* norms;
+  char* ws;
+};
+// mode 0 apply, 1 predict, 2 reconstruct fp32, 3 reconstruct bf16, over
+// 1..kMaxGroup matrices of rank r: three launches (prep, row norms, update)
+// for apply and predict, two for reconstruct.
+int launch_rowadam(int mode, const RowAdamItem* items, int n, int r, float beta2, float eps, int accumulate,
+                   Control* ctl, cudaStream_t s);
 
 }  // namespace logra

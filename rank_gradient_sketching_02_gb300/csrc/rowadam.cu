@@ -1,5 +1,5 @@
-// One RowAdam apply (or predict, or reconstruct) as a short sequence of
-// launches.
+// RowAdam applies (or predicts, or reconstructions) of up to eight matrices
+// as one short sequence of launches.
 //
 // apply / predict (theclarity.today write-up, "What happened": running
 // estimates of squared row magnitudes, no first moment):
@@ -18,6 +18,9 @@
 
 namespace logra {
 
+static_assert(kArrivalBase + kArrivalWords * kMaxGroup <= kCounterWords, "arrival words of a full group");
+static_assert(kGramCountInts >= size_t(kMaxGroup) * 512 * 512, "Gram counts of a full group");
+
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 ApplyWorkspace apply_workspace_layout(int64_t d, int64_t k, int r) {
@@ -32,18 +35,13 @@ ApplyWorkspace apply_workspace_layout(int64_t d, int64_t k, int r) {
   return w;
 }
 
-int launch_rowadam(int mode, float* W, __nv_bfloat16* Wb, void* out, int accumulate, const float* S,
-                   const float* v_in, float* v_out, float* sync_out, int64_t d, int64_t k, int r, uint64_t key,
-                   float beta2, float eps, float lrc, double* norms, char* ws, Control* ctl, cudaStream_t s) {
-  const ApplyWorkspace WL = apply_workspace_layout(d, k, r);
-  float* inv = reinterpret_cast<float*>(ws + WL.inv_off);
-  double* ssq = reinterpret_cast<double*>(ws + WL.ssq_off);
-  double* dw2 = reinterpret_cast<double*>(ws + WL.dw2_off);
-  uint8_t* img = reinterpret_cast<uint8_t*>(ws + WL.img_off);
-  uint8_t* mimg = reinterpret_cast<uint8_t*>(ws + WL.gram_off);
+int launch_rowadam(int mode, const RowAdamItem* items, int n, int r, float beta2, float eps, int accumulate,
+                   Control* ctl, cudaStream_t s) {
+  if (n < 1 || n > kMaxGroup) return LOGRA_ERR_INVALID_ARG;
   const bool rownorms = (mode == 0 || mode == 1);
   // per-stream zeroed scratch: counters [0] the update pass's finished CTAs,
-  // [64..) the Gram tiles' arrivals; the Gram counts
+  // [kArrivalBase + kArrivalWords i, ...) the Gram tiles' arrivals of matrix i;
+  // the Gram counts, r x r per matrix
   unsigned* counters = nullptr;
   int* counts = nullptr;
   if (rownorms) {
@@ -52,31 +50,67 @@ int launch_rowadam(int mode, float* W, __nv_bfloat16* Wb, void* out, int accumul
     if (!st) counts = gram_counts(s, &st);
     if (st) return st;
   }
-  if (int st = launch_apply_prep(key, r, k, rownorms, counts, counters ? counters + 64 : nullptr, mimg, S, d, img, s))
-    return st;
-
+  PrepMatLaunch pm[kMaxGroup];
   ApplyLaunch L{};
-  L.d = d; L.k = k; L.r = r; L.key = key; L.neg_lrc = -lrc;
-  L.s_img = img; L.m_img = mimg; L.S = S; L.inv = inv; L.beta2 = beta2; L.eps = eps;
+  L.nm = n;
+  L.r = r;
+  L.beta2 = beta2;
+  L.eps = eps;
+  for (int i = 0; i < n; ++i) {
+    const RowAdamItem& it = items[i];
+    const ApplyWorkspace WL = apply_workspace_layout(it.d, it.k, r);
+    uint8_t* img = reinterpret_cast<uint8_t*>(it.ws + WL.img_off);
+    uint8_t* mimg = reinterpret_cast<uint8_t*>(it.ws + WL.gram_off);
+    pm[i].key = it.key;
+    pm[i].d = it.d;
+    pm[i].k = it.k;
+    pm[i].counts = counts ? counts + size_t(i) * r * r : nullptr;
+    pm[i].arrivals = counters ? counters + kArrivalBase + kArrivalWords * i : nullptr;
+    pm[i].mimg = mimg;
+    pm[i].S = it.S;
+    pm[i].img = img;
+    ApplyMatLaunch& M = L.m[i];
+    M.d = it.d;
+    M.k = it.k;
+    M.key = it.key;
+    M.neg_lrc = -it.lrc;
+    M.s_img = img;
+    M.m_img = mimg;
+    M.S = it.S;
+    M.inv = reinterpret_cast<float*>(it.ws + WL.inv_off);
+  }
+  if (int st = launch_apply_prep(pm, n, r, rownorms, s)) return st;
+
   int grid_norm = 0, grid_upd = 0;
   if (rownorms) {
     L.mode = 4;
-    L.v_in = v_in;
-    L.v_out = v_out;
-    L.sync_out = sync_out;
-    L.part = ssq;
+    for (int i = 0; i < n; ++i) {
+      const ApplyWorkspace WL = apply_workspace_layout(items[i].d, items[i].k, r);
+      L.m[i].v_in = items[i].v_in;
+      L.m[i].v_out = items[i].v_out;
+      L.m[i].sync_out = items[i].sync_out;
+      L.m[i].part = reinterpret_cast<double*>(items[i].ws + WL.ssq_off);
+    }
     if (int st = launch_apply_tc(L, &grid_norm, ctl, s)) return st;
   }
   L.mode = mode;
-  L.W = W; L.Wb = Wb; L.out = out; L.accumulate = accumulate;
-  L.v_in = nullptr; L.v_out = nullptr; L.sync_out = nullptr;
-  L.part = dw2;
-  L.norms = norms;   // null for predict without norms: no last-CTA sum
-  L.ssq = ssq;
+  L.accumulate = accumulate;
   L.nssq = grid_norm;
   L.counter = counters;
-  if (int st = launch_apply_tc(L, &grid_upd, ctl, s)) return st;
-  return LOGRA_OK;
+  for (int i = 0; i < n; ++i) {
+    const ApplyWorkspace WL = apply_workspace_layout(items[i].d, items[i].k, r);
+    ApplyMatLaunch& M = L.m[i];
+    M.W = items[i].W;
+    M.Wb = items[i].Wb;
+    M.out = items[i].out;
+    M.v_in = nullptr;
+    M.v_out = nullptr;
+    M.sync_out = nullptr;
+    M.part = reinterpret_cast<double*>(items[i].ws + WL.dw2_off);
+    M.norms = items[i].norms;   // null for predict without norms: no last-CTA sum
+    M.ssq = reinterpret_cast<const double*>(items[i].ws + WL.ssq_off);
+  }
+  return launch_apply_tc(L, &grid_upd, ctl, s);
 }
 
 }  // namespace logra

@@ -63,3 +63,39 @@ def test_bad_arguments_rejected_before_any_cuda_call(lib):
     assert lib.logra_sign_matrix(0, 0, 544, 8, 16, None) == LOGRA_ERR_UNSUPPORTED
     assert lib.logra_reconstruct(16, 8, 8, 32, 0, 0, 16, 5, 0, None) == LOGRA_ERR_INVALID_ARG
     assert lib.logra_rowadam_predict(16, 16, 8, 8, 32, 0, 0, 0.9, 1e-8, 1e-3, None, None) == LOGRA_ERR_INVALID_ARG
+
+
+def _items(binding, shapes, W=16, S=16, v=16):
+    arr = (binding.logra_apply_item * max(1, len(shapes)))()
+    for i, (d, k) in enumerate(shapes):
+        arr[i] = binding.logra_apply_item(W, S, v, d, k, i, 1e-3, 1.0, None, None, None)
+    return arr
+
+
+def test_group_workspace_is_the_largest_launch_group(lib):
+    from rank_gradient_sketching_02_gb300 import binding
+    def single(d, k):
+        return (lib.logra_apply_workspace_bytes(d, k, 256) + 255) // 256 * 256
+    small = [(512, 3584)] * 3 + [(3584, 3584)] * 5                     # one launch group of 8
+    assert lib.logra_apply_group_workspace_bytes(_items(binding, small), 8, 256) == sum(single(*s) for s in small)
+    big = small + [(18944, 3584)] * 2                                   # groups of 8 and 2
+    want = max(sum(single(*s) for s in big[:8]), sum(single(*s) for s in big[8:]))
+    assert lib.logra_apply_group_workspace_bytes(_items(binding, big), 10, 256) == want
+    assert lib.logra_apply_group_workspace_bytes(_items(binding, small), 8, 48) == 0   # bad rank
+    assert lib.logra_apply_group_workspace_bytes(None, 8, 256) == 0
+
+
+def test_group_bad_arguments_rejected_before_any_cuda_call(lib):
+    from rank_gradient_sketching_02_gb300.binding import LOGRA_ERR_INVALID_ARG, LOGRA_ERR_UNSUPPORTED
+    from rank_gradient_sketching_02_gb300 import binding
+    ok = [(64, 64), (128, 64)]
+    assert lib.logra_rowadam_apply_group(_items(binding, ok), 0, 256, 0, 0.9, 1e-8, None) == 0   # no-op
+    assert lib.logra_rowadam_apply_group(None, 2, 256, 0, 0.9, 1e-8, None) == LOGRA_ERR_INVALID_ARG
+    assert lib.logra_rowadam_apply_group(_items(binding, ok), -1, 256, 0, 0.9, 1e-8, None) == LOGRA_ERR_INVALID_ARG
+    assert lib.logra_rowadam_apply_group(_items(binding, ok), 2, 48, 0, 0.9, 1e-8, None) == LOGRA_ERR_UNSUPPORTED
+    assert lib.logra_rowadam_apply_group(_items(binding, ok, W=None), 2, 256, 0, 0.9, 1e-8, None) == \
+        LOGRA_ERR_INVALID_ARG
+    assert lib.logra_rowadam_apply_group(_items(binding, [(64, 64), (12, 64)]), 2, 256, 0, 0.9, 1e-8, None) == \
+        LOGRA_ERR_UNSUPPORTED
+    assert lib.logra_rowadam_apply_group(_items(binding, ok, S=24), 2, 256, 0, 0.9, 1e-8, None) == \
+        LOGRA_ERR_UNSUPPORTED

@@ -132,7 +132,8 @@ def _sketch_like(d, r, seed, scale=1e-3):
 
 
 @pytest.mark.parametrize("d,k,r", [(256, 512, 32), (1536, 1536, 256), (40, 1000, 64), (520, 264, 512),
-                                   (8, 8, 32), (392, 1032, 384), (136, 2056, 96), (264, 72, 160)])
+                                   (8, 8, 32), (392, 1032, 384), (136, 2056, 96), (264, 72, 160),
+                                   (40, 4104, 64), (24, 8200, 32)])   # Gram words over 2 and 3 blocks
 def test_apply_stagewise_zero_w0(L, d, k, r):
     import torch
     S32 = _sketch_like(d, r, d + k)
