@@ -20,7 +20,9 @@ fractions alongside.  The matrices are independent, so the step issues them
 round robin on --streams CUDA streams (default 4); per-call durations (the
 components and the dominant call's roofline) come from one extra step on a
 single stream right after the timed region; the apply component also reports all of a
-step's apply calls issued at once on up to --apply-streams streams (default 7).
+step's apply calls issued at once on up to --apply-streams streams (default 7), and
+the whole step is captured once in a CUDA graph whose replays are timed as a
+further component (--graph times the step that way instead).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun (N > 1) every rank sketches its own microbatches (weak
@@ -72,6 +74,10 @@ def parse_args(argv=None):
     p.add_argument("--apply-mode", choices=("group", "single"), default="group",
                    help="group: one logra_rowadam_apply_group call per layer (its matrices in shared launches); "
                         "single: one logra_rowadam_apply_ex call per matrix")
+    p.add_argument("--graph", action="store_true",
+                   help="time the step as replays of one CUDA graph (value); by default the graph-replayed "
+                        "step is reported as a component after the eager timed region")
+    p.add_argument("--no-graph", action="store_true", help="skip the CUDA graph component")
     p.add_argument("--e2e-steps", type=int, default=2)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -279,7 +285,10 @@ def run_ours(args):
                  "norms_out": m["norms"], "W_bf16_out": m["Wb"]} for m in ms]
     input_bytes = sum(m["X"].numel() * m["X"].element_size() + m["dY"].numel() * m["dY"].element_size() for m in mats)
 
-    stream = torch.cuda.current_stream()
+    # a side stream as the step's main stream (a CUDA graph cannot be captured on the legacy
+    # default stream, and the library's per-stream workspaces must be the ones warmed up)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
     # pre-size the per-stream workspace so no allocation happens while timing
     ws = max(max(L.lib().logra_sketch_workspace_bytes(n, m["d"], m["k"], r, 1 if dt == torch.bfloat16 else 0),
                  L.lib().logra_apply_workspace_bytes(m["d"], m["k"], r)) for m in mats)
@@ -346,6 +355,24 @@ def run_ours(args):
     torch.cuda.synchronize()
     if L.logra_get_status() != 0:
         raise RuntimeError("device status word set during warm-up")
+    def capture_step(step_idx):
+        """One whole step (every stream's work, fork and join) captured in a CUDA graph; the
+        graph's sign matrices are those of `step_idx`, and every replay runs all of the step's
+        kernels again on the same resident inputs and state."""
+        g = torch.cuda.CUDAGraph()
+        l0 = L.logra_launch_count()
+        with torch.cuda.graph(g, stream=stream):
+            one_step(step_idx)
+        n_launch = L.logra_launch_count() - l0
+        g.replay()                          # one untimed replay after instantiation
+        torch.cuda.synchronize()
+        if L.logra_get_status() != 0:
+            raise RuntimeError("device status word set by the captured step")
+        return g, n_launch
+
+    graph = None
+    if args.graph:
+        graph, graph_launches = capture_step(args.warmup)
     barrier()
     torch.cuda.synchronize()
 
@@ -356,13 +383,18 @@ def run_ours(args):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for s in range(args.steps):
-        one_step(args.warmup + s)
+        if graph is not None:
+            graph.replay()
+        else:
+            one_step(args.warmup + s)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
     clk = clocks.stop()
     launches = L.logra_launch_count() - launches0
+    if graph is not None:
+        launches = graph_launches * args.steps
 
     # Per-call durations come from one more step issued on a single stream right after the
     # timed region, with CUDA events around every call on that stream: inside the multi-stream
@@ -405,6 +437,22 @@ def run_ours(args):
         torch.cuda.synchronize()
         ap_runs.append(a0.elapsed_time(a1))
     ap_conc_ms = statistics.median(ap_runs)
+
+    # The same step as a CUDA graph (one capture, K timed replays): what launching from the host
+    # costs on top of the GPU work.
+    graph_comp = None
+    if not args.graph and not args.no_graph and world == 1:
+        g, g_launch = capture_step(args.warmup + args.steps + 8)
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        graph_comp = {"ms_per_step": g0.elapsed_time(g1) / args.steps, "launches_per_step": g_launch,
+                      "timing": f"{args.steps} replays of one captured step, CUDA events on the main stream"}
+        del g
     elapsed_ms = t_start.elapsed_time(t_end)
     if world > 1:
         t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
@@ -427,6 +475,8 @@ def run_ours(args):
     peaks, peak_kind = load_peaks()
     hbm, tc = float(peaks["hbm_gbs"]), float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
     value = world * sk_f / (ms_step * 1e-3) / 1e12
+    if graph_comp is not None:
+        graph_comp["tflops"] = world * sk_f / (graph_comp["ms_per_step"] * 1e-3) / 1e12
 
     sk_tflops = sk_f / (sk_ms * 1e-3) / 1e12
     sk_gbs = sk_b / (sk_ms * 1e-3) / 1e9
@@ -461,6 +511,7 @@ def run_ours(args):
                    "microbatches": nmb, "tokens": n, "r": r, "mask_frac": w.mask_frac,
                    "input_bytes_resident": input_bytes, "l2": "inputs larger than L2, no flush",
                    "parallelism": f"dp{world}", "streams": len(streams), "apply_mode": args.apply_mode,
+                   "cuda_graph": bool(args.graph),
                    "component_timing": "components and roofline: CUDA events around each call in one "
                    "extra step issued on a single stream right after the timed region"},
         "components": {
@@ -478,6 +529,7 @@ def run_ours(args):
                                                            "main stream around fork and join"}},
         },
         "roofline": roof,
+        "cuda_graph_step": graph_comp,
         "gpu_launches": launches,
         "clocks": clk,
         "device_status": status,
