@@ -36,7 +36,8 @@ the design notes of this repository):
 * the sign scale is 1/sqrt(r), so diag(A^T A) == 1 and E[A^T A] = I.
 * "row magnitude" is the mean over the k columns of Ghat_ij^2.
 * v is updated with the current Ghat before it scales the step; no bias
-  correction, no weight decay; eps sits inside the square root.
+  correction by default (an optional variant divides v by 1 - beta2^t for the
+  step only), no weight decay; eps sits inside the square root.
 * microbatch contributions are summed; padding tokens are zero rows of X and
   dY supplied by the caller.
 * ||dW||^2 is taken over the intended update -lr*c*Ghat/sqrt(v+eps), not over
@@ -55,7 +56,7 @@ __all__ = [
     "step_key", "sign_words", "sign_matrix", "projection_matrix",
     "projection_matrix_fp32", "sketch_accumulate", "sketch_columns",
     "reconstruct", "rowadam_apply", "rowadam_rows", "gram_matrix",
-    "sync_sketch",
+    "sync_sketch", "bias_corrected",
 ]
 
 MASK64 = (1 << 64) - 1
@@ -162,14 +163,31 @@ def reconstruct(S: np.ndarray, seed: int, step: int, k: int) -> np.ndarray:
     return S @ projection_matrix(seed, step, S.shape[1], k)
 
 
+def bias_corrected(v_new: np.ndarray, beta2: float, t: int) -> np.ndarray:
+    """Adam's bias correction of the second moment, v / (1 - beta2^t), for the
+    t-th update (t >= 1); t = 0 means no correction (the default RowAdam).
+
+    Adam divides its running averages by 1 - beta^t because they start at zero
+    (Kingma & Ba, "Adam: A Method for Stochastic Optimization", ICLR 2015,
+    Algorithm 1); the pages name Adam's correction (academy.dair.ai summary)
+    but leave RowAdam's open, so the corrected form is an optional variant.
+    """
+    v_new = np.asarray(v_new, dtype=np.float64)
+    if t == 0:
+        return v_new
+    return v_new / (1.0 - beta2 ** t)
+
+
 def rowadam_apply(W: np.ndarray, S: np.ndarray, v: np.ndarray, seed: int,
-                  step: int, beta2: float, eps: float, lr: float, c: float):
+                  step: int, beta2: float, eps: float, lr: float, c: float, t: int = 0):
     """RowAdam step from the sketch.
 
     Ghat = S A; m_i = mean_j Ghat_ij^2; v_i <- beta2 v_i + (1-beta2) m_i;
     dW_ij = -lr c Ghat_ij / sqrt(v_i + eps); W <- W + dW.
     RowAdam keeps one squared-row-magnitude statistic per row and no first
     moment (theclarity.today write-up, "What happened" and "Why it matters").
+    With t >= 1 the step uses the bias-corrected v / (1 - beta2^t) in place of
+    v (the stored v stays uncorrected).
 
     Returns (W_new, v_new, norms, dW) with norms = (||S||_F^2, ||dW||_F^2).
     """
@@ -178,25 +196,25 @@ def rowadam_apply(W: np.ndarray, S: np.ndarray, v: np.ndarray, seed: int,
     Ghat = reconstruct(S, seed, step, k)
     m = np.mean(Ghat * Ghat, axis=1)
     v_new = beta2 * np.asarray(v, dtype=np.float64) + (1.0 - beta2) * m
-    dW = -lr * c * Ghat / np.sqrt(v_new + eps)[:, None]
+    dW = -lr * c * Ghat / np.sqrt(bias_corrected(v_new, beta2, t) + eps)[:, None]
     W_new = np.asarray(W, dtype=np.float64) + dW
     norms = np.array([np.sum(S * S), np.sum(dW * dW)])
     return W_new, v_new, norms, dW
 
 
 def rowadam_rows(S_rows: np.ndarray, v_rows: np.ndarray, k: int, seed: int,
-                 step: int, beta2: float, eps: float, lr: float, c: float):
+                 step: int, beta2: float, eps: float, lr: float, c: float, t: int = 0):
     """RowAdam on a subset of rows (rows are independent given S): (v_new, dW, Ghat)."""
     S_rows = np.asarray(S_rows, dtype=np.float64)
     Ghat = reconstruct(S_rows, seed, step, k)
     m = np.mean(Ghat * Ghat, axis=1)
     v_new = beta2 * np.asarray(v_rows, dtype=np.float64) + (1.0 - beta2) * m
-    dW = -lr * c * Ghat / np.sqrt(v_new + eps)[:, None]
+    dW = -lr * c * Ghat / np.sqrt(bias_corrected(v_new, beta2, t) + eps)[:, None]
     return v_new, dW, Ghat
 
 
 def sync_sketch(S: np.ndarray, v_new: np.ndarray, eps: float, lr: float,
-                c: float) -> np.ndarray:
+                c: float, beta2: float = 0.0, t: int = 0) -> np.ndarray:
     """Row-scaled sketch S'_i = -lr c S_i / sqrt(v_i + eps).
 
     The row scaling commutes with the right product by A, so S' A is the
@@ -205,7 +223,7 @@ def sync_sketch(S: np.ndarray, v_new: np.ndarray, eps: float, lr: float,
     which makes policy synchronisation cheaper).
     """
     S = np.asarray(S, dtype=np.float64)
-    return -lr * c * S / np.sqrt(np.asarray(v_new, dtype=np.float64) + eps)[:, None]
+    return -lr * c * S / np.sqrt(bias_corrected(v_new, beta2, t) + eps)[:, None]
 
 
 def gram_matrix(seed: int, step: int, r: int, k: int) -> np.ndarray:

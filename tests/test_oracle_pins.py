@@ -280,6 +280,53 @@ def test_rowadam_rows_match_full():
     np.testing.assert_allclose(dWr, dW[rows], rtol=1e-14)
 
 
+# ---------------------------------------------------------------- bias-corrected variant
+def test_bias_corrected_first_step_has_unit_rms_rows():
+    """From v = 0 with eps = 0, the first corrected step (t = 1) divides each row of Ghat by
+    its own rms, whatever beta2: ||dW_i||^2 = (lr c)^2 k exactly (uncorrected it is that
+    over 1 - beta2), and the stored v keeps its uncorrected value."""
+    d, k, r = 5, 192, 16
+    S = np.random.default_rng(40).standard_normal((d, r)) * np.array([[1e-4], [1e-2], [1.0], [3.0], [1e3]])
+    lr, c = 1e-3, 0.6
+    for beta2 in (0.9, 0.999, 0.99999):
+        _, vn, norms, dW = O.rowadam_apply(np.zeros((d, k)), S, np.zeros(d), 2, 3, beta2, 0.0, lr, c, t=1)
+        np.testing.assert_allclose(np.sum(dW * dW, axis=1), (lr * c) ** 2 * k, rtol=1e-12)
+        np.testing.assert_allclose(norms[1], d * (lr * c) ** 2 * k, rtol=1e-12)
+        m = np.mean(np.array(_brute_ghat(S, O.sign_matrix(2, 3, r, k), r)) ** 2, axis=1)
+        np.testing.assert_allclose(vn, (1 - beta2) * m, rtol=1e-12)
+        _, _, _, dW0 = O.rowadam_apply(np.zeros((d, k)), S, np.zeros(d), 2, 3, beta2, 0.0, lr, c)
+        np.testing.assert_allclose(np.sum(dW0 * dW0, axis=1), (lr * c) ** 2 * k / (1 - beta2), rtol=1e-10)
+
+
+def test_bias_corrected_constant_gradient_same_step_every_t():
+    """A constant gradient from v = 0: v_t = (1 - beta2^t) m, so the corrected v is m at
+    every t and every step is the same; without correction the steps shrink."""
+    d, k, r = 4, 128, 8
+    S = np.random.default_rng(41).standard_normal((d, r))
+    beta2, eps, lr = 0.9, 0.0, 1e-2
+    v = np.zeros(d)
+    steps = []
+    for t in range(1, 6):
+        _, v, _, dW = O.rowadam_apply(np.zeros((d, k)), S, v, 7, 0, beta2, eps, lr, 1.0, t=t)
+        steps.append(dW)
+    for dW in steps[1:]:
+        np.testing.assert_allclose(dW, steps[0], rtol=1e-12)
+    _, _, _, late = O.rowadam_apply(np.zeros((d, k)), S, np.zeros(d), 7, 0, beta2, eps, lr, 1.0, t=10**6)
+    _, _, _, plain = O.rowadam_apply(np.zeros((d, k)), S, np.zeros(d), 7, 0, beta2, eps, lr, 1.0)
+    np.testing.assert_allclose(late, plain, rtol=1e-12)   # 1 - beta2^t -> 1
+
+
+def test_bias_corrected_sync_sketch_and_rows():
+    d, k, r = 6, 256, 16
+    g = np.random.default_rng(42)
+    S, v = g.standard_normal((d, r)), np.abs(g.standard_normal(d)) * 1e-2
+    _, vn, _, dW = O.rowadam_apply(np.zeros((d, k)), S, v, 4, 4, 0.99, 1e-8, 1e-4, 0.9, t=3)
+    Sp = O.sync_sketch(S, vn, 1e-8, 1e-4, 0.9, beta2=0.99, t=3)
+    np.testing.assert_allclose(O.reconstruct(Sp, 4, 4, k), dW, rtol=1e-12, atol=1e-20)
+    vr, dWr, _ = O.rowadam_rows(S[[1, 4]], v[[1, 4]], k, 4, 4, 0.99, 1e-8, 1e-4, 0.9, t=3)
+    np.testing.assert_allclose(dWr, dW[[1, 4]], rtol=1e-14)
+
+
 # ---------------------------------------------------------------- Gram identity
 @pytest.mark.parametrize("k", [64, 200, 640])
 def test_gram_identity_and_popcount(k):
@@ -347,3 +394,9 @@ def test_pins_catch_planted_mistakes(monkeypatch):
             return z ^ (z >> np.uint64(31))
     monkeypatch.setattr(O, "splitmix64_finalize", bad_mix)
     assert [int(x) for x in O.splitmix64_outputs(0, 2)] != _golden_words("splitmix64_seed0.txt")[:2]
+
+    # 4) bias correction one step off (1 - beta2^(t+1)): the unit-rms first step fails.
+    monkeypatch.setattr(O, "bias_corrected", lambda v, b, t: v / (1.0 - b ** (t + 1)) if t else v)
+    S = np.random.default_rng(18).standard_normal((3, 8))
+    _, _, _, dW = O.rowadam_apply(np.zeros((3, 64)), S, np.zeros(3), 0, 0, 0.9, 0.0, 1e-3, 1.0, t=1)
+    assert not np.allclose(np.sum(dW * dW, axis=1), 1e-6 * 64, rtol=1e-6)
