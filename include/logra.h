@@ -150,6 +150,26 @@ int logra_rowadam_apply_ex(float* W, const float* S, float* v, int64_t d,
                            float* sync_sketch_out, logra_stream_t stream);
 
 /*
+ * logra_rowadam_apply_bc -- logra_rowadam_apply_ex with Adam's bias correction
+ * of the second moment.  The pages name Adam's correction but leave RowAdam's
+ * open (academy.dair.ai summary), so the plain calls above apply none; this
+ * variant scales the step by the corrected v_hat_i = v_i / (1 - beta2^t)
+ * (Kingma & Ba, "Adam", ICLR 2015, Algorithm 1):
+ *   dW_ij = -lr * c * Ghat_ij / sqrt(v_hat_i + eps),
+ * and the sync sketch and ||dW||^2 use the same v_hat.  The stored v stays the
+ * uncorrected running average.
+ *   t   the number of RowAdam updates of this matrix including this one
+ *       (t >= 1; t = 0 is the uncorrected step).  t < 0, or t >= 1 with beta2
+ *       outside [0, 1), returns LOGRA_ERR_INVALID_ARG.
+ * Other arguments as for logra_rowadam_apply_ex.
+ */
+int logra_rowadam_apply_bc(float* W, const float* S, float* v, int64_t d,
+                           int64_t k, int r, uint64_t seed, uint64_t step,
+                           float beta2, float eps, float lr, float c, int64_t t,
+                           double* norms_out, uint16_t* W_bf16_out,
+                           float* sync_sketch_out, logra_stream_t stream);
+
+/*
  * logra_apply_item -- one matrix of logra_rowadam_apply_group: the arguments of
  * logra_rowadam_apply_ex that differ between matrices.  Device pointers as
  * there; norms_out, W_bf16_out and sync_sketch_out may be NULL.
@@ -164,6 +184,8 @@ typedef struct logra_apply_item {
   double* norms_out;        /* 2 doubles: {||S||_F^2, ||dW||_F^2}         */
   uint16_t* W_bf16_out;     /* d x k bf16 copy of the updated W           */
   float* sync_sketch_out;   /* d x r, S'_i = -lr c S_i / sqrt(v_i + eps)  */
+  int64_t t;                /* 0: RowAdam as defined; t >= 1: the bias-corrected step of
+                               logra_rowadam_apply_bc for this matrix's t-th update */
 } logra_apply_item;
 
 /*
@@ -203,6 +225,13 @@ int logra_rowadam_predict(const float* S, const float* v, int64_t d, int64_t k,
                           int r, uint64_t seed, uint64_t step, float beta2,
                           float eps, float lr, double* norms_out,
                           logra_stream_t stream);
+
+/* logra_rowadam_predict_bc -- logra_rowadam_predict for the bias-corrected
+ * step of logra_rowadam_apply_bc (t as there). */
+int logra_rowadam_predict_bc(const float* S, const float* v, int64_t d, int64_t k,
+                             int r, uint64_t seed, uint64_t step, float beta2,
+                             float eps, float lr, int64_t t, double* norms_out,
+                             logra_stream_t stream);
 
 /*
  * logra_reconstruct -- dW_out (+)= S A, the d x k matrix rebuilt from a d x r

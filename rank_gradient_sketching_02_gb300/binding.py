@@ -28,7 +28,10 @@ SIGNATURES = {
     "logra_rowadam_apply": (_I, [_VP, _VP, _VP, _I64, _I64, _I, _U64, _U64, _F, _F, _F, _F, _VP, _VP]),
     "logra_rowadam_apply_ex": (_I, [_VP, _VP, _VP, _I64, _I64, _I, _U64, _U64, _F, _F, _F, _F, _VP, _VP, _VP,
                                     _VP]),
+    "logra_rowadam_apply_bc": (_I, [_VP, _VP, _VP, _I64, _I64, _I, _U64, _U64, _F, _F, _F, _F, _I64, _VP, _VP,
+                                    _VP, _VP]),
     "logra_rowadam_predict": (_I, [_VP, _VP, _I64, _I64, _I, _U64, _U64, _F, _F, _F, _VP, _VP]),
+    "logra_rowadam_predict_bc": (_I, [_VP, _VP, _I64, _I64, _I, _U64, _U64, _F, _F, _F, _I64, _VP, _VP]),
     "logra_reconstruct": (_I, [_VP, _I64, _I64, _I, _U64, _U64, _VP, _I, _I, _VP]),
     "logra_get_status": (_I, [_VP]),
     "logra_reserve_workspace": (_I, [_SZ, _VP]),
@@ -44,7 +47,8 @@ SIGNATURES = {
 class logra_apply_item(C.Structure):
     """One matrix of logra_rowadam_apply_group (the C struct of the same name)."""
     _fields_ = [("W", _VP), ("S", _VP), ("v", _VP), ("d", _I64), ("k", _I64), ("seed", _U64),
-                ("lr", _F), ("c", _F), ("norms_out", _VP), ("W_bf16_out", _VP), ("sync_sketch_out", _VP)]
+                ("lr", _F), ("c", _F), ("norms_out", _VP), ("W_bf16_out", _VP), ("sync_sketch_out", _VP),
+                ("t", _I64)]
 
 
 SIGNATURES["logra_rowadam_apply_group"] = (_I, [C.POINTER(logra_apply_item), _I, _I, _U64, _F, _F, _VP])
@@ -186,7 +190,7 @@ def _apply_items(items):
             float(m["lr"]), float(m["c"]),
             _dev(nm, "norms_out", (torch.float64,), (2,)) if nm is not None else None,
             _dev(wb, "W_bf16_out", (torch.bfloat16,), (d, k)) if wb is not None else None,
-            _dev(sq, "sync_sketch_out", f32, (d, r)) if sq is not None else None)
+            _dev(sq, "sync_sketch_out", f32, (d, r)) if sq is not None else None, int(m.get("t", 0)))
     return arr, (r if r is not None else 32)
 
 
@@ -200,6 +204,37 @@ def logra_rowadam_apply_group(items, step: int, beta2: float, eps: float, stream
 def logra_apply_group_workspace_bytes(items) -> int:
     arr, r = _apply_items(items)
     return int(lib().logra_apply_group_workspace_bytes(arr, len(items), r))
+
+
+def logra_rowadam_apply_bc(W, S, v, seed: int, step: int, beta2: float, eps: float, lr: float, c: float, t: int,
+                           norms_out=None, W_bf16_out=None, sync_sketch_out=None, stream=None):
+    """logra_rowadam_apply_ex with Adam's bias correction for the t-th update (t >= 1)."""
+    import torch
+    d, k = W.shape
+    r = S.shape[1]
+    f32 = (torch.float32,)
+    pw = _dev(W, "W", f32)
+    ps = _dev(S, "S", f32, (d, r))
+    pv = _dev(v, "v", f32, (d,))
+    pn = _dev(norms_out, "norms_out", (torch.float64,), (2,)) if norms_out is not None else None
+    pb = _dev(W_bf16_out, "W_bf16_out", (torch.bfloat16,), (d, k)) if W_bf16_out is not None else None
+    pq = _dev(sync_sketch_out, "sync_sketch_out", f32, (d, r)) if sync_sketch_out is not None else None
+    _check(lib().logra_rowadam_apply_bc(pw, ps, pv, d, k, r, seed, step, beta2, eps, lr, c, t, pn, pb, pq,
+                                        _stream(stream)), "logra_rowadam_apply_bc")
+    return W
+
+
+def logra_rowadam_predict_bc(S, v, k: int, seed: int, step: int, beta2: float, eps: float, lr: float, t: int,
+                             norms_out, stream=None):
+    import torch
+    d, r = S.shape
+    f32 = (torch.float32,)
+    ps = _dev(S, "S", f32)
+    pv = _dev(v, "v", f32, (d,))
+    pn = _dev(norms_out, "norms_out", (torch.float64,), (2,))
+    _check(lib().logra_rowadam_predict_bc(ps, pv, d, k, r, seed, step, beta2, eps, lr, t, pn, _stream(stream)),
+           "logra_rowadam_predict_bc")
+    return norms_out
 
 
 def logra_rowadam_predict(S, v, k: int, seed: int, step: int, beta2: float, eps: float, lr: float,

@@ -1,5 +1,6 @@
 // C ABI of liblogra: argument checks, per-(device, stream) workspace, the
 // per-device control block, and the launches behind each logra_* entry point.
+#include <cmath>
 #include <cstdio>
 #include <atomic>
 #include <cstring>
@@ -273,10 +274,23 @@ int logra_sketch_accumulate(const void* X, const void* dY, int in_dtype, int64_t
                             static_cast<float*>(ws), stream);
 }
 
+// 1 / (1 - beta2^t): the factor of Adam's bias correction for the t-th
+// update; 1 for t == 0 (no correction).  0 when t or beta2 is invalid.
+static float bias_scale(float beta2, int64_t t) {
+  if (t == 0) return 1.0f;
+  if (t < 0 || !(beta2 >= 0.0f) || !(beta2 < 1.0f)) return 0.0f;
+  const double den = 1.0 - std::pow(double(beta2), double(t));
+  if (!(den > 0.0)) return 0.0f;
+  const double f = 1.0 / den;
+  return f < 3.0e38 ? float(f) : 0.0f;
+}
+
 static int rowadam_common(int mode, float* W, const float* S, float* v, int64_t d, int64_t k, int r, uint64_t seed,
                           uint64_t step, float beta2, float eps, float lr, float c, double* norms_out,
-                          uint16_t* W_bf16_out, float* sync_out, logra_stream_t stream) {
+                          uint16_t* W_bf16_out, float* sync_out, int64_t t, logra_stream_t stream) {
   if (!S || !v) return LOGRA_ERR_INVALID_ARG;
+  const float vscale = bias_scale(beta2, t);
+  if (vscale == 0.0f) return LOGRA_ERR_INVALID_ARG;
   if (mode == 0 && !W) return LOGRA_ERR_INVALID_ARG;
   if (int st = check_mat(d, k)) return st;
   if (check_rank(r)) return LOGRA_ERR_UNSUPPORTED;
@@ -299,6 +313,7 @@ static int rowadam_common(int mode, float* W, const float* S, float* v, int64_t 
   it.k = k;
   it.key = step_key(seed, step);
   it.lrc = lr * c;
+  it.vscale = vscale;
   it.norms = norms_out;
   it.ws = ws;
   return launch_rowadam(mode, &it, 1, r, beta2, eps, 0, ctl, stream);
@@ -322,22 +337,35 @@ static size_t group_workspace_bytes(const logra_apply_item* items, int count, in
 int logra_rowadam_apply(float* W, const float* S, float* v, int64_t d, int64_t k, int r, uint64_t seed,
                         uint64_t step, float beta2, float eps, float lr, float c, double* norms_out,
                         logra_stream_t stream) {
-  return rowadam_common(0, W, S, v, d, k, r, seed, step, beta2, eps, lr, c, norms_out, nullptr, nullptr, stream);
+  return rowadam_common(0, W, S, v, d, k, r, seed, step, beta2, eps, lr, c, norms_out, nullptr, nullptr, 0, stream);
 }
 
 int logra_rowadam_apply_ex(float* W, const float* S, float* v, int64_t d, int64_t k, int r, uint64_t seed,
                            uint64_t step, float beta2, float eps, float lr, float c, double* norms_out,
                            uint16_t* W_bf16_out, float* sync_sketch_out, logra_stream_t stream) {
   return rowadam_common(0, W, S, v, d, k, r, seed, step, beta2, eps, lr, c, norms_out, W_bf16_out, sync_sketch_out,
-                        stream);
+                        0, stream);
+}
+
+int logra_rowadam_apply_bc(float* W, const float* S, float* v, int64_t d, int64_t k, int r, uint64_t seed,
+                           uint64_t step, float beta2, float eps, float lr, float c, int64_t t, double* norms_out,
+                           uint16_t* W_bf16_out, float* sync_sketch_out, logra_stream_t stream) {
+  return rowadam_common(0, W, S, v, d, k, r, seed, step, beta2, eps, lr, c, norms_out, W_bf16_out, sync_sketch_out,
+                        t, stream);
 }
 
 int logra_rowadam_predict(const float* S, const float* v, int64_t d, int64_t k, int r, uint64_t seed,
                           uint64_t step, float beta2, float eps, float lr, double* norms_out,
                           logra_stream_t stream) {
+  return logra_rowadam_predict_bc(S, v, d, k, r, seed, step, beta2, eps, lr, 0, norms_out, stream);
+}
+
+int logra_rowadam_predict_bc(const float* S, const float* v, int64_t d, int64_t k, int r, uint64_t seed,
+                             uint64_t step, float beta2, float eps, float lr, int64_t t, double* norms_out,
+                             logra_stream_t stream) {
   if (!norms_out) return LOGRA_ERR_INVALID_ARG;
   return rowadam_common(1, nullptr, S, const_cast<float*>(v), d, k, r, seed, step, beta2, eps, lr, 1.0f, norms_out,
-                        nullptr, nullptr, stream);
+                        nullptr, nullptr, t, stream);
 }
 
 int logra_reconstruct(const float* S, int64_t d, int64_t k, int r, uint64_t seed, uint64_t step, void* dW_out,
@@ -355,6 +383,7 @@ int logra_reconstruct(const float* S, int64_t d, int64_t k, int r, uint64_t seed
   if (!ctl) return st;
   RowAdamItem it{};
   it.out = dW_out;
+  it.vscale = 1.0f;
   it.S = S;
   it.d = d;
   it.k = k;
@@ -377,6 +406,7 @@ int logra_rowadam_apply_group(const logra_apply_item* items, int count, int r, u
   for (int i = 0; i < count; ++i) {
     const logra_apply_item& m = items[i];
     if (!m.W || !m.S || !m.v) return LOGRA_ERR_INVALID_ARG;
+    if (bias_scale(beta2, m.t) == 0.0f) return LOGRA_ERR_INVALID_ARG;
     if (int st = check_mat(m.d, m.k)) return st;
     if (!aligned16(m.W) || !aligned16(m.S) || !aligned16(m.v) || (m.W_bf16_out && !aligned16(m.W_bf16_out)) ||
         (m.sync_sketch_out && !aligned16(m.sync_sketch_out)) || (m.norms_out && !aligned16(m.norms_out)))
@@ -404,6 +434,7 @@ int logra_rowadam_apply_group(const logra_apply_item* items, int count, int r, u
       it[i].k = m.k;
       it[i].key = step_key(m.seed, step);
       it[i].lrc = m.lr * m.c;
+      it[i].vscale = bias_scale(beta2, m.t);
       it[i].norms = m.norms_out;
       it[i].ws = ws + off;
       off += align256(apply_workspace_layout(m.d, m.k, r).bytes);

@@ -92,6 +92,7 @@ struct ApplyMat {
   uint64_t key;
   float neg_lrc_scale;        // -lr c / sqrt(r)   (apply, predict)
   float neg_lrc;              // -lr c             (mode 4 sync sketch)
+  float vscale;               // mode 4: 1 / (1 - beta2^t) with Adam's bias correction, else 1
   int write_bf16;             // apply: also store the bf16 copy
   const uint8_t* s_image;     // [row block][rank chunk][hi | lo][128 rows][128 B]
   const uint8_t* m_image;     // [super-tile][rank chunk][hi, lo][32 KB]
@@ -492,7 +493,7 @@ __global__ void __launch_bounds__(480, 1)
         const float mean_sq = float(q) / (float(A.r) * float(M.k));
         const float vn = A.beta2 * M.v_in[row] + (1.f - A.beta2) * mean_sq;
         if (M.v_out) M.v_out[row] = vn;
-        const float inv = 1.f / sqrtf(vn + A.eps);
+        const float inv = 1.f / sqrtf(vn * M.vscale + A.eps);   // vscale == 1: exactly vn + eps
         M.inv[row] = inv;
         if (M.sync_out) {
           const float fs = M.neg_lrc * inv;
@@ -835,6 +836,7 @@ int launch_apply_tc(const ApplyLaunch& L, int* grid_out, Control* ctl, cudaStrea
     M.key = X.key;
     M.neg_lrc = X.neg_lrc;
     M.neg_lrc_scale = X.neg_lrc * A.scale;
+    M.vscale = X.vscale;
     M.write_bf16 = (mode == 0 && X.Wb) ? 1 : 0;
     M.s_image = X.s_img;
     M.m_image = X.m_img;

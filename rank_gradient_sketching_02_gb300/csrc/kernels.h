@@ -58,6 +58,7 @@ struct ApplyMatLaunch {
   int64_t d, k;
   uint64_t key;
   float neg_lrc;            // -lr c
+  float vscale;             // mode 4: the step uses v * vscale (Adam's bias correction), 1 = none
   const uint8_t* s_img;
   const uint8_t* m_img;     // mode 4
   const float* S;           // mode 4
@@ -94,6 +95,7 @@ struct RowAdamItem {
   int64_t d, k;
   uint64_t key;
   float lrc;                // lr c
+  float vscale;             // 1 / (1 - beta2^t) for a bias-corrected step, else 1
   double* norms;
   char* ws;
 };

@@ -74,6 +74,7 @@ int launch_rowadam(int mode, const RowAdamItem* items, int n, int r, float beta2
     M.k = it.k;
     M.key = it.key;
     M.neg_lrc = -it.lrc;
+    M.vscale = it.vscale;
     M.s_img = img;
     M.m_img = mimg;
     M.S = it.S;

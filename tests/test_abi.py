@@ -99,3 +99,18 @@ def test_group_bad_arguments_rejected_before_any_cuda_call(lib):
         LOGRA_ERR_UNSUPPORTED
     assert lib.logra_rowadam_apply_group(_items(binding, ok, S=24), 2, 256, 0, 0.9, 1e-8, None) == \
         LOGRA_ERR_UNSUPPORTED
+
+
+def test_bias_correction_arguments_rejected_before_any_cuda_call(lib):
+    from rank_gradient_sketching_02_gb300.binding import LOGRA_ERR_INVALID_ARG
+    from rank_gradient_sketching_02_gb300 import binding
+    args = (16, 16, 16, 64, 64, 32, 0, 0)
+    assert lib.logra_rowadam_apply_bc(*args, 0.999, 1e-8, 1e-3, 1.0, -1, None, None, None, None) == \
+        LOGRA_ERR_INVALID_ARG                                            # t < 0
+    assert lib.logra_rowadam_apply_bc(*args, 1.0, 1e-8, 1e-3, 1.0, 2, None, None, None, None) == \
+        LOGRA_ERR_INVALID_ARG                                            # beta2 = 1: 1 - beta2^t = 0
+    assert lib.logra_rowadam_predict_bc(16, 16, 64, 64, 32, 0, 0, 1.5, 1e-8, 1e-3, 1, 16, None) == \
+        LOGRA_ERR_INVALID_ARG
+    arr = _items(binding, [(64, 64)])
+    arr[0].t = -3
+    assert lib.logra_rowadam_apply_group(arr, 1, 256, 0, 0.9, 1e-8, None) == LOGRA_ERR_INVALID_ARG

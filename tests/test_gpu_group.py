@@ -185,3 +185,27 @@ def test_group_7b_layer_fullsize(L):
         idx = torch.from_numpy(rows).cuda()
         dW = (g["W"][idx].double() - W0[idx].double()).cpu().numpy()
         assert rel(dW, dW_or) <= TOL_DW
+
+
+def test_group_with_bias_correction_per_matrix(L):
+    """Items with different t (0 = uncorrected) against one logra_rowadam_apply_bc call each."""
+    import torch
+    beta2, eps = float(np.float32(0.99)), float(np.float32(1e-8))
+    shapes = [(264, 520), (72, 520), (520, 264)]
+    ts = [0, 1, 7]
+    case = _case(shapes, 128, seed=11)
+    grouped, single = _device(case, torch), _device(case, torch)
+    for m, t in zip(grouped, ts):
+        m["t"] = t
+    L.logra_rowadam_apply_group(grouped, 4, beta2, eps)
+    for m, t in zip(single, ts):
+        L.logra_rowadam_apply_bc(m["W"], m["S"], m["v"], m["seed"], 4, beta2, eps, m["lr"], m["c"], t,
+                                 m["norms_out"], m["W_bf16_out"], m["sync_sketch_out"])
+    torch.cuda.synchronize()
+    for m, g, s, t in zip(case, grouped, single, ts):
+        assert torch.equal(g["W"], s["W"]) and torch.equal(g["v"], s["v"])
+        assert torch.equal(g["sync_sketch_out"], s["sync_sketch_out"])
+        _, v_or, _, dW_or = O.rowadam_apply(m["W0"].astype(np.float64), m["S"].astype(np.float64),
+                                            m["v0"].astype(np.float64), m["seed"], 4, beta2, eps, m["lr"], m["c"],
+                                            t=t)
+        assert rel(host64(g["W"]), dW_or) <= TOL_DW

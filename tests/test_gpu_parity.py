@@ -260,3 +260,49 @@ def test_sync_sketch_rebuilds_applied_update(L):
 
 def test_status_word_clean(L):
     assert L.logra_get_status() == 0
+
+
+# ------------------------------------------------------------------ bias-corrected variant
+@pytest.mark.parametrize("t", [1, 3])
+def test_apply_bias_corrected(L, t):
+    import torch
+    d, k, r = 392, 1032, 128
+    S32 = _sketch_like(d, r, 50 + t)
+    v0 = (np.abs(np.random.default_rng(t).standard_normal(d)) * 1e-8).astype(np.float32)
+    S, v = to_dev(S32, "f32"), to_dev(v0, "f32")
+    W = torch.zeros((d, k), dtype=torch.float32, device="cuda")
+    sync = torch.empty((d, r), dtype=torch.float32, device="cuda")
+    norms = torch.zeros(2, dtype=torch.float64, device="cuda")
+    pred = torch.zeros(2, dtype=torch.float64, device="cuda")
+    beta2, eps, lr, c = (float(np.float32(x)) for x in (0.99, 1e-8, 1e-5, 0.8))
+    L.logra_rowadam_predict_bc(S, v, k, 3, t, beta2, eps, lr, t, pred)
+    L.logra_rowadam_apply_bc(W, S, v, 3, t, beta2, eps, lr, c, t, norms, None, sync)
+    torch.cuda.synchronize()
+    _, v_or, n_or, dW_or = O.rowadam_apply(np.zeros((d, k)), S32.astype(np.float64), v0.astype(np.float64), 3, t,
+                                           beta2, eps, lr, c, t=t)
+    assert rel(host64(v), v_or) <= TOL_V                     # the stored v is uncorrected
+    assert rel(host64(W), dW_or) <= TOL_DW
+    nr = norms.cpu().numpy()
+    assert abs(nr[0] - n_or[0]) <= TOL_V * n_or[0] and abs(nr[1] - n_or[1]) <= TOL_V * n_or[1]
+    pr = pred.cpu().numpy()                                   # predict at c = 1: c^2 scaling
+    assert abs(pr[1] * c * c - nr[1]) <= 1e-6 * nr[1]
+    assert rel(host64(sync), O.sync_sketch(S32, v_or, eps, lr, c, beta2=beta2, t=t)) <= TOL_V
+
+
+def test_apply_bias_correction_t0_is_the_plain_apply(L):
+    import torch
+    d, k, r = 136, 520, 64
+    S = to_dev(_sketch_like(d, r, 60), "f32")
+    outs = []
+    for fn in ("plain", "bc0"):
+        v = torch.full((d,), 1e-9, device="cuda")
+        W = torch.zeros((d, k), device="cuda")
+        norms = torch.zeros(2, dtype=torch.float64, device="cuda")
+        if fn == "plain":
+            L.logra_rowadam_apply_ex(W, S, v, 5, 5, 0.999, 1e-8, 1e-5, 1.0, norms)
+        else:
+            L.logra_rowadam_apply_bc(W, S, v, 5, 5, 0.999, 1e-8, 1e-5, 1.0, 0, norms)
+        outs.append((W, v, norms))
+    torch.cuda.synchronize()
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
