@@ -191,6 +191,7 @@ __global__ void __launch_bounds__(480, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh->tmem_base;
+  grid_dependency_wait();      // the S image, Gram image and row factors come from the launches before
 
   if (warp == 0) {
     // ------------------------------------------------------------------ A producer (S hi/lo chunks; mode 4: + M)
@@ -749,6 +750,7 @@ struct PrepArgs {
 };
 
 __global__ void __launch_bounds__(256) apply_prep_kernel(const __grid_constant__ PrepArgs P) {
+  grid_dependency_wait();      // S comes from the sketch calls before
   const int b = blockIdx.x;
   if (b < P.ngram) {
     int mi = 0;
@@ -804,7 +806,7 @@ int launch_apply_prep(const PrepMatLaunch* mats, int nm, int r, bool gram, cudaS
   int64_t blocks = (total + 255) / 256;
   if (blocks > int64_t(sm_count()) * 8) blocks = int64_t(sm_count()) * 8;
   if (blocks < 1) blocks = 1;
-  apply_prep_kernel<<<unsigned(blocks + ngram), 256, 0, s>>>(P);
+  LOGRA_CUDA_TRY(launch_overlapped(apply_prep_kernel, dim3(unsigned(blocks + ngram)), dim3(256), size_t(0), s, P));
   LOGRA_LAUNCHED();
   return LOGRA_OK;
 }
@@ -877,7 +879,7 @@ int launch_apply_tc(const ApplyLaunch& L, int* grid_out, Control* ctl, cudaStrea
   *grid_out = grid;
   auto run = [&](auto kern) -> int {
     LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(kern), int(kApplySmem)));
-    kern<<<grid, 480, kApplySmem, s>>>(A, ctl);
+    LOGRA_CUDA_TRY(launch_overlapped(kern, dim3(grid), dim3(480), size_t(kApplySmem), s, A, ctl));
     LOGRA_LAUNCHED();
     return LOGRA_OK;
   };

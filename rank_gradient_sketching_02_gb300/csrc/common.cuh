@@ -75,6 +75,27 @@ cudaError_t ensure_smem(const void* kernel, int bytes);
 
 }  // namespace logra
 
+namespace logra {
+// Launch with programmatic stream serialization (see grid_dependency_wait in
+// tc.cuh): every kernel launched this way waits for its predecessor's
+// completion with griddepcontrol.wait before touching global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+}  // namespace logra
+
 // After every kernel launch: count it and surface a launch error.
 #define LOGRA_LAUNCHED()                                       \
   do {                                                         \

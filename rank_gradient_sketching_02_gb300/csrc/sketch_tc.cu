@@ -233,6 +233,7 @@ __global__ void __launch_bounds__(512, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh->tmem_base;
+  grid_dependency_wait();      // the previous call's kernels still use P^T until they complete
   int grp, c0, c1;
 
   if (warp == 0) {
@@ -377,6 +378,7 @@ __global__ void __launch_bounds__(512, 1)
 // q ^ (row & 7).  Rows >= r and tokens >= n are zero.
 __global__ void __launch_bounds__(256) split_kernel(const float* __restrict__ ppart, SketchShape P,
                                                     uint8_t* __restrict__ image) {
+  grid_dependency_wait();      // P^T comes from the projection just before
   const int64_t total = int64_t(P.n_pad / kChunk) * P.r_pad * 4;
   for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total; e += int64_t(gridDim.x) * blockDim.x) {
     const int g = int(e & 3);
@@ -460,6 +462,7 @@ __global__ void __launch_bounds__(352, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh->tmem_base;
+  grid_dependency_wait();      // the image comes from the split just before, S from earlier calls
   int dt, c0, c1;
 
   if (warp == 0) {
@@ -689,18 +692,21 @@ int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_
   LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(project_tc_kernel), proj_smem));
   // segments with a partial k range reduce-add into P^T, so it starts at zero
   if (P.proj_partial) LOGRA_CUDA_TRY(cudaMemsetAsync(ppart, 0, part, s));
-  project_tc_kernel<<<P.proj_ctas, 512, proj_smem, s>>>(tx, tp, P, key, ctl);
+  LOGRA_CUDA_TRY(launch_overlapped(project_tc_kernel, dim3(P.proj_ctas), dim3(512), size_t(proj_smem), s, tx, tp, P,
+                                   key, ctl));
   LOGRA_LAUNCHED();
 
   const int64_t stotal = int64_t(P.n_pad / kChunk) * P.r_pad * 4;
   int sblocks = int((stotal + 255) / 256);
   if (sblocks > sms * 8) sblocks = sms * 8;
-  split_kernel<<<sblocks, 256, 0, s>>>(ppart, P, image);
+  LOGRA_CUDA_TRY(launch_overlapped(split_kernel, dim3(sblocks), dim3(256), size_t(0), s,
+                                   static_cast<const float*>(ppart), P, image));
   LOGRA_LAUNCHED();
 
   const int acc_smem = acc_smem_bytes(P);
   LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(accumulate_tc_kernel), acc_smem));
-  accumulate_tc_kernel<<<P.acc_ctas, 352, acc_smem, s>>>(tdy, ts, P, image, scale, ctl);
+  LOGRA_CUDA_TRY(launch_overlapped(accumulate_tc_kernel, dim3(P.acc_ctas), dim3(352), size_t(acc_smem), s, tdy, ts, P,
+                                   static_cast<const uint8_t*>(image), scale, ctl));
   LOGRA_LAUNCHED();
   return LOGRA_OK;
 }

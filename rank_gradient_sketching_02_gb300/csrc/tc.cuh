@@ -146,6 +146,17 @@ __device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Programmatic dependent launch.  The pipeline kernels are launched with
+// programmatic stream serialization, which lets the hardware have the next
+// kernel ready while the current one finishes.  None of them signals its
+// dependents early (griddepcontrol.launch_dependents): that signal only
+// promises the dependents the writes made before it, and measured with the
+// signal at kernel start the dependents read unfinished results.  So the
+// dependent is released when this grid completes, and grid_dependency_wait(),
+// called by every CTA after its prologue and before any global access, waits
+// for that completion and its memory.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
