@@ -259,8 +259,9 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     beta2, eps, lr, c = synth.BETA2, synth.EPS, synth.LR, synth.C
 
-    # ---- resident state and inputs
+    # ---- resident state and inputs (the input generation is timed on its own, outside the step)
     mats = []
+    gen_ms = 0.0
     for layer in range(layers):
         for mi, (name, d, k) in enumerate(w.matrices):
             gen = torch.Generator(device=dev)
@@ -272,10 +273,16 @@ def run_ours(args):
                  "norms": torch.zeros(2, dtype=torch.float64, device=dev),
                  "X": torch.empty((nmb, n, k), dtype=dt, device=dev),
                  "dY": torch.empty((nmb, n, d), dtype=dt, device=dev)}
+            g0 = torch.cuda.Event(enable_timing=True)
+            g1 = torch.cuda.Event(enable_timing=True)
+            g0.record()
             for mb in range(nmb):
                 synth.device_microbatch(n, d, k, dy_kind=w.dy_kind, dy_std=w.dy_std, mask_frac=w.mask_frac,
                                         key=(2026, rank, layer, mi, mb), dtype=dt, device=dev,
                                         out_X=m["X"][mb], out_dY=m["dY"][mb])
+            g1.record()
+            g1.synchronize()
+            gen_ms += g0.elapsed_time(g1)
             mats.append(m)
     torch.cuda.synchronize()
     layer_mats = [[m for m in mats if m["layer"] == li] for li in range(layers)]
@@ -509,7 +516,8 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; torch Philox on device)",
         "config": {"workload": w.name, "layers": layers, "matrices": [list(x) for x in w.matrices],
                    "microbatches": nmb, "tokens": n, "r": r, "mask_frac": w.mask_frac,
-                   "input_bytes_resident": input_bytes, "l2": "inputs larger than L2, no flush",
+                   "input_bytes_resident": input_bytes, "input_generation_ms": gen_ms,
+                   "l2": "inputs larger than L2, no flush",
                    "parallelism": f"dp{world}", "streams": len(streams), "apply_mode": args.apply_mode,
                    "cuda_graph": bool(args.graph),
                    "component_timing": "components and roofline: CUDA events around each call in one "
