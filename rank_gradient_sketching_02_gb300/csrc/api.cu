@@ -57,6 +57,7 @@ struct Buffer {
   size_t bytes = 0;
   unsigned* counters = nullptr;   // kCounterWords zero-initialised words, never freed while the stream's entry lives
   int* gram = nullptr;            // kGramCountInts Gram counts, zero between applies
+  size_t zero = 0;                // leading bytes of ptr known to be zero
 };
 std::map<std::pair<int, cudaStream_t>, Buffer> g_ws;
 
@@ -95,12 +96,18 @@ int sm_count() {
   return g_sm_count[dev];
 }
 
-void* workspace(cudaStream_t stream, size_t bytes, int* status) {
+void forget_zero_workspaces() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (auto& e : g_ws) e.second.zero = 0;
+}
+
+void* workspace(cudaStream_t stream, size_t bytes, int* status, size_t** zero_bytes) {
   *status = LOGRA_OK;
   int dev;
   if ((*status = current_device(&dev))) return nullptr;
   std::lock_guard<std::mutex> lk(g_mu);
   Buffer& b = g_ws[std::make_pair(dev, stream)];
+  if (zero_bytes) *zero_bytes = &b.zero;
   if (b.bytes < bytes) {
     if (b.ptr) {
       // Work already queued on this stream may still read the old buffer.
@@ -114,6 +121,7 @@ void* workspace(cudaStream_t stream, size_t bytes, int* status) {
       }
     }
     size_t want = bytes < (size_t(1) << 20) ? (size_t(1) << 20) : bytes;
+    b.zero = 0;
     cudaError_t e = cudaMalloc(&b.ptr, want);
     if (e != cudaSuccess) {
       b.ptr = nullptr;
@@ -263,13 +271,15 @@ int logra_sketch_accumulate(const void* X, const void* dY, int in_dtype, int64_t
   if (!X || !dY) return LOGRA_ERR_INVALID_ARG;
   if (!aligned16(X) || !aligned16(dY) || !aligned16(S)) return LOGRA_ERR_UNSUPPORTED;
   int st;
-  void* ws = workspace(stream, logra_sketch_workspace_bytes(n, d, k, r, in_dtype), &st);
+  size_t* zero = nullptr;
+  void* ws = workspace(stream, logra_sketch_workspace_bytes(n, d, k, r, in_dtype), &st, &zero);
   if (st) return st;
   if (in_dtype == LOGRA_BF16) {
     Control* ctl = control_block(&st);
     if (!ctl) return st;
-    return launch_sketch_tc(X, dY, n, d, k, r, step_key(seed, step), inv_sqrt_r(r), S, ws, ctl, stream);
+    return launch_sketch_tc(X, dY, n, d, k, r, step_key(seed, step), inv_sqrt_r(r), S, ws, zero, ctl, stream);
   }
+  *zero = 0;                      // the fp32 path keeps its P in the workspace
   return launch_sketch_simt(X, dY, in_dtype, n, d, k, r, step_key(seed, step), inv_sqrt_r(r), S,
                             static_cast<float*>(ws), stream);
 }
@@ -298,8 +308,10 @@ static int rowadam_common(int mode, float* W, const float* S, float* v, int64_t 
       (sync_out && !aligned16(sync_out)) || (norms_out && !aligned16(norms_out)))
     return LOGRA_ERR_UNSUPPORTED;
   int st;
-  char* ws = static_cast<char*>(workspace(stream, logra_apply_workspace_bytes(d, k, r), &st));
+  size_t* zero = nullptr;
+  char* ws = static_cast<char*>(workspace(stream, logra_apply_workspace_bytes(d, k, r), &st, &zero));
   if (st) return st;
+  *zero = 0;                      // the apply overwrites the workspace
   Control* ctl = control_block(&st);
   if (!ctl) return st;
   RowAdamItem it{};
@@ -377,8 +389,10 @@ int logra_reconstruct(const float* S, int64_t d, int64_t k, int r, uint64_t seed
   if (check_rank(r)) return LOGRA_ERR_UNSUPPORTED;
   if (!aligned16(S) || !aligned16(dW_out)) return LOGRA_ERR_UNSUPPORTED;
   int st;
-  char* ws = static_cast<char*>(workspace(stream, logra_apply_workspace_bytes(d, k, r), &st));
+  size_t* zero = nullptr;
+  char* ws = static_cast<char*>(workspace(stream, logra_apply_workspace_bytes(d, k, r), &st, &zero));
   if (st) return st;
+  *zero = 0;
   Control* ctl = control_block(&st);
   if (!ctl) return st;
   RowAdamItem it{};
@@ -414,8 +428,10 @@ int logra_rowadam_apply_group(const logra_apply_item* items, int count, int r, u
   }
   if (count == 0) return LOGRA_OK;
   int st;
-  char* ws = static_cast<char*>(workspace(stream, group_workspace_bytes(items, count, r), &st));
+  size_t* zero = nullptr;
+  char* ws = static_cast<char*>(workspace(stream, group_workspace_bytes(items, count, r), &st, &zero));
   if (st) return st;
+  *zero = 0;
   Control* ctl = control_block(&st);
   if (!ctl) return st;
   for (int g = 0; g < count; g += kMaxGroup) {
@@ -453,6 +469,7 @@ int logra_get_status(logra_stream_t stream) {
   LOGRA_CUDA_TRY(cudaMemcpy(&code, &ctl->status, sizeof(int), cudaMemcpyDeviceToHost));
   const int zero = 0;
   LOGRA_CUDA_TRY(cudaMemcpy(&ctl->status, &zero, sizeof(int), cudaMemcpyHostToDevice));
+  if (code != 0) forget_zero_workspaces();   // an aborted kernel may have left scratch dirty
   return code;
 }
 

@@ -52,7 +52,13 @@ __device__ __forceinline__ void record_status(Control* ctl, int code) {
 }
 
 Control* control_block(int* status);                     // current device
-void* workspace(cudaStream_t stream, size_t bytes, int* status);
+// The per-(device, stream) scratch workspace, grown on demand.  zero_bytes
+// (optional) receives the address of its count of leading bytes known to be
+// zero: 0 after every (re)allocation; users that overwrite the workspace set
+// it to 0, the sketch keeps it up to date.
+void* workspace(cudaStream_t stream, size_t bytes, int* status, size_t** zero_bytes = nullptr);
+// Forget every workspace's known-zero prefix (after a device-side failure).
+void forget_zero_workspaces();
 // Zero-initialised counters per (device, stream) for in-kernel last-CTA
 // detection; every user leaves them at zero.  Word 0: the apply's update
 // pass; from kArrivalBase, kArrivalWords per matrix of a grouped apply: the

@@ -68,5 +68,5 @@ extern "C" int logra_sketch_accumulate_noalloc(const void* X, const void* dY, in
   int st;
   Control* ctl = control_block(&st);
   if (!ctl) return st;
-  return launch_sketch_tc(X, dY, n, d, k, r, step_key(seed, step), inv_sqrt_r(r), S, scratch, ctl, stream);
+  return launch_sketch_tc(X, dY, n, d, k, r, step_key(seed, step), inv_sqrt_r(r), S, scratch, nullptr, ctl, stream);
 }

@@ -417,7 +417,8 @@ __global__ void __launch_bounds__(256) split_kernel(const float* __restrict__ pp
 // between them so the drain of one overlaps the MMAs of the next.
 __global__ void __launch_bounds__(352, 1)
     accumulate_tc_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_s,
-                         SketchShape sh_, const uint8_t* __restrict__ image, float scale, Control* ctl) {
+                         SketchShape sh_, const uint8_t* __restrict__ image, float scale, float4* pzero,
+                         int64_t pzero_n, Control* ctl) {
   extern __shared__ uint8_t smem_raw[];
   const SketchShape& P = sh_;
   uint8_t* base = align1024(smem_raw);
@@ -555,6 +556,14 @@ __global__ void __launch_bounds__(352, 1)
     const int eidx = grp * 4 + (warp - (grp ? 7 : 2));
     float* tile = reinterpret_cast<float*>(staging + eidx * kStageTile);
     const int cbeg = grp * (N / 2), cend = cbeg + N / 2;
+    // The split has consumed this call's P^T: set it back to zero for the next
+    // call's projection (its partial segments reduce-add into it) while this
+    // warp still waits for its first accumulator.
+    if (pzero) {
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int64_t i = int64_t(blockIdx.x) * 256 + eidx * 32 + lane; i < pzero_n; i += int64_t(gridDim.x) * 256)
+        pzero[i] = z;
+    }
     SegIter it(total, nchunks);
     for (int seg = 0; it.next(dt, c0, c1); ++seg) {
       const int ab = seg & (nacc - 1);
@@ -666,7 +675,7 @@ size_t sketch_tc_workspace_bytes(int64_t n, int64_t d, int64_t k, int r, int sms
 }
 
 int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_t k, int r, uint64_t key,
-                     float scale, float* S, void* ws, Control* ctl, cudaStream_t s) {
+                     float scale, float* S, void* ws, size_t* ws_zero, Control* ctl, cudaStream_t s) {
   const int sms = sm_count();
   const SketchShape P = plan(n, d, k, r, sms);
   float* ppart = static_cast<float*>(ws);
@@ -690,8 +699,11 @@ int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_
 
   const int proj_smem = proj_smem_bytes(P);
   LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(project_tc_kernel), proj_smem));
-  // segments with a partial k range reduce-add into P^T, so it starts at zero
-  if (P.proj_partial) LOGRA_CUDA_TRY(cudaMemsetAsync(ppart, 0, part, s));
+  // segments with a partial k range reduce-add into P^T, so it starts at zero:
+  // each call's accumulate leaves its P^T at zero for the next, and
+  // `ws_zero` (null: unknown) counts the leading workspace bytes known to be
+  // zero; only a larger P^T, or other use of the workspace, needs a memset
+  if (P.proj_partial && (!ws_zero || *ws_zero < part)) LOGRA_CUDA_TRY(cudaMemsetAsync(ppart, 0, part, s));
   LOGRA_CUDA_TRY(launch_overlapped(project_tc_kernel, dim3(P.proj_ctas), dim3(512), size_t(proj_smem), s, tx, tp, P,
                                    key, ctl));
   LOGRA_LAUNCHED();
@@ -705,9 +717,12 @@ int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_
 
   const int acc_smem = acc_smem_bytes(P);
   LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(accumulate_tc_kernel), acc_smem));
+  float4* pzero = ws_zero ? reinterpret_cast<float4*>(ppart) : nullptr;
   LOGRA_CUDA_TRY(launch_overlapped(accumulate_tc_kernel, dim3(P.acc_ctas), dim3(352), size_t(acc_smem), s, tdy, ts, P,
-                                   static_cast<const uint8_t*>(image), scale, ctl));
+                                   static_cast<const uint8_t*>(image), scale, pzero, int64_t(part / 16), ctl));
   LOGRA_LAUNCHED();
+  // known zero now: this call's P^T region, and nothing past it (the image follows it)
+  if (ws_zero) *ws_zero = part;
   return LOGRA_OK;
 }
 

@@ -90,6 +90,27 @@ def test_sketch_bf16(L, n, d, k, r):
     assert rel(S, S_or) <= TOL_S_BF16
 
 
+def test_sketch_scratch_reuse_across_shapes(L):
+    """Calls on one stream whose P^T scratch shrinks, grows and comes back, with an apply and
+    an fp32 sketch (both overwrite the scratch) in between: each call's accumulate leaves its
+    P^T at zero for the next projection, and the library memsets only what it cannot vouch for."""
+    import torch
+    seq = [(1024, 264, 1032, 128, "bf16"), (300, 72, 520, 256, "bf16"), (2048, 136, 2056, 256, "bf16"),
+           ("apply",), (1024, 264, 1032, 128, "bf16"), (257, 64, 72, 32, "f32"), (2048, 136, 2056, 256, "bf16"),
+           (2048, 136, 2056, 256, "bf16")]
+    for i, job in enumerate(seq):
+        if job[0] == "apply":
+            W = torch.zeros((256, 512), device="cuda")
+            L.logra_rowadam_apply(W, to_dev(_sketch_like(256, 32, 3), "f32"), torch.zeros(256, device="cuda"),
+                                  1, 1, 0.999, 1e-8, 1e-5, 1.0)
+            continue
+        n, d, k, r, dt = job
+        mbs = [synth.host_microbatch(n, d, k, dy_kind="lognormal", mask_frac=0.25, key=(6, i, mb))[:2]
+               for mb in range(2)]
+        S, S_or = run_sketch(L, mbs, d, r, dt, 40 + i, i)
+        assert rel(S, S_or) <= (TOL_S_BF16 if dt == "bf16" else TOL_S_F32), i
+
+
 @pytest.mark.parametrize("n,d,k,r", [(257, 64, 72, 32), (100, 24, 1000, 64)])
 def test_sketch_fp32_ragged(L, n, d, k, r):
     mbs = [synth.host_microbatch(n, d, k, dy_kind="gauss", dy_std=1e-3, mask_frac=0.2, key=(2, n, mb))[:2]
