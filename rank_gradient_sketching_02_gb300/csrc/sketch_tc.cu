@@ -4,14 +4,19 @@
 //             (D[128 tokens x r] in TMEM per token tile, two token tiles per
 //             generated sign tile; A = X tile by TMA, B = Sigma tile generated
 //             in shared memory from the sign hash); segments covering a whole
-//             k range store, the others reduce-add into the zeroed P^T buffer
+//             k range store, the others reduce-add into the P^T buffer (kept
+//             at zero between calls)
 //   split     P^T stored as a two-term bf16 expansion P^T = hi + lo, written
 //             pre-swizzled in 32-token chunks so the next kernel loads one
 //             chunk with a single bulk copy
 //   accumulate S += (P^T dY)^T / sqrt(r): D[r x N d-columns] in TMEM with
 //             A = P^T chunk (hi and lo, two MMAs into one accumulator),
 //             B = dY tile (MN-major, TMA); each segment adds its tile into S
-//             with TMA tensor reduce-adds (fp32).
+//             with TMA tensor reduce-adds (fp32); the epilogue warps first
+//             set the consumed P^T back to zero for the next call.
+//
+// The three kernels are launched with programmatic stream serialization and
+// wait for their predecessor (griddepcontrol.wait) after their prologue.
 //
 // Both tensor-core kernels split their work stream-K style: every CTA takes an
 // equal contiguous range of the flattened (tile, chunk) space (SegIter), which
