@@ -71,6 +71,9 @@ def parse_args(argv=None):
                    help="CUDA streams the matrices are issued on, round robin (each keeps its own workspace)")
     p.add_argument("--apply-streams", type=int, default=7,
                    help="streams for the all-applies-at-once measurement (each with its own workspace)")
+    p.add_argument("--spread", choices=("auto", "on", "off"), default="auto",
+                   help="issue a matrix's microbatch calls round robin over the streams (they add into the same "
+                        "S with atomic reductions); auto: when the workload has fewer matrices than streams")
     p.add_argument("--apply-mode", choices=("group", "single"), default="group",
                    help="group: one logra_rowadam_apply_group call per layer (its matrices in shared launches); "
                         "single: one logra_rowadam_apply_ex call per matrix")
@@ -319,6 +322,8 @@ def run_ours(args):
         b.record(st)
         ev[kind].append((a, b) + tag)
 
+    spread = (len(mats) < len(streams)) if args.spread == "auto" else (args.spread == "on")
+
     def one_step(step_idx, ev=None, sts=None):
         sts = sts or streams
         for st in sts[1:]:
@@ -328,8 +333,33 @@ def run_ours(args):
             used = []
             for m in lm:
                 st = sts[i % len(sts)]
-                i += 1
                 used.append(st)
+                if spread and len(sts) > 1:
+                    # the matrix's microbatches round robin over the streams, after S is zeroed on the
+                    # matrix's own stream; the others join it before the all-reduce and the apply
+                    with torch.cuda.stream(st):
+                        m["S"].zero_()
+                    zeroed = torch.cuda.Event()
+                    zeroed.record(st)
+                    mb_streams = []
+                    for mb in range(nmb):
+                        smb = sts[(i + mb) % len(sts)]
+                        if smb is not st and smb not in mb_streams:
+                            smb.wait_event(zeroed)
+                        mb_streams.append(smb)
+                        with torch.cuda.stream(smb):
+                            L.logra_sketch_accumulate(m["X"][mb], m["dY"][mb], m["S"], m["seed"], step_idx)
+                    for smb in set(mb_streams):
+                        if smb is not st:
+                            st.wait_stream(smb)
+                    i += 1
+                    with torch.cuda.stream(st):
+                        dp.allreduce_sketch(m["S"])
+                        if args.apply_mode == "single":
+                            L.logra_rowadam_apply_ex(m["W"], m["S"], m["v"], m["seed"], step_idx, beta2, eps, lr,
+                                                     c, m["norms"], m["Wb"], None)
+                    continue
+                i += 1
                 with torch.cuda.stream(st):
                     m["S"].zero_()
                     for mb in range(nmb):
@@ -519,6 +549,7 @@ def run_ours(args):
                    "input_bytes_resident": input_bytes, "input_generation_ms": gen_ms,
                    "l2": "inputs larger than L2, no flush",
                    "parallelism": f"dp{world}", "streams": len(streams), "apply_mode": args.apply_mode,
+                   "microbatches_spread_over_streams": bool(spread),
                    "cuda_graph": bool(args.graph),
                    "component_timing": "components and roofline: CUDA events around each call in one "
                    "extra step issued on a single stream right after the timed region"},

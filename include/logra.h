@@ -106,6 +106,9 @@ int logra_sign_matrix(uint64_t seed, uint64_t step, int r, int64_t k,
  * exactly and accumulated in fp32; the X A^T intermediate is kept as a
  * two-term bf16 expansion (relative error about 2^-16), fp32 inputs run in fp32.
  * Uses the internal workspace (r * n * 4 bytes for bf16 inputs).
+ * S is updated with atomic fp32 additions, so calls that add into the same S
+ * (different microbatches of one step) may run concurrently on different
+ * streams; the sum is then formed in an unspecified order.
  */
 int logra_sketch_accumulate(const void* X, const void* dY, int in_dtype,
                             int64_t n, int64_t d, int64_t k, int r,

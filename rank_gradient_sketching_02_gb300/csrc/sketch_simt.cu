@@ -105,7 +105,8 @@ __global__ void __launch_bounds__(256) accumulate_simt_kernel(const T* __restric
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int b = b0 + tx * 4 + q;
-      if (b < r) S[a * r + b] += scale * acc[i][q];
+      // atomic, so that calls into one S may run concurrently on several streams
+      if (b < r) atomicAdd(&S[a * r + b], scale * acc[i][q]);
     }
   }
 }

@@ -64,3 +64,30 @@ def test_three_streams_interleaved_match_oracle(L):
         assert rel(W.double().cpu().numpy(), dW_or) <= TOL_DW
         nr = norms.cpu().numpy()
         assert abs(nr[0] - n_or[0]) <= TOL_V * n_or[0] and abs(nr[1] - n_or[1]) <= TOL_V * n_or[1]
+
+
+def test_microbatches_of_one_matrix_on_several_streams(L):
+    """Microbatch calls that add into the same S, issued on four streams at once (bf16 and fp32
+    paths): the atomic updates of S give the oracle's sum up to its tolerance."""
+    import torch
+    for dtype, (n, d, k, r), tol in (("bf16", (1024, 520, 1032, 128), 1e-3), ("f32", (257, 64, 72, 32), 1e-5)):
+        mbs = [synth.host_microbatch(n, d, k, dy_kind="lognormal", mask_frac=0.25, key=(8, mb))[:2] for mb in range(8)]
+        tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+        dev = [(torch.from_numpy(X).to(tdt).cuda(), torch.from_numpy(dY).to(tdt).cuda()) for X, dY in mbs]
+        S = torch.zeros((d, r), device="cuda")
+        main = torch.cuda.current_stream()
+        sts = [torch.cuda.Stream() for _ in range(4)]
+        for st in sts:
+            st.wait_stream(main)
+        for i, (X, dY) in enumerate(dev):
+            with torch.cuda.stream(sts[i % 4]):
+                L.logra_sketch_accumulate(X, dY, S, 21, 3)
+        for st in sts:
+            main.wait_stream(st)
+        torch.cuda.synchronize()
+        assert L.logra_get_status() == 0
+        S_or = np.zeros((d, r))
+        for X, dY in dev:
+            S_or = O.sketch_accumulate(S_or, X.double().cpu().numpy(), dY.double().cpu().numpy(), 21, 3, r)
+        err = np.linalg.norm(S.double().cpu().numpy() - S_or) / np.linalg.norm(S_or)
+        assert err <= tol, (dtype, err)
