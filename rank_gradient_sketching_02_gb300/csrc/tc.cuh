@@ -92,7 +92,7 @@ __device__ __forceinline__ bool wait_or_abort(SH* sh, uint64_t* bar, uint32_t pa
   return true;
 }
 
-// Warp-uniform version: lane 0 waits, the verdict is broadcast, and every lane
+// Warp-uniform version: lane 0 waits, the outcome is broadcast, and every lane
 // then observes the completed phase itself (acquire) before touching the data.
 template <class SH>
 __device__ __forceinline__ bool warp_wait(SH* sh, uint64_t* bar, uint32_t parity, unsigned long long limit,
