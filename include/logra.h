@@ -39,7 +39,10 @@
  *     workspace per (device, stream), grown on demand (on first use of a
  *     larger shape) and kept for the life of the process;
  *     logra_reserve_workspace pre-sizes it so that no allocation happens
- *     later (e.g. inside a stream capture).
+ *     later (e.g. inside a stream capture).  The first apply on a stream
+ *     also allocates, once, that stream's zero-kept scratch: 16 KB of
+ *     counters and 8 MB of Gram-pass counts (make one apply on a stream
+ *     before capturing its applies).
  */
 #ifndef LOGRA_H
 #define LOGRA_H

@@ -50,7 +50,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 Control* g_ctl_ptr[kMaxDevices] = {};
-int g_sm_count[kMaxDevices] = {};
+std::atomic<int> g_sm_count[kMaxDevices] = {};
 
 struct Buffer {
   void* ptr = nullptr;
@@ -88,12 +88,13 @@ Control* control_block(int* status) {
 int sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
-  if (!g_sm_count[dev]) {
-    int n = 0;
+  int n = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (!n) {
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    g_sm_count[dev] = n > 0 ? n : 148;
+    if (n <= 0) n = 148;
+    g_sm_count[dev].store(n, std::memory_order_relaxed);
   }
-  return g_sm_count[dev];
+  return n;
 }
 
 void forget_zero_workspaces() {
@@ -177,9 +178,11 @@ unsigned* stream_counter(cudaStream_t stream, int* status) {
 int make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, uint32_t elem_bytes, uint64_t inner,
                  uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
                  CUtensorMapSwizzle swizzle) {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> encode_fn{nullptr};
+  PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn.load(std::memory_order_acquire);
   if (!encode) {
     std::lock_guard<std::mutex> lk(g_mu);
+    encode = encode_fn.load(std::memory_order_relaxed);
     if (!encode) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
@@ -187,6 +190,7 @@ int make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, 
       if (e != cudaSuccess) return cuda_fail(e);
       if (q != cudaDriverEntryPointSuccess || !fn) return cuda_fail(cudaErrorNotSupported);
       encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+      encode_fn.store(encode, std::memory_order_release);
     }
   }
   (void)elem_bytes;
