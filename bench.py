@@ -50,8 +50,8 @@ METRIC = "sketch TFLOP/s + fused RowAdam-apply GB/s per GB300; % of roofline"
 # (profiles/sketch_kernels_gate27b.md): key (n, d, k, r).  Shapes without an
 # entry report null.
 SKETCH_TRAFFIC_PER_CALL = {
-    # project 92.51 + 2.50 MB, split 8.40 + 0 MB, accumulate 512.64 + 23.33 MB
-    (8192, 27648, 5120, 256): 639.4e6,
+    # project 92.50 + 2.45 MB, split 8.40 + 0 MB, accumulate 512.66 + 31.71 MB (incl. re-zeroing P^T)
+    (8192, 27648, 5120, 256): 647.7e6,
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
