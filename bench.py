@@ -387,6 +387,9 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
 
+    # the step issues sketch calls on len(streams) streams at once: tell the library, so that
+    # each call's accumulate leaves SMs to the other streams (the launch shape only)
+    L.logra_set_concurrency(len(streams))
     for s in range(args.warmup):
         one_step(s)
     torch.cuda.synchronize()
@@ -437,6 +440,7 @@ def run_ours(args):
     # timed region, with CUDA events around every call on that stream: inside the multi-stream
     # step a call's event span would also cover the other streams' kernels.
     ev = {"sketch": [], "apply": []}
+    L.logra_set_concurrency(1)
     one_step(args.warmup + args.steps, ev, [stream])
     torch.cuda.synchronize()
 
@@ -479,6 +483,7 @@ def run_ours(args):
     # costs on top of the GPU work.
     graph_comp = None
     if not args.graph and not args.no_graph and world == 1:
+        L.logra_set_concurrency(len(streams))
         g, g_launch = capture_step(args.warmup + args.steps + 8)
         g0 = torch.cuda.Event(enable_timing=True)
         g1 = torch.cuda.Event(enable_timing=True)
@@ -549,7 +554,7 @@ def run_ours(args):
                    "input_bytes_resident": input_bytes, "input_generation_ms": gen_ms,
                    "l2": "inputs larger than L2, no flush",
                    "parallelism": f"dp{world}", "streams": len(streams), "apply_mode": args.apply_mode,
-                   "microbatches_spread_over_streams": bool(spread),
+                   "microbatches_spread_over_streams": bool(spread), "concurrency_hint": len(streams),
                    "cuda_graph": bool(args.graph),
                    "component_timing": "components and roofline: CUDA events around each call in one "
                    "extra step issued on a single stream right after the timed region"},
@@ -576,6 +581,7 @@ def run_ours(args):
 
     # ---- end to end through the public API from pinned host memory
     if not args.no_e2e:
+        L.logra_set_concurrency(1)      # one stream
         line["e2e"] = run_e2e(args, L, dp, mats, w, r, dt, dev, stream, sk_f, world, layer_mats, group_items)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

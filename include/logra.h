@@ -303,6 +303,17 @@ int logra_sketch_accumulate_noalloc(const void* X, const void* dY, int64_t n, in
 size_t logra_noalloc_scratch_bytes(void);
 
 /*
+ * logra_set_concurrency -- tell the library on how many streams the caller
+ * issues sketch calls at the same time (default 1; process-wide, any thread).
+ * It only shapes launches, never results: with streams > 1 each call's
+ * accumulate kernel runs on fewer, longer-running CTAs (at least 12 * streams
+ * 32-token chunks each), which leaves SMs to the other streams' kernels and
+ * reduces the partial-sum traffic into S; with one stream every call spreads
+ * over all SMs.  Returns LOGRA_ERR_INVALID_ARG outside [1, 64].
+ */
+int logra_set_concurrency(int streams);
+
+/*
  * logra_debug_inject -- TEST ONLY.  fault = 1 makes the next pipelined kernel
  * launch drop one producer arrival, so that its consumer's bounded wait runs
  * out and the kernel records LOGRA_ERR_TIMEOUT and exits cleanly (no trap, no

@@ -38,6 +38,7 @@ SIGNATURES = {
     "logra_sketch_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I, _I]),
     "logra_apply_workspace_bytes": (_SZ, [_I64, _I64, _I]),
     "logra_debug_inject": (_I, [_I, _U64]),
+    "logra_set_concurrency": (_I, [_I]),
     "logra_sketch_accumulate_noalloc": (_I, [_VP, _VP, _I64, _I64, _I64, _I, _U64, _U64, _VP, _VP]),
     "logra_noalloc_scratch_bytes": (_SZ, []),
 }
@@ -270,6 +271,10 @@ def logra_reserve_workspace(nbytes: int, stream=None):
 
 def logra_launch_count() -> int:
     return int(lib().logra_launch_count())
+
+
+def logra_set_concurrency(streams: int):
+    _check(lib().logra_set_concurrency(int(streams)), "logra_set_concurrency")
 
 
 def logra_debug_inject(fault: int, timeout_cycles: int = 0):

@@ -22,6 +22,9 @@ namespace logra {
 static __device__ Control g_control = {0, 0, 2000000000ull};
 
 static thread_local int t_last_cuda_error = 0;
+static std::atomic<int> g_concurrency{1};
+
+int concurrency() { return g_concurrency.load(std::memory_order_relaxed); }
 static std::atomic<unsigned long long> g_launches{0};
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
@@ -475,6 +478,12 @@ int logra_get_status(logra_stream_t stream) {
   LOGRA_CUDA_TRY(cudaMemcpy(&ctl->status, &zero, sizeof(int), cudaMemcpyHostToDevice));
   if (code != 0) forget_zero_workspaces();   // an aborted kernel may have left scratch dirty
   return code;
+}
+
+int logra_set_concurrency(int streams) {
+  if (streams < 1 || streams > 64) return LOGRA_ERR_INVALID_ARG;
+  g_concurrency.store(streams, std::memory_order_relaxed);
+  return LOGRA_OK;
 }
 
 int logra_debug_inject(int fault, uint64_t timeout_cycles) {

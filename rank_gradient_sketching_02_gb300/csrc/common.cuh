@@ -73,6 +73,8 @@ constexpr size_t kGramCountInts = size_t(8) * 512 * 512;
 int* gram_counts(cudaStream_t stream, int* status);
 unsigned* stream_counter(cudaStream_t stream, int* status);
 int sm_count();
+// Streams on which the caller issues sketch calls at the same time (logra_set_concurrency).
+int concurrency();
 int cuda_fail(cudaError_t e);
 void count_launch();
 // Raise a kernel's dynamic shared-memory limit to at least `bytes` on the

@@ -114,3 +114,11 @@ def test_bias_correction_arguments_rejected_before_any_cuda_call(lib):
     arr = _items(binding, [(64, 64)])
     arr[0].t = -3
     assert lib.logra_rowadam_apply_group(arr, 1, 256, 0, 0.9, 1e-8, None) == LOGRA_ERR_INVALID_ARG
+
+
+def test_concurrency_hint_is_validated(lib):
+    from rank_gradient_sketching_02_gb300.binding import LOGRA_ERR_INVALID_ARG
+    assert lib.logra_set_concurrency(0) == LOGRA_ERR_INVALID_ARG
+    assert lib.logra_set_concurrency(65) == LOGRA_ERR_INVALID_ARG
+    assert lib.logra_set_concurrency(4) == 0
+    assert lib.logra_set_concurrency(1) == 0

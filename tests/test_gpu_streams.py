@@ -91,3 +91,25 @@ def test_microbatches_of_one_matrix_on_several_streams(L):
             S_or = O.sketch_accumulate(S_or, X.double().cpu().numpy(), dY.double().cpu().numpy(), 21, 3, r)
         err = np.linalg.norm(S.double().cpu().numpy() - S_or) / np.linalg.norm(S_or)
         assert err <= tol, (dtype, err)
+
+
+@pytest.mark.parametrize("streams", [2, 4, 16])
+def test_concurrency_hint_changes_launches_not_results(L, streams):
+    """The concurrency hint only reshapes the accumulate's grid: the sketch still equals the oracle."""
+    import torch
+    n, d, k, r = 2048, 1032, 520, 256
+    mbs = [synth.host_microbatch(n, d, k, dy_kind="lognormal", mask_frac=0.25, key=(9, streams, mb))[:2]
+           for mb in range(2)]
+    L.logra_set_concurrency(streams)
+    try:
+        S = torch.zeros((d, r), device="cuda")
+        S_or = np.zeros((d, r))
+        for X, dY in mbs:
+            Xb, dYb = synth.to_bf16_bits(X), synth.to_bf16_bits(dY)
+            L.logra_sketch_accumulate(Xb.cuda(), dYb.cuda(), S, 31, 2)
+            S_or = O.sketch_accumulate(S_or, Xb.double().numpy(), dYb.double().numpy(), 31, 2, r)
+        torch.cuda.synchronize()
+    finally:
+        L.logra_set_concurrency(1)
+    assert L.logra_get_status() == 0
+    assert rel(S.double().cpu().numpy(), S_or) <= 1e-3
