@@ -307,9 +307,10 @@ size_t logra_noalloc_scratch_bytes(void);
  * issues sketch calls at the same time (default 1; process-wide, any thread).
  * It only shapes launches, never results: with streams > 1 each call's
  * accumulate kernel runs on fewer, longer-running CTAs (at least 12 * streams
- * 32-token chunks each), which leaves SMs to the other streams' kernels and
- * reduces the partial-sum traffic into S; with one stream every call spreads
- * over all SMs.  Returns LOGRA_ERR_INVALID_ARG outside [1, 64].
+ * 32-token chunks each) and so does its projection (at least 4 * streams
+ * k-chunks, when above 8), which leaves SMs to the other streams' kernels and
+ * reduces the partial-sum traffic; with one stream every call spreads over
+ * all SMs.  Returns LOGRA_ERR_INVALID_ARG outside [1, 64].
  */
 int logra_set_concurrency(int streams);
 
