@@ -623,6 +623,19 @@ static int stream_k_ctas(int64_t total, int sms, int min_chunks) {
   return g < 1 ? 1 : int(g);
 }
 
+// The grid for `hint` streams issuing calls at once: longer ranges
+// (hint_min_chunks) leave SMs to the other streams and reduce fewer partial
+// sums, but a call never drops below its fair share of the SMs (sms / hint)
+// unless its one-stream grid is already smaller.
+static int stream_k_ctas_hinted(int64_t total, int sms, int min_chunks, int hint_min_chunks, int hint) {
+  const int base = stream_k_ctas(total, sms, min_chunks);
+  if (hint <= 1) return base;
+  const int wide = stream_k_ctas(total, sms, hint_min_chunks);
+  const int fair = sms / hint > 1 ? sms / hint : 1;
+  const int floor_ctas = base < fair ? base : fair;
+  return wide > floor_ctas ? wide : floor_ctas;
+}
+
 // True when some CTA's range starts or ends inside a tile, i.e. some segment
 // covers only part of that tile's chunks.
 static bool has_partial_segment(int64_t total, int per, int ctas) {
@@ -644,7 +657,8 @@ static SketchShape plan(int64_t n, int64_t d, int64_t k, int r, int sms) {
   const int64_t ptotal = int64_t(P.groups) * P.nchunks;
   // (with calls on several streams, longer projection ranges too: 16 chunks at
   // four streams, 7B layers +3%; 32 made the eagerly issued 27B step slower)
-  P.proj_ctas = stream_k_ctas(ptotal, sms, 4 * concurrency() > 8 ? 4 * concurrency() : 8);
+  const int hint = concurrency();
+  P.proj_ctas = stream_k_ctas_hinted(ptotal, sms, 8, 4 * hint > 8 ? 4 * hint : 8, hint);
   P.proj_partial = has_partial_segment(ptotal, P.nchunks, P.proj_ctas) ? 1 : 0;
   P.ntile_n = (P.r_pad <= 256) ? 256 : 128;
   P.dtiles = ceil_div(d, P.ntile_n);
@@ -653,7 +667,7 @@ static SketchShape plan(int64_t n, int64_t d, int64_t k, int r, int sms) {
   // fewer, longer CTA ranges: SMs stay free for the other streams' kernels and
   // fewer partial S tiles are reduced in L2 (4 streams, 27B layers: +1.6% on
   // the step; one stream keeps every SM busy)
-  P.acc_ctas = stream_k_ctas(int64_t(P.dtiles) * tchunks, sms, 12 * concurrency());
+  P.acc_ctas = stream_k_ctas_hinted(int64_t(P.dtiles) * tchunks, sms, 12, 12 * hint, hint);
   // project: three sign-tile stages when three X stages still fit beside
   // them (the generators then have a whole chunk of MMA time of slack), else
   // two; the rest of shared memory for X tiles
