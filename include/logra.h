@@ -309,8 +309,10 @@ size_t logra_noalloc_scratch_bytes(void);
  * accumulate kernel runs on fewer, longer-running CTAs (at least 12 * streams
  * 32-token chunks each) and so does its projection (at least 4 * streams
  * k-chunks, when above 8), which leaves SMs to the other streams' kernels and
- * reduces the partial-sum traffic; with one stream every call spreads over
- * all SMs.  Returns LOGRA_ERR_INVALID_ARG outside [1, 64].
+ * reduces the partial-sum traffic; a call still keeps at least its fair share
+ * of the SMs (SM count / streams) unless its one-stream grid is smaller.
+ * With one stream every call spreads over all SMs.  Returns
+ * LOGRA_ERR_INVALID_ARG outside [1, 64].
  */
 int logra_set_concurrency(int streams);
 
