@@ -10,10 +10,16 @@ logra_rowadam_apply_ex per matrix instead).  Inputs
 (bf16 X and dY for every microbatch) are resident in HBM before timing; they
 are far larger than L2, so no L2 flush is needed between steps.
 
-Default workload: 4 decoder layers of 27B-class shapes (q/o 5120x5120, k/v
-1024x5120, gate/up 27648x5120, down 5120x27648), r = 256, 16 microbatches x
-8192 tokens, 30% padding rows; the largest workload whose inputs fit in one
-GPU's memory.  The metric is sketch TFLOP/s over the whole step (algorithmic
+Default workload: the 7B-class model, all 28 decoder layers (q/o 3584x3584,
+k/v 512x3584, gate/up 18944x3584, down 3584x18944), r = 256, 8 microbatches x
+8192 tokens, 25% padding rows.  Its inputs (330 GB of bf16 X and dY per step)
+do not fit in one GPU's memory, so they come from a resident pool of
+--input-layers layers' inputs (default 4, 47 GB): layer l reads pool slot
+l mod P.  Every layer still has its own weights, sketch, v and sign matrices
+(per-matrix seeds), so the kernel work per layer is unchanged; only the input
+values repeat, 47 GB apart, far beyond L2.  --workload layers27b (4 layers of
+27B-class shapes, 16 x 8192 tokens, r in {128, 256, 512}) and the smaller
+workloads remain available.  The metric is sketch TFLOP/s over the whole step (algorithmic
 sketch FLOPs 2 n r (k + d) per matrix-microbatch, divided by the step time
 including the apply), with the apply's GB/s and both kernels' roofline
 fractions alongside.  The matrices are independent, so the step issues them
@@ -46,12 +52,13 @@ if ROOT not in sys.path:
 METRIC = "sketch TFLOP/s + fused RowAdam-apply GB/s per GB300; % of roofline"
 
 # DRAM bytes (read + write) of one logra_sketch_accumulate call, summed over
-# its three launches, from one ncu capture of the kernels as they stand
-# (profiles/sketch_kernels_gate27b.md): key (n, d, k, r).  Shapes without an
-# entry report null.
+# its three launches, from one ncu capture per shape of the kernels as they
+# stood when captured (the profile summaries name the capture): key
+# (n, d, k, r) -> (bytes, what was captured).  Shapes without an entry report
+# null traffic.
 SKETCH_TRAFFIC_PER_CALL = {
     # project 92.50 + 2.45 MB, split 8.40 + 0 MB, accumulate 512.66 + 31.71 MB (incl. re-zeroing P^T)
-    (8192, 27648, 5120, 256): 647.7e6,
+    (8192, 27648, 5120, 256): (647.7e6, "ncu dram__bytes of the three launches, gate 27648x5120 call"),
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -62,11 +69,14 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=5)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    p.add_argument("--workload", default="layers27b")
+    p.add_argument("--workload", default="model7b")
     p.add_argument("--rank", type=int, default=256)
     p.add_argument("--layers", type=int, default=None, help="override the workload's layer count")
     p.add_argument("--microbatches", type=int, default=None,
                    help="override the workload's microbatches per step (small profiling cases)")
+    p.add_argument("--input-layers", type=int, default=4,
+                   help="distinct layers of resident inputs; layer l reads the inputs of slot l mod this "
+                        "(0: every layer its own inputs)")
     p.add_argument("--streams", type=int, default=4,
                    help="CUDA streams the matrices are issued on, round robin (each keeps its own workspace)")
     p.add_argument("--apply-streams", type=int, default=7,
@@ -95,6 +105,13 @@ def load_peaks():
             pk = json.load(f)
         return pk, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_config(w, layers, nmb, r, world, pool):
+    """The `config` object of the JSON line: what defines the workload, identical in both arms."""
+    return {"workload": w.name, "layers": layers, "matrices": [list(x) for x in w.matrices],
+            "microbatches": nmb, "tokens": w.tokens, "r": r, "mask_frac": w.mask_frac,
+            "input_pool_layers": pool, "l2": "inputs larger than L2, no flush", "parallelism": f"dp{world}"}
 
 
 # ----------------------------------------------------------------------------- work accounting
@@ -212,6 +229,8 @@ def run_reference(args):
     from rank_gradient_sketching_02_gb300 import synth
     w = synth.WORKLOADS[args.workload]
     r = args.rank
+    layers = args.layers or w.layers
+    pool = layers if args.input_layers <= 0 else min(layers, args.input_layers)
     per_step = max(2.0, args.cpu_seconds / 2)
     for _ in range(args.warmup):
         time_oracle(w, r, 0.5)
@@ -227,9 +246,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": w.name, "layers": args.layers or w.layers,
-                       "matrices": [list(x) for x in w.matrices], "microbatches": w.microbatches,
-                       "tokens": w.tokens, "r": r, "mask_frac": w.mask_frac, "parallelism": "dp1"},
+            "config": workload_config(w, layers, args.microbatches or w.microbatches, r, args.gpus, pool),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": res["cores"], "kind": "oracle",
                              "sample": res["sample"]},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -263,29 +280,37 @@ def run_ours(args):
     beta2, eps, lr, c = synth.BETA2, synth.EPS, synth.LR, synth.C
 
     # ---- resident state and inputs (the input generation is timed on its own, outside the step)
+    # Inputs of `pool` distinct layers stay resident; layer l reads slot l mod pool (every layer
+    # keeps its own W, S, v and seeds, so the work per layer is the same as with its own inputs).
+    pool = layers if args.input_layers <= 0 else min(layers, args.input_layers)
     mats = []
+    inputs = {}
     gen_ms = 0.0
     for layer in range(layers):
         for mi, (name, d, k) in enumerate(w.matrices):
             gen = torch.Generator(device=dev)
             gen.manual_seed(1000 + 16 * layer + mi)
             W = torch.empty((d, k), dtype=torch.float32, device=dev).normal_(0.0, 0.02, generator=gen)
+            slot = (layer % pool, mi)
+            if slot not in inputs:
+                Xs = torch.empty((nmb, n, k), dtype=dt, device=dev)
+                Ys = torch.empty((nmb, n, d), dtype=dt, device=dev)
+                g0 = torch.cuda.Event(enable_timing=True)
+                g1 = torch.cuda.Event(enable_timing=True)
+                g0.record()
+                for mb in range(nmb):
+                    synth.device_microbatch(n, d, k, dy_kind=w.dy_kind, dy_std=w.dy_std, mask_frac=w.mask_frac,
+                                            key=(2026, rank, slot[0], mi, mb), dtype=dt, device=dev,
+                                            out_X=Xs[mb], out_dY=Ys[mb])
+                g1.record()
+                g1.synchronize()
+                gen_ms += g0.elapsed_time(g1)
+                inputs[slot] = (Xs, Ys)
             m = {"name": name, "layer": layer, "d": d, "k": k, "seed": synth.matrix_seed(2026, layer, mi), "W": W,
                  "Wb": W.to(torch.bfloat16), "v": torch.zeros(d, dtype=torch.float32, device=dev),
                  "S": torch.zeros((d, r), dtype=torch.float32, device=dev),
                  "norms": torch.zeros(2, dtype=torch.float64, device=dev),
-                 "X": torch.empty((nmb, n, k), dtype=dt, device=dev),
-                 "dY": torch.empty((nmb, n, d), dtype=dt, device=dev)}
-            g0 = torch.cuda.Event(enable_timing=True)
-            g1 = torch.cuda.Event(enable_timing=True)
-            g0.record()
-            for mb in range(nmb):
-                synth.device_microbatch(n, d, k, dy_kind=w.dy_kind, dy_std=w.dy_std, mask_frac=w.mask_frac,
-                                        key=(2026, rank, layer, mi, mb), dtype=dt, device=dev,
-                                        out_X=m["X"][mb], out_dY=m["dY"][mb])
-            g1.record()
-            g1.synchronize()
-            gen_ms += g0.elapsed_time(g1)
+                 "X": inputs[slot][0], "dY": inputs[slot][1]}
             mats.append(m)
     torch.cuda.synchronize()
     layer_mats = [[m for m in mats if m["layer"] == li] for li in range(layers)]
@@ -293,7 +318,9 @@ def run_ours(args):
     def group_items(ms):
         return [{"W": m["W"], "S": m["S"], "v": m["v"], "seed": m["seed"], "lr": lr, "c": c,
                  "norms_out": m["norms"], "W_bf16_out": m["Wb"]} for m in ms]
-    input_bytes = sum(m["X"].numel() * m["X"].element_size() + m["dY"].numel() * m["dY"].element_size() for m in mats)
+    input_bytes = sum(X.numel() * X.element_size() + Y.numel() * Y.element_size() for X, Y in inputs.values())
+    step_input_bytes = sum(m["X"].numel() * m["X"].element_size() + m["dY"].numel() * m["dY"].element_size()
+                           for m in mats)
 
     # a side stream as the step's main stream (a CUDA graph cannot be captured on the legacy
     # default stream, and the library's per-stream workspaces must be the ones warmed up)
@@ -539,7 +566,9 @@ def run_ours(args):
     else:
         ach = f1 / (call_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": ach, "peak": tc, "unit": "TFLOP/s", "frac": ach / tc}
-    roof.update({"traffic": SKETCH_TRAFFIC_PER_CALL.get((n, dmax, kmax, r)),
+    traffic = SKETCH_TRAFFIC_PER_CALL.get((n, dmax, kmax, r))
+    roof.update({"traffic": traffic[0] if traffic else None,
+                 "traffic_source": traffic[1] if traffic else "no ncu capture of this shape: null",
                  "algorithmic_bytes_per_call": b1, "flops_per_call": f1, "ms_per_call": call_ms,
                  "kernel": f"logra_sketch_accumulate on the {dmax}x{kmax} matrix, n={n}, r={r} "
                            "(project + split + accumulate launches)",
@@ -549,15 +578,16 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; torch Philox on device)",
-        "config": {"workload": w.name, "layers": layers, "matrices": [list(x) for x in w.matrices],
-                   "microbatches": nmb, "tokens": n, "r": r, "mask_frac": w.mask_frac,
-                   "input_bytes_resident": input_bytes, "input_generation_ms": gen_ms,
-                   "l2": "inputs larger than L2, no flush",
-                   "parallelism": f"dp{world}", "streams": len(streams), "apply_mode": args.apply_mode,
-                   "microbatches_spread_over_streams": bool(spread), "concurrency_hint": len(streams),
-                   "cuda_graph": bool(args.graph),
-                   "component_timing": "components and roofline: CUDA events around each call in one "
-                   "extra step issued on a single stream right after the timed region"},
+        "config": workload_config(w, layers, nmb, r, world, pool),
+        "run": {"input_bytes_resident": input_bytes, "input_bytes_per_step": step_input_bytes,
+                "input_pool": (f"layer l reads the inputs of resident slot l mod {pool}; W, S, v and the "
+                               "sign matrices are per layer") if pool < layers else "every layer its own inputs",
+                "input_generation_ms": gen_ms,
+                "streams": len(streams), "apply_mode": args.apply_mode,
+                "microbatches_spread_over_streams": bool(spread), "concurrency_hint": len(streams),
+                "cuda_graph": bool(args.graph),
+                "component_timing": "components and roofline: CUDA events around each call in one "
+                "extra step issued on a single stream right after the timed region"},
         "components": {
             "sketch": {"ms_per_step": sk_ms, "tflops": sk_tflops, "gbs": sk_gbs,
                        "frac_of_roofline": sk_roof_ms / sk_ms, "roofline_ms": sk_roof_ms},

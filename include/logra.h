@@ -112,6 +112,17 @@ int logra_sign_matrix(uint64_t seed, uint64_t step, int r, int64_t k,
  * S is updated with atomic fp32 additions, so calls that add into the same S
  * (different microbatches of one step) may run concurrently on different
  * streams; the sum is then formed in an unspecified order.
+ * Run-to-run determinism: partial sums of the projection and of S are added
+ * by TMA reduce-adds whose order depends on CTA timing, so S may differ in
+ * its last bits between two identical calls, even on one stream (the spread
+ * is rounding-sized, far inside the 1e-3 parity tolerance).  A, and the
+ * apply's W, v, bf16 copy and sync sketch for given S bits, are
+ * deterministic.
+ * CUDA graphs: a captured call keeps using the capturing stream's workspace
+ * when replayed, so replays must be ordered with other work on that stream.
+ * Once any call on a stream has been captured, that stream's sketch calls
+ * clear their projection scratch with a memset on every call (eager calls
+ * otherwise skip it when the previous sketch on the stream left it zero).
  */
 int logra_sketch_accumulate(const void* X, const void* dY, int in_dtype,
                             int64_t n, int64_t d, int64_t k, int r,

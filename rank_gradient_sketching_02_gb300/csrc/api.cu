@@ -60,7 +60,7 @@ struct Buffer {
   size_t bytes = 0;
   unsigned* counters = nullptr;   // kCounterWords zero-initialised words, never freed while the stream's entry lives
   int* gram = nullptr;            // kGramCountInts Gram counts, zero between applies
-  size_t zero = 0;                // leading bytes of ptr known to be zero
+  ZeroTrack zero;                 // leading bytes of ptr known to be zero
 };
 std::map<std::pair<int, cudaStream_t>, Buffer> g_ws;
 
@@ -102,16 +102,23 @@ int sm_count() {
 
 void forget_zero_workspaces() {
   std::lock_guard<std::mutex> lk(g_mu);
-  for (auto& e : g_ws) e.second.zero = 0;
+  for (auto& e : g_ws) e.second.zero.bytes.store(0);
 }
 
-void* workspace(cudaStream_t stream, size_t bytes, int* status, size_t** zero_bytes) {
+void* workspace(cudaStream_t stream, size_t bytes, int* status, ZeroTrack** zt) {
   *status = LOGRA_OK;
   int dev;
   if ((*status = current_device(&dev))) return nullptr;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t ce = cudaStreamIsCapturing(stream, &cap);
+  if (ce != cudaSuccess) {
+    *status = cuda_fail(ce);
+    return nullptr;
+  }
   std::lock_guard<std::mutex> lk(g_mu);
   Buffer& b = g_ws[std::make_pair(dev, stream)];
-  if (zero_bytes) *zero_bytes = &b.zero;
+  if (cap != cudaStreamCaptureStatusNone) b.zero.captured.store(true);
+  if (zt) *zt = &b.zero;
   if (b.bytes < bytes) {
     if (b.ptr) {
       // Work already queued on this stream may still read the old buffer.
@@ -125,7 +132,7 @@ void* workspace(cudaStream_t stream, size_t bytes, int* status, size_t** zero_by
       }
     }
     size_t want = bytes < (size_t(1) << 20) ? (size_t(1) << 20) : bytes;
-    b.zero = 0;
+    b.zero.bytes.store(0);
     cudaError_t e = cudaMalloc(&b.ptr, want);
     if (e != cudaSuccess) {
       b.ptr = nullptr;
@@ -278,7 +285,7 @@ int logra_sketch_accumulate(const void* X, const void* dY, int in_dtype, int64_t
   if (!X || !dY) return LOGRA_ERR_INVALID_ARG;
   if (!aligned16(X) || !aligned16(dY) || !aligned16(S)) return LOGRA_ERR_UNSUPPORTED;
   int st;
-  size_t* zero = nullptr;
+  ZeroTrack* zero = nullptr;
   void* ws = workspace(stream, logra_sketch_workspace_bytes(n, d, k, r, in_dtype), &st, &zero);
   if (st) return st;
   if (in_dtype == LOGRA_BF16) {
@@ -286,7 +293,7 @@ int logra_sketch_accumulate(const void* X, const void* dY, int in_dtype, int64_t
     if (!ctl) return st;
     return launch_sketch_tc(X, dY, n, d, k, r, step_key(seed, step), inv_sqrt_r(r), S, ws, zero, ctl, stream);
   }
-  *zero = 0;                      // the fp32 path keeps its P in the workspace
+  zero->bytes.store(0);           // the fp32 path keeps its P in the workspace
   return launch_sketch_simt(X, dY, in_dtype, n, d, k, r, step_key(seed, step), inv_sqrt_r(r), S,
                             static_cast<float*>(ws), stream);
 }
@@ -315,10 +322,10 @@ static int rowadam_common(int mode, float* W, const float* S, float* v, int64_t 
       (sync_out && !aligned16(sync_out)) || (norms_out && !aligned16(norms_out)))
     return LOGRA_ERR_UNSUPPORTED;
   int st;
-  size_t* zero = nullptr;
+  ZeroTrack* zero = nullptr;
   char* ws = static_cast<char*>(workspace(stream, logra_apply_workspace_bytes(d, k, r), &st, &zero));
   if (st) return st;
-  *zero = 0;                      // the apply overwrites the workspace
+  zero->bytes.store(0);           // the apply overwrites the workspace
   Control* ctl = control_block(&st);
   if (!ctl) return st;
   RowAdamItem it{};
@@ -396,10 +403,10 @@ int logra_reconstruct(const float* S, int64_t d, int64_t k, int r, uint64_t seed
   if (check_rank(r)) return LOGRA_ERR_UNSUPPORTED;
   if (!aligned16(S) || !aligned16(dW_out)) return LOGRA_ERR_UNSUPPORTED;
   int st;
-  size_t* zero = nullptr;
+  ZeroTrack* zero = nullptr;
   char* ws = static_cast<char*>(workspace(stream, logra_apply_workspace_bytes(d, k, r), &st, &zero));
   if (st) return st;
-  *zero = 0;
+  zero->bytes.store(0);
   Control* ctl = control_block(&st);
   if (!ctl) return st;
   RowAdamItem it{};
@@ -435,10 +442,10 @@ int logra_rowadam_apply_group(const logra_apply_item* items, int count, int r, u
   }
   if (count == 0) return LOGRA_OK;
   int st;
-  size_t* zero = nullptr;
+  ZeroTrack* zero = nullptr;
   char* ws = static_cast<char*>(workspace(stream, group_workspace_bytes(items, count, r), &st, &zero));
   if (st) return st;
-  *zero = 0;
+  zero->bytes.store(0);
   Control* ctl = control_block(&st);
   if (!ctl) return st;
   for (int g = 0; g < count; g += kMaxGroup) {

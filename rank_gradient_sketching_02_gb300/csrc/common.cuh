@@ -1,6 +1,7 @@
 // Shared device helpers of liblogra: the sign hash, status word, launch checks.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -52,11 +53,22 @@ __device__ __forceinline__ void record_status(Control* ctl, int code) {
 }
 
 Control* control_block(int* status);                     // current device
-// The per-(device, stream) scratch workspace, grown on demand.  zero_bytes
-// (optional) receives the address of its count of leading bytes known to be
-// zero: 0 after every (re)allocation; users that overwrite the workspace set
-// it to 0, the sketch keeps it up to date.
-void* workspace(cudaStream_t stream, size_t bytes, int* status, size_t** zero_bytes = nullptr);
+// What the host knows about the leading bytes of a workspace being zero
+// (the sketch's projection reduce-adds into a zeroed P^T at its start).
+// `bytes` holds only for eagerly issued work: once any call on the workspace
+// has been captured into a CUDA graph, replays may change it behind the
+// host's back, so `captured` is set for good and nothing is trusted again.
+struct ZeroTrack {
+  std::atomic<size_t> bytes{0};
+  std::atomic<bool> captured{false};
+  // leading bytes that are zero for certain when the next launch runs
+  size_t trusted() const { return captured.load() ? 0 : bytes.load(); }
+};
+// The per-(device, stream) scratch workspace, grown on demand.  zt (optional)
+// receives its ZeroTrack: bytes = 0 after every (re)allocation; users that
+// overwrite the workspace set it to 0, the sketch keeps it up to date.  A call
+// made while `stream` is capturing marks the workspace as captured.
+void* workspace(cudaStream_t stream, size_t bytes, int* status, ZeroTrack** zt = nullptr);
 // Forget every workspace's known-zero prefix (after a device-side failure).
 void forget_zero_workspaces();
 // Zero-initialised counters per (device, stream) for in-kernel last-CTA

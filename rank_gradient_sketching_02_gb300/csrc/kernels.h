@@ -24,9 +24,10 @@ int launch_sketch_simt(const void* X, const void* dY, int dtype, int64_t n, int6
                        uint64_t key, float scale, float* S, float* P, cudaStream_t s);
 
 size_t sketch_tc_workspace_bytes(int64_t n, int64_t d, int64_t k, int r, int sms);
-// ws_zero: leading bytes of ws known to be zero (read and updated), or null
+struct ZeroTrack;
+// zt: what is known about ws being zero (read and updated), or null (nothing)
 int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_t k, int r, uint64_t key,
-                     float scale, float* S, void* ws, size_t* ws_zero, Control* ctl, cudaStream_t s);
+                     float scale, float* S, void* ws, ZeroTrack* zt, Control* ctl, cudaStream_t s);
 
 size_t s_image_bytes(int64_t d, int r);
 

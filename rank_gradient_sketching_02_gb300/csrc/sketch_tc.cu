@@ -250,8 +250,8 @@ __global__ void __launch_bounds__(512, 1)
       while (it.next(grp, c0, c1)) {
         for (int c = c0; c < c1; ++c) {
           if (!wait_or_abort(sh, &sh->s_empty[xr.stage], xr.phase ^ 1u, limit, ctl)) goto producer_done;
-          if (inject && c == c0 + 1) {
-            inject = 0;                      // test hook: this stage never fills
+          if (inject) {
+            inject = 0;                      // test hook: this CTA's first stage never fills
           } else {
             uint8_t* dst = x_tiles + size_t(xr.stage) * x_bytes;
             mbar_arrive_expect_tx(&sh->s_full[xr.stage], x_bytes);
@@ -480,8 +480,8 @@ __global__ void __launch_bounds__(352, 1)
       while (it.next(dt, c0, c1)) {
         for (int c = c0; c < c1; ++c) {
           if (!wait_or_abort(sh, &sh->o_empty[ar.stage], ar.phase ^ 1u, limit, ctl)) goto a_done;
-          if (inject && c == c0 + 1) {
-            inject = 0;
+          if (inject) {
+            inject = 0;                      // test hook: this CTA's first stage never fills
           } else {
             mbar_arrive_expect_tx(&sh->o_full[ar.stage], a_bytes);
             bulk_load(a_tiles + size_t(ar.stage) * a_bytes, image + size_t(c) * a_bytes, a_bytes,
@@ -700,7 +700,7 @@ size_t sketch_tc_workspace_bytes(int64_t n, int64_t d, int64_t k, int r, int sms
 }
 
 int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_t k, int r, uint64_t key,
-                     float scale, float* S, void* ws, size_t* ws_zero, Control* ctl, cudaStream_t s) {
+                     float scale, float* S, void* ws, ZeroTrack* zt, Control* ctl, cudaStream_t s) {
   const int sms = sm_count();
   const SketchShape P = plan(n, d, k, r, sms);
   float* ppart = static_cast<float*>(ws);
@@ -724,11 +724,17 @@ int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_
 
   const int proj_smem = proj_smem_bytes(P);
   LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(project_tc_kernel), proj_smem));
-  // segments with a partial k range reduce-add into P^T, so it starts at zero:
-  // each call's accumulate leaves its P^T at zero for the next, and
-  // `ws_zero` (null: unknown) counts the leading workspace bytes known to be
-  // zero; only a larger P^T, or other use of the workspace, needs a memset
-  if (P.proj_partial && (!ws_zero || *ws_zero < part)) LOGRA_CUDA_TRY(cudaMemsetAsync(ppart, 0, part, s));
+  // Segments with a partial k range reduce-add into P^T, so it starts at zero:
+  // each call's accumulate leaves its P^T at zero for the next, and `zt`
+  // (null: unknown) says how many leading workspace bytes are zero for
+  // certain; only a larger P^T, other use of the workspace, a call that did
+  // not complete, or any stream capture on the workspace needs a memset.
+  // Nothing is known while these launches are outstanding: `bytes` is set
+  // again only once all three have been issued.
+  const bool tracked = zt && !zt->captured.load();
+  const bool trusted = tracked && zt->trusted() >= part;
+  if (zt) zt->bytes.store(0);
+  if (P.proj_partial && !trusted) LOGRA_CUDA_TRY(cudaMemsetAsync(ppart, 0, part, s));
   LOGRA_CUDA_TRY(launch_overlapped(project_tc_kernel, dim3(P.proj_ctas), dim3(512), size_t(proj_smem), s, tx, tp, P,
                                    key, ctl));
   LOGRA_LAUNCHED();
@@ -742,12 +748,12 @@ int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_
 
   const int acc_smem = acc_smem_bytes(P);
   LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(accumulate_tc_kernel), acc_smem));
-  float4* pzero = ws_zero ? reinterpret_cast<float4*>(ppart) : nullptr;
+  float4* pzero = tracked ? reinterpret_cast<float4*>(ppart) : nullptr;
   LOGRA_CUDA_TRY(launch_overlapped(accumulate_tc_kernel, dim3(P.acc_ctas), dim3(352), size_t(acc_smem), s, tdy, ts, P,
                                    static_cast<const uint8_t*>(image), scale, pzero, int64_t(part / 16), ctl));
   LOGRA_LAUNCHED();
   // known zero now: this call's P^T region, and nothing past it (the image follows it)
-  if (ws_zero) *ws_zero = part;
+  if (tracked) zt->bytes.store(part);
   return LOGRA_OK;
 }
 

@@ -14,6 +14,7 @@ import math
 import numpy as np
 import pytest
 
+from canary import Guarded
 from oracle import logra_oracle as O
 from rank_gradient_sketching_02_gb300 import synth
 
@@ -54,7 +55,11 @@ def host64(t):
 @pytest.mark.parametrize("seed,step,r,k", [(0, 0, 32, 512), (12345, 7, 256, 1536), (2**63 + 5, 2**40, 512, 200),
                                            (3, 1, 64, 1), (9, 9, 128, 27648)])
 def test_sign_matrix_bit_exact(L, seed, step, r, k):
-    A = L.logra_sign_matrix(seed, step, r, k).cpu().numpy()
+    import torch
+    gA = Guarded((r, k), torch.float32)
+    L.logra_sign_matrix(seed, step, r, k, gA.t)
+    gA.check("A")
+    A = gA.t.cpu().numpy()
     want = O.projection_matrix_fp32(seed, step, r, k)
     assert np.array_equal(A.view(np.uint32), want.view(np.uint32))
 
@@ -62,13 +67,14 @@ def test_sign_matrix_bit_exact(L, seed, step, r, k):
 # ------------------------------------------------------------------ sketch
 def run_sketch(L, mbs, d, r, dtype, seed, step):
     import torch
-    S = torch.zeros((d, r), dtype=torch.float32, device="cuda")
+    gS = Guarded((d, r), torch.float32, fill=0.0)           # S between guard regions
+    S = gS.t
     S_or = np.zeros((d, r))
     for X, dY in mbs:
         Xd, dYd = to_dev(X, dtype), to_dev(dY, dtype)
         L.logra_sketch_accumulate(Xd, dYd, S, seed, step)
         S_or = O.sketch_accumulate(S_or, host64(Xd), host64(dYd), seed, step, r)
-    torch.cuda.synchronize()
+    gS.check("S")
     return host64(S), S_or
 
 
@@ -159,14 +165,14 @@ def test_apply_stagewise_zero_w0(L, d, k, r):
     import torch
     S32 = _sketch_like(d, r, d + k)
     v0 = (np.abs(np.random.default_rng(1).standard_normal(d)) * 1e-8).astype(np.float32)
-    S, v = to_dev(S32, "f32"), to_dev(v0, "f32")
-    W = torch.zeros((d, k), dtype=torch.float32, device="cuda")
-    Wb = torch.empty((d, k), dtype=torch.bfloat16, device="cuda")
-    sync = torch.empty((d, r), dtype=torch.float32, device="cuda")
-    norms = torch.zeros(2, dtype=torch.float64, device="cuda")
+    S = to_dev(S32, "f32")
+    guards = [Guarded((d,), torch.float32, fill=to_dev(v0, "f32")), Guarded((d, k), torch.float32, fill=0.0),
+              Guarded((d, k), torch.bfloat16), Guarded((d, r), torch.float32), Guarded((2,), torch.float64, fill=0.0)]
+    v, W, Wb, sync, norms = (g.t for g in guards)
     beta2, eps, lr, c = (float(np.float32(x)) for x in (0.999, 1e-8, 1e-5, 0.75))
     L.logra_rowadam_apply_ex(W, S, v, 11, 4, beta2, eps, lr, c, norms, Wb, sync)
-    torch.cuda.synchronize()
+    for g, what in zip(guards, ("v", "W", "W bf16", "sync sketch", "norms")):
+        g.check(what)
     W_or, v_or, n_or, dW_or = O.rowadam_apply(np.zeros((d, k)), S32.astype(np.float64), v0.astype(np.float64),
                                               11, 4, beta2, eps, lr, c)
     assert rel(host64(v), v_or) <= TOL_V
@@ -249,18 +255,20 @@ def test_reconstruct(L, d, k, r):
     S32 = _sketch_like(d, r, 7)
     S = to_dev(S32, "f32")
     want = O.reconstruct(S32.astype(np.float64), 13, 2, k)
-    out = torch.empty((d, k), dtype=torch.float32, device="cuda")
+    gout = Guarded((d, k), torch.float32)
+    out = gout.t
     L.logra_reconstruct(S, k, 13, 2, out)
-    torch.cuda.synchronize()
+    gout.check("reconstruct out")
     assert rel(host64(out), want) <= 1e-5
     base = np.random.default_rng(8).standard_normal((d, k)).astype(np.float32)
     out = to_dev(base, "f32")
     L.logra_reconstruct(S, k, 13, 2, out, accumulate=True)
     torch.cuda.synchronize()
     assert rel(host64(out) - base, want) <= 1e-4
-    ob = torch.empty((d, k), dtype=torch.bfloat16, device="cuda")
+    gob = Guarded((d, k), torch.bfloat16)
+    ob = gob.t
     L.logra_reconstruct(S, k, 13, 2, ob)
-    torch.cuda.synchronize()
+    gob.check("reconstruct bf16 out")
     assert rel(host64(ob), want) <= 4e-3          # one bf16 rounding of each element
 
 
