@@ -68,6 +68,9 @@ struct SketchShape {
   int ntile_n, dtiles, acc_ctas;   // accumulate: d tile width, d tiles, grid
   int x_stages, g_stages;      // project rings: X tiles, sign tiles
   int a_stages, b_stages;      // accumulate rings: P^T chunks, dY tiles
+  // accumulate on CTA pairs (r_pad 256 or 512): rank blocks of 256 and d blocks
+  // of 256 per pair tile (prb * pdb = 2), pair tiles along d, pairs (clusters)
+  int pair, prb, pdb, pdtiles, pairs;
 };
 
 struct Shared {
@@ -99,6 +102,11 @@ struct SegIter {
   __device__ __forceinline__ SegIter(int64_t total, int per_) : per(per_) {
     f = total * blockIdx.x / gridDim.x;
     f1 = total * (blockIdx.x + 1) / gridDim.x;
+  }
+  // range number `idx` of `count` (e.g. one per CTA pair)
+  __device__ __forceinline__ SegIter(int64_t total, int per_, int idx, int count) : per(per_) {
+    f = total * idx / count;
+    f1 = total * (idx + 1) / count;
   }
   __device__ __forceinline__ bool next(int& tile, int& c0, int& c1) {
     if (f >= f1) return false;
@@ -149,6 +157,39 @@ __device__ __forceinline__ void accumulate_chunk_mmas(uint32_t acc0, uint32_t N,
       mma_bf16(acc0 + uint32_t(m) * N, am + 4, bk, idesc, 1u);   // lo term: bytes 64..127 of each row
     }
   }
+}
+
+// Accumulate on a CTA pair, one token chunk: RB rank blocks x DB d blocks of
+// M256 x N256 accumulators (TMEM columns (rb * DB + db) * 256), hi and lo terms.
+// A: this CTA's 128 rows of each rank block, 16 KB apart; B: this CTA's 128
+// d-columns of each d block, two 64-column boxes of kChunk tokens, 8 KB apart.
+template <int RB, int DB>
+__device__ __forceinline__ void accumulate_pair_mmas(uint32_t tmem, uint64_t ad, uint64_t bd, uint32_t idesc,
+                                                     uint32_t first) {
+#pragma unroll
+  for (int ks = 0; ks < kChunk / 16; ++ks)
+#pragma unroll
+    for (int rb = 0; rb < RB; ++rb) {
+      const uint64_t am = ad + uint64_t(rb * (16384 >> 4) + 2 * ks);
+#pragma unroll
+      for (int db = 0; db < DB; ++db) {
+        const uint32_t acc = tmem + uint32_t((rb * DB + db) * 256);
+        const uint64_t bk = bd + uint64_t(db * ((2 * kChunk * 128) >> 4) + ks * (2048 >> 4));
+        mma_bf16_pair(acc, am, bk, idesc, ks ? 1u : first);
+        mma_bf16_pair(acc, am + 4, bk, idesc, 1u);     // lo term: bytes 64..127 of each row
+      }
+    }
+}
+
+// warp_wait for a barrier completed from the other CTA of a pair.
+template <class SH>
+__device__ __forceinline__ bool warp_wait_cluster(SH* sh, uint64_t* bar, uint32_t parity, unsigned long long limit,
+                                                  Control* ctl) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = wait_or_abort_cluster(sh, bar, parity, limit, ctl) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) (void)mbar_try_wait_cluster(bar, parity);
+  return ok != 0;
 }
 
 // Copies still in flight land before the CTA exits: wait (bounded) for the
@@ -612,6 +653,220 @@ __global__ void __launch_bounds__(352, 1)
   }
 }
 
+// ============================================================================ accumulate on CTA pairs
+// For r_pad = 256 or 512.  The MMAs of a pair tile run on two CTAs of a cluster
+// (tcgen05 cta_group::2, M = 256 ranks across the pair): each CTA holds only
+// its own half of every operand (its 128 ranks of each 256-rank block of the
+// P^T chunk, its 128 d-columns of each 256-column block of the dY tile), and
+// the hardware hands the B halves across the pair.  A pair tile is
+// 256 prb ranks x 256 pdb d-columns with prb * pdb = 2, so each CTA's TMEM
+// holds two 128 x 256 fp32 accumulators (512 columns); per 32-token chunk a
+// CTA takes in 32 KB (prb 1) or 40 KB (prb 2) of operands for 1024 MMA cycles,
+// against 48 KB (r_pad 256) or 72 KB (r_pad 512) on a single CTA, which is
+// what limits the single-CTA kernel (operand ingest, not the tensor pipe).
+//
+// Protocol: the even CTA (leader) issues every MMA.  Both CTAs' producers load
+// into their own shared memory and signal the LEADER's full barriers
+// (cta_group::2 tensor copies); the leader's producers post the expected bytes
+// of both halves.  The leader's commits arrive on both CTAs' empty and
+// accumulator-full barriers (multicast); both CTAs' epilogue warps drain their
+// own TMEM lanes and arrive on the leader's accumulator-empty barrier.  Every
+// wait is bounded; a cluster barrier precedes the first cross-CTA signal and
+// the TMEM release, so neither CTA leaves while the other may still use it.
+__global__ void __launch_bounds__(352, 1)
+    accumulate_pair_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_s,
+                           const __grid_constant__ CUtensorMap tmap_img, SketchShape sh_, float scale, float4* pzero,
+                           int64_t pzero_n, Control* ctl) {
+  extern __shared__ uint8_t smem_raw[];
+  const SketchShape& P = sh_;
+  uint8_t* base = align1024(smem_raw);
+  const int AS = P.a_stages, BS = P.b_stages;
+  const int RB = P.prb, DB = P.pdb;
+  const uint32_t a_bytes = uint32_t(RB) * 128 * 128;           // 128 ranks per rank block, 32 tokens hi + lo
+  const uint32_t b_bytes = uint32_t(DB) * 2 * kChunk * 128;    // 128 d-columns per d block, 32 tokens
+  uint8_t* a_tiles = base;
+  uint8_t* b_tiles = base + size_t(AS) * a_bytes;
+  uint8_t* staging = b_tiles + size_t(BS) * b_bytes;
+  Shared* sh = reinterpret_cast<Shared*>(staging + kStagingBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned long long limit = ctl->wait_limit;
+  const uint32_t cta = cluster_ctarank();
+  const bool leader = cta == 0;
+  const int pair = int(cluster_id_x()), npairs = int(cluster_count_x());
+  const int nchunks = P.n_pad / kChunk;
+  const int64_t total = int64_t(P.pdtiles) * nchunks;
+  const int pdt = DB * 256;
+  constexpr uint32_t kTmemCols = 512;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < BS; ++s) {
+      mbar_init(&sh->s_full[s], 1);
+      mbar_init(&sh->s_empty[s], 1);
+    }
+    for (int s = 0; s < AS; ++s) {
+      mbar_init(&sh->o_full[s], 1);
+      mbar_init(&sh->o_empty[s], 1);
+    }
+    mbar_init(&sh->tmem_full[0], 1);
+    mbar_init(&sh->tmem_empty[0], 16);     // the 8 epilogue warps of each CTA of the pair
+    mbar_init(&sh->drain, 1);
+    sh->abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmap_dy);
+    prefetch_tmap(&tmap_img);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&sh->tmem_base, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = sh->tmem_base;
+  grid_dependency_wait();      // the image comes from the split just before, S from earlier calls
+  int dt, c0, c1;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- P^T chunk producer (L2)
+    if (lane == 0) {
+      Ring ar;
+      int inject = ctl->inject_fault && blockIdx.x == 0;
+      SegIter it(total, nchunks, pair, npairs);
+      while (it.next(dt, c0, c1)) {
+        for (int c = c0; c < c1; ++c) {
+          if (!wait_or_abort_cluster(sh, &sh->o_empty[ar.stage], ar.phase ^ 1u, limit, ctl)) goto a_done;
+          if (inject) {
+            inject = 0;                      // test hook: this pair's first stage never fills
+          } else {
+            const uint32_t full = mapa_shared(smem_addr(&sh->o_full[ar.stage]), 0);
+            if (leader) mbar_arrive_expect_tx(&sh->o_full[ar.stage], 2 * a_bytes);
+            for (int rb = 0; rb < RB; ++rb)
+              tma_load_2d_pair(a_tiles + size_t(ar.stage) * a_bytes + rb * 16384, &tmap_img, full, 0,
+                               c * P.r_pad + rb * 256 + int(cta) * 128);
+          }
+          ar.next(AS);
+        }
+      }
+    a_done:
+      // the peer's copies complete on the leader's barriers: the leader waits for both halves
+      if (leader) drain_ring(sh->o_full, ar, AS, limit);
+    }
+  } else if (warp == 6) {
+    // ---------------------------------------------------------------- dY tile producer (HBM)
+    if (lane == 0) {
+      Ring br;
+      SegIter it(total, nchunks, pair, npairs);
+      while (it.next(dt, c0, c1)) {
+        for (int c = c0; c < c1; ++c) {
+          if (!wait_or_abort_cluster(sh, &sh->s_empty[br.stage], br.phase ^ 1u, limit, ctl)) goto b_done;
+          const uint32_t full = mapa_shared(smem_addr(&sh->s_full[br.stage]), 0);
+          if (leader) mbar_arrive_expect_tx(&sh->s_full[br.stage], 2 * b_bytes);
+          uint8_t* st = b_tiles + size_t(br.stage) * b_bytes;
+          for (int db = 0; db < DB; ++db)
+            for (int h = 0; h < 2; ++h)
+              tma_load_2d_pair(st + (db * 2 + h) * (kChunk * 128), &tmap_dy, full,
+                               dt * pdt + db * 256 + int(cta) * 128 + h * 64, c * kChunk);
+          br.next(BS);
+        }
+      }
+    b_done:
+      if (leader) drain_ring(sh->s_full, br, BS, limit);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer (leader only)
+    if (lane == 0 && leader) {
+      Ring ar, br;
+      const uint32_t idesc = idesc_bf16(256, 256, 0, 1);
+      const uint64_t adesc0 = smem_desc(smem_addr(a_tiles), 16, 1024, kSw128);
+      const uint64_t bdesc0 = smem_desc(smem_addr(b_tiles), kChunk * 128, 1024, kSw128);
+      SegIter it(total, nchunks, pair, npairs);
+      for (int seg = 0; !sh->abort && it.next(dt, c0, c1); ++seg) {
+        // both CTAs have drained the accumulators of the previous segment
+        if (!wait_or_abort_cluster(sh, &sh->tmem_empty[0], (uint32_t(seg) & 1u) ^ 1u, limit, ctl)) goto mma_done;
+        tc_fence_after();
+        for (int c = c0; c < c1; ++c) {
+          if (!wait_or_abort_cluster(sh, &sh->o_full[ar.stage], ar.phase, limit, ctl)) goto mma_done;
+          if (!wait_or_abort_cluster(sh, &sh->s_full[br.stage], br.phase, limit, ctl)) goto mma_done;
+          tc_fence_after();
+          const uint64_t ad = adesc0 + uint64_t(uint32_t(ar.stage) * (a_bytes >> 4));
+          const uint64_t bd = bdesc0 + uint64_t(uint32_t(br.stage) * (b_bytes >> 4));
+          const uint32_t first = (c == c0) ? 0u : 1u;
+          if (RB == 1)
+            accumulate_pair_mmas<1, 2>(tmem, ad, bd, idesc, first);
+          else
+            accumulate_pair_mmas<2, 1>(tmem, ad, bd, idesc, first);
+          mma_commit_pair(&sh->o_empty[ar.stage], 3);
+          mma_commit_pair(&sh->s_empty[br.stage], 3);
+          ar.next(AS);
+          br.next(BS);
+        }
+        mma_commit_pair(&sh->tmem_full[0], 3);
+      }
+    mma_done:
+      mma_commit_pair(&sh->drain, 1);
+      mbar_wait(&sh->drain, 0, limit);
+    }
+  } else if ((warp >= 2 && warp < 6) || (warp >= 7 && warp < 11)) {
+    // ---------------------------------------------------------------- epilogue: TMEM -> smem -> TMA reduce-add into S
+    // Two groups of four warps cover all four TMEM lane quadrants each; group g
+    // drains columns [128 g, 128 g + 128) of both accumulators.
+    const int quad = warp & 3;
+    const int grp = warp >= 7 ? 1 : 0;
+    const int eidx = grp * 4 + (warp - (grp ? 7 : 2));
+    float* tile = reinterpret_cast<float*>(staging + eidx * kStageTile);
+    const uint32_t empty_leader = mapa_shared(smem_addr(&sh->tmem_empty[0]), 0);
+    // the split has consumed this call's P^T: set it back to zero for the next call
+    if (pzero) {
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int64_t i = int64_t(blockIdx.x) * 256 + eidx * 32 + lane; i < pzero_n; i += int64_t(gridDim.x) * 256)
+        pzero[i] = z;
+    }
+    SegIter it(total, nchunks, pair, npairs);
+    for (int seg = 0; it.next(dt, c0, c1); ++seg) {
+      if (!warp_wait_cluster(sh, &sh->tmem_full[0], uint32_t(seg) & 1u, limit, ctl)) break;
+      tc_fence_after();
+      for (int a = 0; a < RB * DB; ++a) {
+        const int rb = a / DB, db = a - (a / DB) * DB;
+        const int r0 = rb * 256 + int(cta) * 128 + quad * 32;     // first rank of this warp's lanes
+        for (int c = grp * 128; c < grp * 128 + 128; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + uint32_t(a * 256 + c), v);
+          tmem_ld_wait();
+          // staging tile [32 d-rows][32 ranks] = a box of S (d x r, row-major); lane = rank
+#pragma unroll
+          for (int j = 0; j < 32; ++j) tile[j * 32 + lane] = __uint_as_float(v[j]) * scale;
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int64_t d0 = int64_t(dt) * pdt + db * 256 + c;
+            if (r0 < P.r && d0 < P.d) tma_reduce_add_2d(&tmap_s, tile, r0, int32_t(d0));
+            bulk_commit();
+            bulk_wait_read_all();    // the staging tile is free again
+          }
+          __syncwarp();
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(&sh->tmem_empty[0]);
+        else mbar_arrive_cluster(empty_leader);
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();              // the leader's MMAs are done with this CTA's memory; no more signals
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
 // ============================================================================ host side
 static int ceil_div(int64_t a, int64_t b) { return int((a + b - 1) / b); }
 
@@ -663,11 +918,18 @@ static SketchShape plan(int64_t n, int64_t d, int64_t k, int r, int sms) {
   P.ntile_n = (P.r_pad <= 256) ? 256 : 128;
   P.dtiles = ceil_div(d, P.ntile_n);
   const int tchunks = P.n_pad / kChunk;
+  P.pair = (P.r_pad == 256 || P.r_pad == 512) && sms >= 2 ? 1 : 0;
+  if (P.pair) {
+    P.prb = P.r_pad / 256;
+    P.pdb = 2 / P.prb;
+    P.pdtiles = ceil_div(d, P.pdb * 256);
+    P.pairs = stream_k_ctas_hinted(int64_t(P.pdtiles) * tchunks, sms / 2, 12, 12 * hint, hint);
+  }
   // With sketch calls running on several streams at once, each accumulate takes
   // fewer, longer CTA ranges: SMs stay free for the other streams' kernels and
   // fewer partial S tiles are reduced in L2 (4 streams, 27B layers: +1.6% on
   // the step; one stream keeps every SM busy)
-  P.acc_ctas = stream_k_ctas_hinted(int64_t(P.dtiles) * tchunks, sms, 12, 12 * hint, hint);
+  P.acc_ctas = P.pair ? 2 * P.pairs : stream_k_ctas_hinted(int64_t(P.dtiles) * tchunks, sms, 12, 12 * hint, hint);
   // project: three sign-tile stages when three X stages still fit beside
   // them (the generators then have a whole chunk of MMA time of slack), else
   // two; the rest of shared memory for X tiles
@@ -676,8 +938,9 @@ static SketchShape plan(int64_t n, int64_t d, int64_t k, int r, int sms) {
   P.x_stages = (kSmemBudget - kStagingBytes - P.g_stages * r * 128) / x_bytes;
   if (P.x_stages > kMaxStages) P.x_stages = kMaxStages;
   // accumulate: P^T chunks come from L2 (three stages), dY from HBM (the rest)
-  const int a_bytes = P.r_pad * 128, b_bytes = P.ntile_n * kChunk * 2;
-  P.a_stages = P.r_pad >= 512 ? 2 : 3;
+  const int a_bytes = P.pair ? P.prb * 128 * 128 : P.r_pad * 128;
+  const int b_bytes = P.pair ? P.pdb * 2 * kChunk * 128 : P.ntile_n * kChunk * 2;
+  P.a_stages = (P.r_pad >= 512 && !P.pair) ? 2 : 3;
   P.b_stages = (kSmemBudget - kStagingBytes - P.a_stages * a_bytes) / b_bytes;
   if (P.b_stages > kMaxStages) P.b_stages = kMaxStages;
   return P;
@@ -688,6 +951,9 @@ static int proj_smem_bytes(const SketchShape& P) {
 }
 
 static int acc_smem_bytes(const SketchShape& P) {
+  if (P.pair)
+    return 1024 + P.a_stages * P.prb * 128 * 128 + P.b_stages * P.pdb * 2 * kChunk * 128 + kStagingBytes +
+           int(sizeof(Shared));
   return 1024 + P.a_stages * P.r_pad * 128 + P.b_stages * P.ntile_n * kChunk * 2 + kStagingBytes +
          int(sizeof(Shared));
 }
@@ -747,10 +1013,23 @@ int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_
   LOGRA_LAUNCHED();
 
   const int acc_smem = acc_smem_bytes(P);
-  LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(accumulate_tc_kernel), acc_smem));
   float4* pzero = tracked ? reinterpret_cast<float4*>(ppart) : nullptr;
-  LOGRA_CUDA_TRY(launch_overlapped(accumulate_tc_kernel, dim3(P.acc_ctas), dim3(352), size_t(acc_smem), s, tdy, ts, P,
-                                   static_cast<const uint8_t*>(image), scale, pzero, int64_t(part / 16), ctl));
+  if (P.pair) {
+    // the P^T image as a 2-D bf16 tensor of 128-byte rows (r_pad rows per 32-token chunk),
+    // already swizzled in memory, loaded in boxes of 128 rows
+    CUtensorMap timg;
+    if (int st = make_tmap_2d(&timg, image, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64,
+                              uint64_t(P.n_pad / kChunk) * uint64_t(P.r_pad), 128, 64, 128,
+                              CU_TENSOR_MAP_SWIZZLE_NONE))
+      return st;
+    LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(accumulate_pair_kernel), acc_smem));
+    LOGRA_CUDA_TRY(launch_overlapped_cluster(accumulate_pair_kernel, dim3(P.acc_ctas), dim3(352), size_t(acc_smem), s,
+                                             2u, tdy, ts, timg, P, scale, pzero, int64_t(part / 16), ctl));
+  } else {
+    LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(accumulate_tc_kernel), acc_smem));
+    LOGRA_CUDA_TRY(launch_overlapped(accumulate_tc_kernel, dim3(P.acc_ctas), dim3(352), size_t(acc_smem), s, tdy, ts,
+                                     P, static_cast<const uint8_t*>(image), scale, pzero, int64_t(part / 16), ctl));
+  }
   LOGRA_LAUNCHED();
   // known zero now: this call's P^T region, and nothing past it (the image follows it)
   if (tracked) zt->bytes.store(part);

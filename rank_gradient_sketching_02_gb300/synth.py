@@ -63,8 +63,9 @@ WORKLOADS = {
                           256, "bf16", 0.25, "lognormal", steps=3),
     "model7b": Workload("model7b", _layer(3584, 512, 18944), 28, 8, 8192, 256,
                         "bf16", 0.25, "lognormal"),
-    # one 27B-class gate projection, for kernel profiling at a size well past L2
+    # one 27B-class / 7B-class gate projection, for kernel profiling at a size well past L2
     "gate27b": Workload("gate27b", (("gate", 27648, 5120),), 1, 2, 8192, 256, "bf16", 0.30, "lognormal"),
+    "gate7b": Workload("gate7b", (("gate", 18944, 3584),), 1, 2, 8192, 256, "bf16", 0.25, "lognormal"),
     "layers27b": Workload("layers27b", _layer(5120, 1024, 27648), 4, 16, 8192,
                           256, "bf16", 0.30, "lognormal", r_sweep=(128, 256, 512)),
 }

@@ -161,9 +161,10 @@ def test_reconstruct_bf16_accumulate_matches_oracle(L):
     got = out.t.cpu()
     want = (base.double() + torch.from_numpy(want_d)).to(torch.bfloat16)     # one rounding of the exact sum
     gv, wv = got.double().numpy(), want.double().numpy()
-    # one bf16 rounding of a sum whose fp32 update term carries its own ~1e-6 relative error: within
+    # one bf16 rounding of a sum whose fp32 update term carries its own error (the sketch enters the
+    # contraction as a two-term bf16 expansion, ~2^-16 relative per element, summed over r terms): within
     # one bf16 ulp of the correctly rounded exact sum, plus that term's error where the sum cancels
     ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(wv), 1e-30))) - 7)
-    assert np.all(np.abs(gv - wv) <= ulp + 1e-5 * scale)
+    assert np.all(np.abs(gv - wv) <= ulp + 2e-4 * scale)
     assert np.mean(gv == wv) >= 0.99
     assert np.linalg.norm(gv - wv) / np.linalg.norm(wv) <= 1e-3

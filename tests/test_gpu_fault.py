@@ -38,12 +38,13 @@ def _clean_sketch(L):
     return np.linalg.norm(got - want) / np.linalg.norm(want)
 
 
-def test_sketch_timeout_is_reported_and_context_survives(L):
+@pytest.mark.parametrize("r", [128, 256, 512])      # single-CTA accumulate; CTA-pair accumulate (256, 512)
+def test_sketch_timeout_is_reported_and_context_survives(L, r):
     import torch
     assert L.logra_get_status() == 0
     L.logra_debug_inject(1, SHORT_WAIT)
     try:
-        n, d, k, r = 512, 512, 1024, 128
+        n, d, k = 512, 512, 1024
         X = torch.randn((n, k), device="cuda").to(torch.bfloat16)
         dY = torch.randn((n, d), device="cuda").to(torch.bfloat16)
         S = torch.zeros((d, r), device="cuda")
