@@ -46,12 +46,14 @@ def _one_hot_rows(n, width, cols, dtype):
     return X
 
 
-# (r, k): k % 64 != 0 (a partial last sign word) and k over several 64-column chunks
-SKETCH_CASES = [(32, 200), (96, 1000), (256, 4104), (384, 776), (512, 2056), (256, 27656)]
+# (r, k, tokens per call): k % 64 != 0 (a partial last sign word) and k over several 64-column
+# chunks; r over the single-CTA accumulate (32, 96, 128, 384) and the CTA-pair one (256, 512).
+SKETCH_CASES = [(32, 200, 1500), (96, 1000, 1500), (256, 4104, 1500), (384, 776, 600), (512, 2056, 600),
+                (256, 27656, 1500), (256, 1032, 1500), (128, 520, 1500), (512, 776, 1500)]
 
 
-@pytest.mark.parametrize("r,k", SKETCH_CASES)
-def test_sketch_generator_bit_exact(L, r, k):
+@pytest.mark.parametrize("r,k,per", SKETCH_CASES)
+def test_sketch_generator_bit_exact(L, r, k, per):
     import torch
     seed, step = 0x5EED0000 + r, 3 + k
     A = O.projection_matrix_fp32(seed, step, r, k)            # r x k fp32
@@ -60,7 +62,6 @@ def test_sketch_generator_bit_exact(L, r, k):
     cols = g.permutation(k)
     if k > 5000:
         cols = np.concatenate([cols[:1400], np.arange(k - 70, k)])
-    per = 600 if r >= 384 else 1500
     for c0 in range(0, len(cols), per):
         J = cols[c0:c0 + per]
         n = len(J)
