@@ -23,7 +23,7 @@ workloads remain available.  The metric is sketch TFLOP/s over the whole step (a
 sketch FLOPs 2 n r (k + d) per matrix-microbatch, divided by the step time
 including the apply), with the apply's GB/s and both kernels' roofline
 fractions alongside.  The matrices are independent, so the step issues them
-round robin on --streams CUDA streams (default 4); per-call durations (the
+round robin on --streams CUDA streams (default 8); per-call durations (the
 components and the dominant call's roofline) come from one extra step on a
 single stream right after the timed region; the apply component also reports all of a
 step's apply calls issued at once on up to --apply-streams streams (default 7), and
@@ -57,8 +57,9 @@ METRIC = "sketch TFLOP/s + fused RowAdam-apply GB/s per GB300; % of roofline"
 # (n, d, k, r) -> (bytes, what was captured).  Shapes without an entry report
 # null traffic.
 SKETCH_TRAFFIC_PER_CALL = {
-    # project 92.50 + 2.45 MB, split 8.40 + 0 MB, accumulate 512.66 + 31.71 MB (incl. re-zeroing P^T)
-    (8192, 27648, 5120, 256): (647.7e6, "ncu dram__bytes of the three launches, gate 27648x5120 call"),
+    # project 67.15 + 0.01 MB, split 8.40 + 0 MB, accumulate (CTA pairs) 351.54 + 21.66 MB (incl. re-zeroing P^T)
+    (8192, 18944, 3584, 256): (448.8e6, "ncu dram__bytes_read.sum + dram__bytes_write.sum of the three launches "
+                                        "of one 18944x3584 gate call, kernels as they stand"),
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -77,7 +78,7 @@ def parse_args(argv=None):
     p.add_argument("--input-layers", type=int, default=4,
                    help="distinct layers of resident inputs; layer l reads the inputs of slot l mod this "
                         "(0: every layer its own inputs)")
-    p.add_argument("--streams", type=int, default=4,
+    p.add_argument("--streams", type=int, default=8,
                    help="CUDA streams the matrices are issued on, round robin (each keeps its own workspace)")
     p.add_argument("--apply-streams", type=int, default=7,
                    help="streams for the all-applies-at-once measurement (each with its own workspace)")
