@@ -318,10 +318,12 @@ size_t logra_noalloc_scratch_bytes(void);
  * issues sketch calls at the same time (default 1; process-wide, any thread).
  * It only shapes launches, never results: with streams > 1 each call's
  * accumulate kernel runs on fewer, longer-running CTAs (at least 12 * streams
- * 32-token chunks each) and so does its projection (at least 4 * streams
- * k-chunks, when above 8), which leaves SMs to the other streams' kernels and
- * reduces the partial-sum traffic; a call still keeps at least its fair share
- * of the SMs (SM count / streams) unless its one-stream grid is smaller.
+ * 32-token chunks each) and its projection on one CTA per 256-token group
+ * over the whole k range (no partial sums), which leaves SMs to the other
+ * streams' kernels and removes the partial-sum traffic; a call still keeps at
+ * least its fair share of the SMs (SM count / streams) unless its one-stream
+ * grid is smaller (a projection with fewer groups than that splits their k
+ * ranges evenly over the fair share).
  * With one stream every call spreads over all SMs.  Returns
  * LOGRA_ERR_INVALID_ARG outside [1, 64].
  */

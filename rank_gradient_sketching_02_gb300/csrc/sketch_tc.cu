@@ -910,10 +910,23 @@ static SketchShape plan(int64_t n, int64_t d, int64_t k, int r, int sms) {
   P.groups = ceil_div(P.tiles, P.tgroup);
   P.nchunks = ceil_div(k, kKc);
   const int64_t ptotal = int64_t(P.groups) * P.nchunks;
-  // (with calls on several streams, longer projection ranges too: 16 chunks at
-  // four streams, 7B layers +3%; 32 made the eagerly issued 27B step slower)
+  // With calls on several streams, the projection runs on one CTA per token
+  // group over the whole k range (no partial sums: plain stores, no reduction
+  // at the end) unless that is fewer CTAs than a stream's fair share of the SMs,
+  // in which case the groups' k ranges are split evenly over the fair share.
+  // The projection then takes a quarter of the SM-time of its all-SM form
+  // (most of which is spent on the end-of-kernel L2 reduction of 152 CTAs'
+  // partial sums) and leaves the other SMs to the other streams' accumulates:
+  // 28-layer 7B step on 8 streams 797.9 -> 825.2 TFLOP/s, as a graph 806 -> 848.
   const int hint = concurrency();
-  P.proj_ctas = stream_k_ctas_hinted(ptotal, sms, 8, 4 * hint > 8 ? 4 * hint : 8, hint);
+  if (hint > 1) {
+    const int fair = sms / hint > 1 ? sms / hint : 1;
+    int c = P.groups > fair ? P.groups : fair;
+    if (int64_t(c) > ptotal) c = int(ptotal);
+    P.proj_ctas = c < sms ? c : sms;
+  } else {
+    P.proj_ctas = stream_k_ctas(ptotal, sms, 8);
+  }
   P.proj_partial = has_partial_segment(ptotal, P.nchunks, P.proj_ctas) ? 1 : 0;
   P.ntile_n = (P.r_pad <= 256) ? 256 : 128;
   P.dtiles = ceil_div(d, P.ntile_n);
