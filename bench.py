@@ -84,7 +84,8 @@ def parse_args(argv=None):
                    help="streams for the all-applies-at-once measurement (each with its own workspace)")
     p.add_argument("--spread", choices=("auto", "on", "off"), default="auto",
                    help="issue a matrix's microbatch calls round robin over the streams (they add into the same "
-                        "S with atomic reductions); auto: when the workload has fewer matrices than streams")
+                        "S with atomic reductions); auto: when the workload has at most half as many matrices as "
+                        "streams")
     p.add_argument("--apply-mode", choices=("group", "single"), default="group",
                    help="group: one logra_rowadam_apply_group call per layer (its matrices in shared launches); "
                         "single: one logra_rowadam_apply_ex call per matrix")
@@ -350,7 +351,9 @@ def run_ours(args):
         b.record(st)
         ev[kind].append((a, b) + tag)
 
-    spread = (len(mats) < len(streams)) if args.spread == "auto" else (args.spread == "on")
+    # auto: only when at least half of the streams would otherwise sit idle (one or two matrices);
+    # spreading costs an event round trip per call, which a host-bound step of many matrices feels
+    spread = (2 * len(mats) <= len(streams)) if args.spread == "auto" else (args.spread == "on")
 
     def one_step(step_idx, ev=None, sts=None):
         sts = sts or streams

@@ -71,6 +71,8 @@ struct SketchShape {
   // accumulate on CTA pairs (r_pad 256 or 512): rank blocks of 256 and d blocks
   // of 256 per pair tile (prb * pdb = 2), pair tiles along d, pairs (clusters)
   int pair, prb, pdb, pdtiles, pairs;
+  int direct;                  // every projection segment covers the whole k range: the projection
+                               // writes the accumulate's hi/lo image itself and the split is skipped
 };
 
 struct Shared {
@@ -228,7 +230,7 @@ __device__ __forceinline__ void gen_sigma_kmajor(uint8_t* tile, const uint2* nib
 // between them, so the drain of one overlaps the MMAs of the next.
 __global__ void __launch_bounds__(512, 1)
     project_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_p,
-                      SketchShape sh_, uint64_t key, Control* ctl) {
+                      SketchShape sh_, uint64_t key, uint8_t* __restrict__ image, Control* ctl) {
   extern __shared__ uint8_t smem_raw[];
   const SketchShape& P = sh_;
   uint8_t* base = align1024(smem_raw);
@@ -359,6 +361,58 @@ __global__ void __launch_bounds__(512, 1)
       const bool whole = (c0 == 0 && c1 == P.nchunks);
       if (!warp_wait(sh, &sh->tmem_full[ab], uphase, limit, ctl)) break;
       tc_fence_after();
+      if (P.direct) {
+        // Whole k range: P^T is final here, so write the accumulate's image directly.
+        // This warp's 32 tokens are one 32-token image chunk; per 32-rank block a
+        // 4 KB tile of 32 rows (hi bf16 of the 32 tokens at bytes 0..63, lo at
+        // 64..127, 16-byte chunk q at q ^ (row & 7)) goes out by one bulk copy.
+        // Rows from r up to r_pad are zero.  Lanes pair up: the even lane stores
+        // the hi word of tokens (t, t + 1), the odd lane the lo word.
+        const int nchunk32 = P.n_pad / kChunk;
+        const int t2 = lane & ~1;
+        const bool odd = lane & 1;
+        for (int t = 0; t < T; ++t) {
+          const uint32_t acc = tmem + uint32_t(ab * T + t) * acc_cols + (uint32_t(quad * 32) << 16);
+          const int ci = ((grp * T + t) * kTok + quad * 32) / kChunk;
+          if (ci < nchunk32) {
+            for (int j0 = 0; j0 < P.r_pad; j0 += 32) {
+              uint32_t v[32];
+              if (j0 < P.r) {
+                tmem_ld32(acc + uint32_t(j0), v);
+                tmem_ld_wait();
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0u;
+              }
+              uint8_t* tile = reinterpret_cast<uint8_t*>(stg + sb * (32 * 32));
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj) {
+                const float p = __uint_as_float(v[jj]);
+                const __nv_bfloat16 h = __float2bfloat16_rn(p);
+                const __nv_bfloat16 l = __float2bfloat16_rn(p - __bfloat162float(h));
+                const uint32_t hu = __bfloat16_as_ushort(h), lu = __bfloat16_as_ushort(l);
+                const uint32_t other = __shfl_xor_sync(0xffffffffu, odd ? hu : lu, 1);
+                const uint32_t word = odd ? (other | (lu << 16)) : (hu | (other << 16));
+                const int q = (odd ? 4 : 0) + (t2 >> 3);
+                *reinterpret_cast<uint32_t*>(tile + jj * 128 + ((q ^ (jj & 7)) << 4) + ((t2 & 7) << 1)) = word;
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                bulk_store(image + (size_t(ci) * P.r_pad + j0) * 128, tile, 32 * 32 * 4);
+                bulk_commit();
+                bulk_wait_read_1();      // the other staging tile is free again
+              }
+              __syncwarp();
+              sb ^= 1;
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh->tmem_empty[ab * T + t]);
+        }
+        continue;
+      }
       for (int t = 0; t < T; ++t) {
         const uint32_t acc = tmem + uint32_t(ab * T + t) * acc_cols;
         const int x0 = (grp * T + t) * kTok + quad * 32;   // first token of this warp's lanes
@@ -928,6 +982,7 @@ static SketchShape plan(int64_t n, int64_t d, int64_t k, int r, int sms) {
     P.proj_ctas = stream_k_ctas(ptotal, sms, 8);
   }
   P.proj_partial = has_partial_segment(ptotal, P.nchunks, P.proj_ctas) ? 1 : 0;
+  P.direct = P.proj_partial ? 0 : 1;
   P.ntile_n = (P.r_pad <= 256) ? 256 : 128;
   P.dtiles = ceil_div(d, P.ntile_n);
   const int tchunks = P.n_pad / kChunk;
@@ -1012,21 +1067,28 @@ int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_
   // again only once all three have been issued.
   const bool tracked = zt && !zt->captured.load();
   const bool trusted = tracked && zt->trusted() >= part;
+  // With every segment covering the whole k range the projection writes the
+  // image itself: the fp32 P^T region is left untouched, so what is known to be
+  // zero there stays known (up to where the image begins), and no split runs.
+  const size_t img_off = (part + 1023) & ~size_t(1023);
+  const size_t keep = (P.direct && tracked) ? zt->trusted() : 0;
   if (zt) zt->bytes.store(0);
   if (P.proj_partial && !trusted) LOGRA_CUDA_TRY(cudaMemsetAsync(ppart, 0, part, s));
   LOGRA_CUDA_TRY(launch_overlapped(project_tc_kernel, dim3(P.proj_ctas), dim3(512), size_t(proj_smem), s, tx, tp, P,
-                                   key, ctl));
+                                   key, image, ctl));
   LOGRA_LAUNCHED();
 
-  const int64_t stotal = int64_t(P.n_pad / kChunk) * P.r_pad * 4;
-  int sblocks = int((stotal + 255) / 256);
-  if (sblocks > sms * 8) sblocks = sms * 8;
-  LOGRA_CUDA_TRY(launch_overlapped(split_kernel, dim3(sblocks), dim3(256), size_t(0), s,
-                                   static_cast<const float*>(ppart), P, image));
-  LOGRA_LAUNCHED();
+  if (!P.direct) {
+    const int64_t stotal = int64_t(P.n_pad / kChunk) * P.r_pad * 4;
+    int sblocks = int((stotal + 255) / 256);
+    if (sblocks > sms * 8) sblocks = sms * 8;
+    LOGRA_CUDA_TRY(launch_overlapped(split_kernel, dim3(sblocks), dim3(256), size_t(0), s,
+                                     static_cast<const float*>(ppart), P, image));
+    LOGRA_LAUNCHED();
+  }
 
   const int acc_smem = acc_smem_bytes(P);
-  float4* pzero = tracked ? reinterpret_cast<float4*>(ppart) : nullptr;
+  float4* pzero = (tracked && !P.direct) ? reinterpret_cast<float4*>(ppart) : nullptr;
   if (P.pair) {
     // the P^T image as a 2-D bf16 tensor of 128-byte rows (r_pad rows per 32-token chunk),
     // already swizzled in memory, loaded in boxes of 128 rows
@@ -1045,7 +1107,7 @@ int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_
   }
   LOGRA_LAUNCHED();
   // known zero now: this call's P^T region, and nothing past it (the image follows it)
-  if (tracked) zt->bytes.store(part);
+  if (tracked) zt->bytes.store(P.direct ? (keep < img_off ? keep : img_off) : part);
   return LOGRA_OK;
 }
 

@@ -78,6 +78,55 @@ def test_sketch_generator_bit_exact(L, r, k, per):
     assert L.logra_get_status() == 0
 
 
+@pytest.mark.parametrize("r,k", [(96, 1000), (256, 1032), (512, 520)])
+def test_sketch_direct_image_bit_exact(L, r, k):
+    """With calls on several streams (concurrency hint) and at least one 256-token group per stream
+    share of the SMs, every projection CTA covers a whole k range and writes the accumulate's hi/lo
+    image itself (no fp32 P^T, no split launch).  6000 tokens: token t takes column t mod k."""
+    import torch
+    seed, step = 0xD1EC7 + r, 2
+    A = O.projection_matrix_fp32(seed, step, r, k)
+    n = 6000
+    J = np.arange(n) % k
+    d = n + 8
+    X = _one_hot_rows(n, k, J, torch.bfloat16).cuda()
+    dY = _one_hot_rows(n, d, np.arange(n), torch.bfloat16).cuda()
+    L.logra_set_concurrency(8)
+    try:
+        S = Guarded((d, r), torch.float32, fill=0.0)
+        L.logra_sketch_accumulate(X, dY, S.t, seed, step)
+        S.check("S")
+    finally:
+        L.logra_set_concurrency(1)
+    got = S.t.cpu().numpy()
+    want = np.ascontiguousarray(A[:, J].T)
+    assert np.array_equal(got[:n].view(np.uint32), want.view(np.uint32))
+    assert not np.any(got[n:])
+    assert L.logra_get_status() == 0
+
+
+@pytest.mark.parametrize("n,d,k,r", [(8192, 1032, 1544, 256), (5000, 264, 3080, 160), (6144, 2056, 520, 512)])
+def test_sketch_direct_image_matches_oracle(L, n, d, k, r):
+    """The direct-image projection on realistic inputs, two microbatches, against the oracle (1e-3)."""
+    import torch
+    from rank_gradient_sketching_02_gb300 import synth
+    L.logra_set_concurrency(8)
+    try:
+        S = Guarded((d, r), torch.float32, fill=0.0)
+        S_or = np.zeros((d, r))
+        for mb in range(2):
+            X, dY, _ = synth.host_microbatch(n, d, k, dy_kind="lognormal", mask_frac=0.25, key=(71, n, mb))
+            Xb, dYb = synth.to_bf16_bits(X), synth.to_bf16_bits(dY)
+            L.logra_sketch_accumulate(Xb.cuda(), dYb.cuda(), S.t, 9, 4)
+            S_or = O.sketch_accumulate(S_or, Xb.double().numpy(), dYb.double().numpy(), 9, 4, r)
+        S.check("S")
+    finally:
+        L.logra_set_concurrency(1)
+    got = S.t.double().cpu().numpy()
+    assert np.linalg.norm(got - S_or) / np.linalg.norm(S_or) <= 1e-3
+    assert L.logra_get_status() == 0
+
+
 @pytest.mark.parametrize("r,k", [(32, 200), (96, 1000), (256, 4104), (384, 776), (512, 2056), (128, 18952)])
 def test_reconstruct_generator_bit_exact(L, r, k):
     import torch
