@@ -223,6 +223,26 @@ def time_oracle(w, r, seconds, host_seed=0):
                        f"FLOPs / ({w.microbatches} sketches + 1 apply)")}
 
 
+def time_oracle_one_thread(workload, r, seconds):
+    """The same bounded oracle sample in a child process whose BLAS and OpenMP pools have one thread."""
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
+                "NUMEXPR_NUM_THREADS", "VECLIB_MAXIMUM_THREADS"):
+        env[var] = "1"
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; from rank_gradient_sketching_02_gb300 import "
+            "synth; print(json.dumps(bench.time_oracle(synth.WORKLOADS[%r], %d, %f)))" % (ROOT, workload, r, seconds))
+    try:
+        p = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, cwd=ROOT,
+                           timeout=max(60.0, 10 * seconds))
+        if p.returncode != 0:
+            return None
+        res = json.loads(p.stdout.strip().splitlines()[-1])
+        res["cores"] = 1
+        return res
+    except Exception:  # noqa: BLE001 - a missing one-thread figure does not fail the bench
+        return None
+
+
 def run_reference(args):
     """Reference arm: the fp64 CPU oracle, as it stands, on the machine's host cores."""
     rank = int(os.environ.get("RANK", "0"))
@@ -620,6 +640,10 @@ def run_ours(args):
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = time_oracle(w, r, args.cpu_seconds)
+        one = time_oracle_one_thread(w.name, r, max(2.0, args.cpu_seconds / 3))
+        if one is not None:
+            line["cpu_baseline"]["one_thread"] = {"value": one["value"], "unit": one["unit"], "cores": 1,
+                                                  "sample": one["sample"]}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
