@@ -130,6 +130,44 @@ int logra_sketch_accumulate(const void* X, const void* dY, int in_dtype,
                             logra_stream_t stream);
 
 /*
+ * logra_sketch_item -- one sketch of logra_sketch_accumulate_group: the
+ * arguments of logra_sketch_accumulate that differ between sketches (device
+ * pointers as there; bf16 X and dY).
+ */
+typedef struct logra_sketch_item {
+  const void* X;            /* n x k bf16 activations of one microbatch        */
+  const void* dY;           /* n x d bf16 output gradients of that microbatch  */
+  float* S;                 /* d x r fp32 sketch, accumulated in place         */
+  int64_t d, k;
+  uint64_t seed;            /* this matrix's seed                               */
+} logra_sketch_item;
+
+/*
+ * logra_sketch_accumulate_group -- logra_sketch_accumulate (bf16) for `count`
+ * sketches of one token count n, one rank r and one step, issued from a
+ * single caller stream: S += dY^T (X A^T) for every item.  (theclarity.today
+ * write-up, "Why it matters": the sketches of a backward pass are
+ * independent per weight matrix.)
+ *   items   HOST array of `count` items, read during the call only.  Items may
+ *           share an S (microbatches of one matrix): S is updated with atomic
+ *           additions, so their sum is formed in an unspecified order.
+ * The library forks the sketches round robin onto up to 8 side streams of its
+ * own (created on the device's first group call and kept), shapes their
+ * launches as for logra_set_concurrency(number of side streams used), and
+ * joins the side streams back into `stream` before returning: work issued on
+ * `stream` afterwards runs after every sketch of the group.  One matrix's
+ * small calls then overlap another's, which a single stream cannot do.
+ * Each side stream has its own workspace (allocated on first use; make one
+ * group call of the largest shapes before capturing groups into a CUDA graph,
+ * which records the fork and join like any other).  Every item is checked
+ * before anything is launched; a failing launch still joins what was issued.
+ * count == 0 or n == 0 is a no-op.
+ */
+int logra_sketch_accumulate_group(const logra_sketch_item* items, int count,
+                                  int64_t n, int r, uint64_t step,
+                                  logra_stream_t stream);
+
+/*
  * logra_rowadam_apply -- RowAdam update rebuilt from the sketch:
  *   Ghat = S A;  v_i <- beta2 v_i + (1-beta2) * mean_j Ghat_ij^2;
  *   W_ij <- W_ij - lr * c * Ghat_ij / sqrt(v_i + eps).

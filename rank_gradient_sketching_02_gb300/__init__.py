@@ -9,4 +9,5 @@ from .binding import (  # noqa: F401
     logra_apply_group_workspace_bytes, logra_apply_item, logra_reconstruct, logra_reserve_workspace,
     logra_rowadam_apply, logra_rowadam_apply_bc, logra_rowadam_apply_ex, logra_rowadam_apply_group,
     logra_rowadam_predict, logra_rowadam_predict_bc, logra_set_concurrency, logra_sign_matrix, logra_sketch_accumulate,
+    logra_sketch_accumulate_group, logra_sketch_item,
 )

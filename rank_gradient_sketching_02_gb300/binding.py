@@ -52,7 +52,13 @@ class logra_apply_item(C.Structure):
                 ("t", _I64)]
 
 
+class logra_sketch_item(C.Structure):
+    """One sketch of logra_sketch_accumulate_group (the C struct of the same name)."""
+    _fields_ = [("X", _VP), ("dY", _VP), ("S", _VP), ("d", _I64), ("k", _I64), ("seed", _U64)]
+
+
 SIGNATURES["logra_rowadam_apply_group"] = (_I, [C.POINTER(logra_apply_item), _I, _I, _U64, _F, _F, _VP])
+SIGNATURES["logra_sketch_accumulate_group"] = (_I, [C.POINTER(logra_sketch_item), _I, _I64, _I, _U64, _VP])
 SIGNATURES["logra_apply_group_workspace_bytes"] = (_SZ, [C.POINTER(logra_apply_item), _I, _I])
 
 _lib = None
@@ -137,6 +143,29 @@ def logra_sketch_accumulate(X, dY, S, seed: int, step: int, stream=None):
     _check(lib().logra_sketch_accumulate(px, py, _in_dtype(X), n, d, k, r, seed, step, ps, _stream(stream)),
            "logra_sketch_accumulate")
     return S
+
+
+def logra_sketch_accumulate_group(items, step: int, stream=None):
+    """logra_sketch_accumulate for several bf16 sketches of one n and r from one caller stream.
+
+    items: sequence of dicts with X (n x k), dY (n x d) bf16 CUDA tensors, S (d x r fp32) and seed;
+    the library spreads them over its own side streams and joins them back into the stream."""
+    import torch
+    items = list(items)
+    arr = (logra_sketch_item * max(1, len(items)))()
+    n = r = None
+    for i, m in enumerate(items):
+        X, dY, S = m["X"], m["dY"], m["S"]
+        if n is None:
+            n, r = X.shape[0], S.shape[1]
+        elif X.shape[0] != n or S.shape[1] != r:
+            raise ValueError("every sketch of a group has the same token count n and rank r")
+        k, d = X.shape[1], S.shape[0]
+        bf = (torch.bfloat16,)
+        arr[i] = logra_sketch_item(_dev(X, "X", bf), _dev(dY, "dY", bf, (n, d)), _dev(S, "S", (torch.float32,)),
+                                   d, k, int(m["seed"]))
+    _check(lib().logra_sketch_accumulate_group(arr, len(items), n or 0, r or 32, step, _stream(stream)),
+           "logra_sketch_accumulate_group")
 
 
 def logra_rowadam_apply(W, S, v, seed: int, step: int, beta2: float, eps: float, lr: float, c: float,

@@ -24,7 +24,14 @@ static __device__ Control g_control = {0, 0, 2000000000ull};
 static thread_local int t_last_cuda_error = 0;
 static std::atomic<int> g_concurrency{1};
 
-int concurrency() { return g_concurrency.load(std::memory_order_relaxed); }
+// A grouped sketch call shapes its launches for the side streams it uses,
+// whatever the process-wide hint says; the override lives for the calling
+// thread's issue loop only.
+static thread_local int t_hint_override = 0;
+
+int concurrency() {
+  return t_hint_override > 0 ? t_hint_override : g_concurrency.load(std::memory_order_relaxed);
+}
 static std::atomic<unsigned long long> g_launches{0};
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
@@ -275,6 +282,18 @@ int logra_reserve_workspace(size_t bytes, logra_stream_t stream) {
   return st;
 }
 
+// The bf16 sketch of one microbatch on `stream` (arguments already checked).
+static int sketch_bf16_on(const void* X, const void* dY, int64_t n, int64_t d, int64_t k, int r, uint64_t seed,
+                          uint64_t step, float* S, cudaStream_t stream) {
+  int st;
+  ZeroTrack* zero = nullptr;
+  void* ws = workspace(stream, logra_sketch_workspace_bytes(n, d, k, r, LOGRA_BF16), &st, &zero);
+  if (st) return st;
+  Control* ctl = control_block(&st);
+  if (!ctl) return st;
+  return launch_sketch_tc(X, dY, n, d, k, r, step_key(seed, step), inv_sqrt_r(r), S, ws, zero, ctl, stream);
+}
+
 int logra_sketch_accumulate(const void* X, const void* dY, int in_dtype, int64_t n, int64_t d, int64_t k, int r,
                             uint64_t seed, uint64_t step, float* S, logra_stream_t stream) {
   if (!S || n < 0) return LOGRA_ERR_INVALID_ARG;
@@ -296,6 +315,71 @@ int logra_sketch_accumulate(const void* X, const void* dY, int in_dtype, int64_t
   zero->bytes.store(0);           // the fp32 path keeps its P in the workspace
   return launch_sketch_simt(X, dY, in_dtype, n, d, k, r, step_key(seed, step), inv_sqrt_r(r), S,
                             static_cast<float*>(ws), stream);
+}
+
+// Side streams of the grouped sketch, per device: created on first use and kept.
+namespace {
+constexpr int kSideStreams = 8;
+struct SideStreams {
+  cudaStream_t s[kSideStreams] = {};
+  cudaEvent_t fork = nullptr;
+  cudaEvent_t join[kSideStreams] = {};
+  bool ready = false;
+};
+std::mutex g_side_mu;                 // also serialises the fork/issue/join sequence of a device
+SideStreams g_side[kMaxDevices];
+
+int side_streams(SideStreams** out) {
+  int dev;
+  if (int st = current_device(&dev)) return st;
+  SideStreams& sd = g_side[dev];
+  if (!sd.ready) {
+    cudaError_t e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming);
+    for (int i = 0; e == cudaSuccess && i < kSideStreams; ++i) {
+      e = cudaStreamCreateWithFlags(&sd.s[i], cudaStreamNonBlocking);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sd.join[i], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    sd.ready = true;
+  }
+  *out = &sd;
+  return LOGRA_OK;
+}
+}  // namespace
+
+int logra_sketch_accumulate_group(const logra_sketch_item* items, int count, int64_t n, int r, uint64_t step,
+                                  logra_stream_t stream) {
+  if (count < 0 || (count > 0 && !items) || n < 0) return LOGRA_ERR_INVALID_ARG;
+  if (check_rank(r)) return LOGRA_ERR_UNSUPPORTED;
+  for (int i = 0; i < count; ++i) {
+    const logra_sketch_item& it = items[i];
+    if (!it.S) return LOGRA_ERR_INVALID_ARG;
+    if (int st = check_mat(it.d, it.k)) return st;
+    if (n > 0 && (!it.X || !it.dY)) return LOGRA_ERR_INVALID_ARG;
+    if (!aligned16(it.X) || !aligned16(it.dY) || !aligned16(it.S)) return LOGRA_ERR_UNSUPPORTED;
+  }
+  if (count == 0 || n == 0) return LOGRA_OK;
+  std::lock_guard<std::mutex> lk(g_side_mu);
+  SideStreams* sd = nullptr;
+  if (int st = side_streams(&sd)) return st;
+  const int ns = count < kSideStreams ? count : kSideStreams;
+  LOGRA_CUDA_TRY(cudaEventRecord(sd->fork, stream));
+  for (int j = 0; j < ns; ++j) LOGRA_CUDA_TRY(cudaStreamWaitEvent(sd->s[j], sd->fork, 0));
+  int first_error = LOGRA_OK;
+  t_hint_override = ns;
+  for (int i = 0; i < count && first_error == LOGRA_OK; ++i) {
+    const logra_sketch_item& it = items[i];
+    first_error = sketch_bf16_on(it.X, it.dY, n, it.d, it.k, r, it.seed, step, it.S, sd->s[i % ns]);
+  }
+  t_hint_override = 0;
+  // join every side stream back, also after an error, so that the caller's
+  // later work stays ordered after whatever was launched
+  for (int j = 0; j < ns; ++j) {
+    cudaError_t e = cudaEventRecord(sd->join[j], sd->s[j]);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, sd->join[j], 0);
+    if (e != cudaSuccess && first_error == LOGRA_OK) first_error = cuda_fail(e);
+  }
+  return first_error;
 }
 
 // 1 / (1 - beta2^t): the factor of Adam's bias correction for the t-th

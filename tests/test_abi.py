@@ -122,3 +122,27 @@ def test_concurrency_hint_is_validated(lib):
     assert lib.logra_set_concurrency(65) == LOGRA_ERR_INVALID_ARG
     assert lib.logra_set_concurrency(4) == 0
     assert lib.logra_set_concurrency(1) == 0
+
+
+def test_sketch_group_bad_arguments_rejected_before_any_cuda_call(lib):
+    from rank_gradient_sketching_02_gb300.binding import LOGRA_ERR_INVALID_ARG, LOGRA_ERR_UNSUPPORTED
+    from rank_gradient_sketching_02_gb300 import binding
+
+    def items(shapes, X=4096, dY=8192, S=16384):
+        arr = (binding.logra_sketch_item * len(shapes))()
+        for i, (d, k) in enumerate(shapes):
+            arr[i] = binding.logra_sketch_item(X, dY, S, d, k, 7)
+        return arr
+
+    ok = [(64, 64), (128, 72)]
+    assert lib.logra_sketch_accumulate_group(items(ok), 0, 128, 256, 0, None) == 0           # no-op
+    assert lib.logra_sketch_accumulate_group(items(ok), 2, 0, 256, 0, None) == 0             # n == 0
+    assert lib.logra_sketch_accumulate_group(None, 2, 128, 256, 0, None) == LOGRA_ERR_INVALID_ARG
+    assert lib.logra_sketch_accumulate_group(items(ok), -1, 128, 256, 0, None) == LOGRA_ERR_INVALID_ARG
+    assert lib.logra_sketch_accumulate_group(items(ok), 2, -5, 256, 0, None) == LOGRA_ERR_INVALID_ARG
+    assert lib.logra_sketch_accumulate_group(items(ok), 2, 128, 40, 0, None) == LOGRA_ERR_UNSUPPORTED
+    assert lib.logra_sketch_accumulate_group(items([(64, 64), (12, 64)]), 2, 128, 256, 0, None) == \
+        LOGRA_ERR_UNSUPPORTED
+    assert lib.logra_sketch_accumulate_group(items(ok, S=0), 2, 128, 256, 0, None) == LOGRA_ERR_INVALID_ARG
+    assert lib.logra_sketch_accumulate_group(items(ok, X=0), 2, 128, 256, 0, None) == LOGRA_ERR_INVALID_ARG
+    assert lib.logra_sketch_accumulate_group(items(ok, dY=8200), 2, 128, 256, 0, None) == LOGRA_ERR_UNSUPPORTED
