@@ -220,6 +220,62 @@ __device__ __forceinline__ void gen_sigma_kmajor(uint8_t* tile, const uint2* nib
   }
 }
 
+// Direct image drain of one segment's accumulators (whole k range): this
+// warp's 32 tokens of token tile t are one 32-token image chunk; per 32-rank
+// block a 4 KB tile of 32 rows (hi bf16 of the 32 tokens at bytes 0..63, lo at
+// 64..127, 16-byte chunk q at q ^ (row & 7)) goes out by one bulk copy.  Rows
+// from r up to r_pad are zero.  Lanes pair up: the even lane stores the hi
+// word of tokens (t, t + 1), the odd lane the lo word.  Only the blocks
+// b = t * (r_pad / 32) + j0 / 32 with b % nslots == slot are drained, so that
+// several warps of one TMEM lane quadrant can share the work.  `stg` holds two
+// 4 KB staging tiles; `sb` alternates between them.
+__device__ __forceinline__ void drain_image_blocks(uint32_t acc_tile0, uint32_t acc_cols, int T, int quad, int grp,
+                                                   const SketchShape& P, uint8_t* __restrict__ image, uint8_t* stg,
+                                                   int& sb, int slot, int nslots, int lane) {
+  const int nchunk32 = P.n_pad / kChunk;
+  const int t2 = lane & ~1;
+  const bool odd = lane & 1;
+  const int nb = P.r_pad / 32;
+  for (int t = 0; t < T; ++t) {
+    const uint32_t acc = acc_tile0 + uint32_t(t) * acc_cols + (uint32_t(quad * 32) << 16);
+    const int ci = ((grp * T + t) * kTok + quad * 32) / kChunk;
+    if (ci >= nchunk32) continue;
+    for (int jb = 0; jb < nb; ++jb) {
+      if ((t * nb + jb) % nslots != slot) continue;
+      const int j0 = jb * 32;
+      uint32_t v[32];
+      if (j0 < P.r) {
+        tmem_ld32(acc + uint32_t(j0), v);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0u;
+      }
+      uint8_t* tile = stg + sb * kStageTile;
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) {
+        const float p = __uint_as_float(v[jj]);
+        const __nv_bfloat16 h = __float2bfloat16_rn(p);
+        const __nv_bfloat16 l = __float2bfloat16_rn(p - __bfloat162float(h));
+        const uint32_t hu = __bfloat16_as_ushort(h), lu = __bfloat16_as_ushort(l);
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, odd ? hu : lu, 1);
+        const uint32_t word = odd ? (other | (lu << 16)) : (hu | (other << 16));
+        const int q = (odd ? 4 : 0) + (t2 >> 3);
+        *reinterpret_cast<uint32_t*>(tile + jj * 128 + ((q ^ (jj & 7)) << 4) + ((t2 & 7) << 1)) = word;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        bulk_store(image + (size_t(ci) * P.r_pad + j0) * 128, tile, kStageTile);
+        bulk_commit();
+        bulk_wait_read_1();      // the other staging tile is free again
+      }
+      __syncwarp();
+      sb ^= 1;
+    }
+  }
+}
+
 // A segment is (group of `tgroup` 128-token tiles, k-chunk range): each
 // generated sign tile feeds the MMAs of every token tile of the group, so the
 // generation cost per MMA falls with the group size.  The epilogue stages
@@ -251,6 +307,10 @@ __global__ void __launch_bounds__(512, 1)
   uint32_t tmem_cols = 32;
   while (tmem_cols < acc_cols * uint32_t(T * nacc)) tmem_cols <<= 1;
   const int64_t total = int64_t(P.groups) * P.nchunks;
+  // The image drain of a CTA's only segment is shared by 12 warps (3 per TMEM
+  // lane quadrant: the epilogue warp and two of warps 6..13, free by then) when
+  // the X ring, idle after the last MMA, can hold their 8 KB of staging each.
+  const bool extra_drain = P.direct && uint32_t(XS) * x_bytes >= 8u * 2u * kStageTile;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < XS; ++s) {
@@ -362,55 +422,24 @@ __global__ void __launch_bounds__(512, 1)
       if (!warp_wait(sh, &sh->tmem_full[ab], uphase, limit, ctl)) break;
       tc_fence_after();
       if (P.direct) {
-        // Whole k range: P^T is final here, so write the accumulate's image directly.
-        // This warp's 32 tokens are one 32-token image chunk; per 32-rank block a
-        // 4 KB tile of 32 rows (hi bf16 of the 32 tokens at bytes 0..63, lo at
-        // 64..127, 16-byte chunk q at q ^ (row & 7)) goes out by one bulk copy.
-        // Rows from r up to r_pad are zero.  Lanes pair up: the even lane stores
-        // the hi word of tokens (t, t + 1), the odd lane the lo word.
-        const int nchunk32 = P.n_pad / kChunk;
-        const int t2 = lane & ~1;
-        const bool odd = lane & 1;
-        for (int t = 0; t < T; ++t) {
-          const uint32_t acc = tmem + uint32_t(ab * T + t) * acc_cols + (uint32_t(quad * 32) << 16);
-          const int ci = ((grp * T + t) * kTok + quad * 32) / kChunk;
-          if (ci < nchunk32) {
-            for (int j0 = 0; j0 < P.r_pad; j0 += 32) {
-              uint32_t v[32];
-              if (j0 < P.r) {
-                tmem_ld32(acc + uint32_t(j0), v);
-                tmem_ld_wait();
-              } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = 0u;
-              }
-              uint8_t* tile = reinterpret_cast<uint8_t*>(stg + sb * (32 * 32));
-#pragma unroll
-              for (int jj = 0; jj < 32; ++jj) {
-                const float p = __uint_as_float(v[jj]);
-                const __nv_bfloat16 h = __float2bfloat16_rn(p);
-                const __nv_bfloat16 l = __float2bfloat16_rn(p - __bfloat162float(h));
-                const uint32_t hu = __bfloat16_as_ushort(h), lu = __bfloat16_as_ushort(l);
-                const uint32_t other = __shfl_xor_sync(0xffffffffu, odd ? hu : lu, 1);
-                const uint32_t word = odd ? (other | (lu << 16)) : (hu | (other << 16));
-                const int q = (odd ? 4 : 0) + (t2 >> 3);
-                *reinterpret_cast<uint32_t*>(tile + jj * 128 + ((q ^ (jj & 7)) << 4) + ((t2 & 7) << 1)) = word;
-              }
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (lane == 0) {
-                bulk_store(image + (size_t(ci) * P.r_pad + j0) * 128, tile, 32 * 32 * 4);
-                bulk_commit();
-                bulk_wait_read_1();      // the other staging tile is free again
-              }
-              __syncwarp();
-              sb ^= 1;
-            }
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh->tmem_empty[ab * T + t]);
-        }
+        // Whole k range: P^T is final here, so the accumulate's image is written directly.
+        // When this is the CTA's only segment, the idle generator warps share the drain
+        // (extra_drain).  Only then: they wait on tmem_full with the parity of the segment
+        // they drain, which identifies the phase only while no earlier phase is pending.
+        SegIter peek = it;
+        int g2, d0, d1;
+        const bool only = seg == 0 && !peek.next(g2, d0, d1);
+        uint8_t* stg8 = reinterpret_cast<uint8_t*>(stg);
+        if (only && extra_drain)
+          drain_image_blocks(tmem + uint32_t(ab * T) * acc_cols, acc_cols, T, quad, grp, P, image, stg8, sb, 0, 3,
+                             lane);
+        else
+          drain_image_blocks(tmem + uint32_t(ab * T) * acc_cols, acc_cols, T, quad, grp, P, image, stg8, sb, 0, 1,
+                             lane);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0)
+          for (int t = 0; t < T; ++t) mbar_arrive(&sh->tmem_empty[ab * T + t]);
         continue;
       }
       for (int t = 0; t < T; ++t) {
@@ -444,24 +473,49 @@ __global__ void __launch_bounds__(512, 1)
     }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
-  } else if (warp != 9 && warp != 13) {
-    // ---------------------------------------------------------------- sign-tile generators (8 warps)
-    // Warps 9 and 13 stay idle so that no generator shares the MMA warp's
-    // scheduler (warp % 4 == 1): the single issuing thread keeps its issue slots.
-    const int gtid = (warp - 6 - (warp > 9) - (warp > 13)) * 32 + lane;
-    Ring gr;
-    SegIter it(total, P.nchunks);
-    while (it.next(grp, c0, c1)) {
-      for (int c = c0; c < c1; ++c) {
-        if (!warp_wait(sh, &sh->o_empty[gr.stage], gr.phase ^ 1u, limit, ctl)) goto gen_done;
-        gen_sigma_kmajor(g_tiles + size_t(gr.stage) * g_bytes, sh->nib, key, P.r, c, gtid, 256);
-        fence_proxy_async_smem();
+  } else {
+    if (warp != 9 && warp != 13) {
+      // -------------------------------------------------------------- sign-tile generators (8 warps)
+      // Warps 9 and 13 stay idle so that no generator shares the MMA warp's
+      // scheduler (warp % 4 == 1): the single issuing thread keeps its issue slots.
+      const int gtid = (warp - 6 - (warp > 9) - (warp > 13)) * 32 + lane;
+      Ring gr;
+      SegIter it(total, P.nchunks);
+      while (it.next(grp, c0, c1)) {
+        for (int c = c0; c < c1; ++c) {
+          if (!warp_wait(sh, &sh->o_empty[gr.stage], gr.phase ^ 1u, limit, ctl)) goto gen_done;
+          gen_sigma_kmajor(g_tiles + size_t(gr.stage) * g_bytes, sh->nib, key, P.r, c, gtid, 256);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh->o_full[gr.stage]);
+          gr.next(GS);
+        }
+      }
+    gen_done:;
+    }
+    if (extra_drain && warp < 14 && !*reinterpret_cast<volatile int*>(&sh->abort)) {
+      // -------------------------------------------------------------- share the final segment's image drain
+      SegIter it(total, P.nchunks);
+      int nseg = 0, fg = 0;
+      while (it.next(grp, c0, c1)) {
+        ++nseg;
+        fg = grp;
+      }
+      if (nseg == 1) {              // the CTA's only segment: accumulator set 0, first phase
+        const int ab = 0;
+        const uint32_t uphase = 0u;
+        if (warp_wait(sh, &sh->tmem_full[ab], uphase, limit, ctl)) {
+          tc_fence_after();
+          uint8_t* stg8 = x_tiles + size_t(warp - 6) * 2 * kStageTile;
+          int sb = 0;
+          drain_image_blocks(tmem + uint32_t(ab * T) * acc_cols, acc_cols, T, warp & 3, fg, P, image, stg8, sb,
+                             warp < 10 ? 1 : 2, 3, lane);
+          tc_fence_before();
+        }
+        if (lane == 0) bulk_wait_all();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->o_full[gr.stage]);
-        gr.next(GS);
       }
     }
-  gen_done:;
   }
 
   tc_fence_before();
