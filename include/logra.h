@@ -108,7 +108,9 @@ int logra_sign_matrix(uint64_t seed, uint64_t step, int r, int64_t k,
  * Padding tokens are zero rows of X and dY.  bf16 inputs are multiplied
  * exactly and accumulated in fp32; the X A^T intermediate is kept as a
  * two-term bf16 expansion (relative error about 2^-16), fp32 inputs run in fp32.
- * Uses the internal workspace (r * n * 4 bytes for bf16 inputs).
+ * Uses the internal workspace: for bf16 inputs about 8 * r * n bytes (an fp32
+ * P^T buffer and the two-term bf16 image the accumulate reads;
+ * logra_sketch_workspace_bytes gives the exact figure), r * n * 4 for fp32.
  * S is updated with atomic fp32 additions, so calls that add into the same S
  * (different microbatches of one step) may run concurrently on different
  * streams; the sum is then formed in an unspecified order.
@@ -180,7 +182,9 @@ int logra_sketch_accumulate_group(const logra_sketch_item* items, int count,
  *   norms_out  device, 2 doubles, overwritten: {||S||_F^2, ||dW||_F^2} where
  *              dW is the fp32 update added to W -- the controller's inputs.
  *              May be NULL.
- * Uses the internal workspace (d * 4 + small bytes).
+ * Uses the internal workspace: the Gram image of A (r x r, two bf16 terms),
+ * the two-term bf16 image of S (d x r x 4 bytes) and d x 4 bytes of row
+ * factors plus small partials (logra_apply_workspace_bytes gives the figure).
  */
 int logra_rowadam_apply(float* W, const float* S, float* v, int64_t d,
                         int64_t k, int r, uint64_t seed, uint64_t step,
