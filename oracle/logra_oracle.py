@@ -56,7 +56,7 @@ __all__ = [
     "step_key", "sign_words", "sign_matrix", "projection_matrix",
     "projection_matrix_fp32", "sketch_accumulate", "sketch_columns",
     "reconstruct", "rowadam_apply", "rowadam_rows", "gram_matrix",
-    "sync_sketch", "bias_corrected",
+    "sync_sketch", "bias_corrected", "input_gradient", "linear_backward",
 ]
 
 MASK64 = (1 << 64) - 1
@@ -142,6 +142,23 @@ def sketch_accumulate(S: np.ndarray, X: np.ndarray, dY: np.ndarray,
     A = projection_matrix(seed, step, r, X.shape[1])
     P = X @ A.T                     # n x r
     return np.asarray(S, dtype=np.float64) + dY.T @ P
+
+
+def input_gradient(dY: np.ndarray, W: np.ndarray) -> np.ndarray:
+    """dX = dY W (n x k): the gradient with respect to the input of a Linear
+    layer Y = X W^T.  The method leaves this half of the backward pass as it
+    is; only the weight gradient dY^T X is replaced by the sketch
+    (theclarity.today write-up, "Why it matters")."""
+    return np.asarray(dY, dtype=np.float64) @ np.asarray(W, dtype=np.float64)
+
+
+def linear_backward(S: np.ndarray, X: np.ndarray, dY: np.ndarray, W: np.ndarray,
+                    seed: int, step: int, r: int):
+    """One microbatch of a Linear layer's backward as the method runs it:
+    returns (dX, S + dY^T (X A^T)), the input gradient and the updated sketch,
+    with no d x k gradient buffer (academy.dair.ai summary, "Gradient
+    sketches")."""
+    return input_gradient(dY, W), sketch_accumulate(S, X, dY, seed, step, r)
 
 
 def sketch_columns(X: np.ndarray, dY: np.ndarray, seed: int, step: int,

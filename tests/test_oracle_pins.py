@@ -151,6 +151,36 @@ def test_sketch_padding_rows_contribute_nothing():
     np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
 
 
+def test_input_gradient_brute_force_loops():
+    n, d, k = 4, 6, 5
+    X, dY = _tiny(n, d, k, seed=11)
+    W = np.random.default_rng(12).standard_normal((d, k))
+    got = O.input_gradient(dY, W)
+    for t in range(n):
+        for j in range(k):
+            acc = 0.0
+            for a in range(d):
+                acc += dY[t, a] * W[a, j]
+            assert abs(got[t, j] - acc) <= 1e-12 * max(1.0, abs(acc))
+
+
+def test_linear_backward_matches_autograd_of_the_layer():
+    """dX is what autograd gives for Y = X W^T, and the sketch is the autograd
+    weight gradient times A^T (S = G A^T with G from the layer itself)."""
+    torch = pytest.importorskip("torch")
+    n, d, k, r = 19, 13, 136, 32
+    X, dY = _tiny(n, d, k, seed=13)
+    W = np.random.default_rng(14).standard_normal((d, k))
+    Xt = torch.tensor(X, dtype=torch.float64, requires_grad=True)
+    Wt = torch.tensor(W, dtype=torch.float64, requires_grad=True)
+    torch.nn.functional.linear(Xt, Wt).backward(torch.tensor(dY, dtype=torch.float64))
+    S0 = np.random.default_rng(15).standard_normal((d, r))
+    dX, S = O.linear_backward(S0, X, dY, W, 6, 2, r)
+    np.testing.assert_allclose(dX, Xt.grad.numpy(), rtol=1e-12, atol=1e-12)
+    A = O.projection_matrix(6, 2, r, k)
+    np.testing.assert_allclose(S - S0, Wt.grad.numpy() @ A.T, rtol=1e-10, atol=1e-10)
+
+
 def test_sketch_columns_match_full():
     n, d, k, r = 21, 11, 200, 32
     X, dY = _tiny(n, d, k, seed=5)
