@@ -577,6 +577,50 @@ def run_ours(args):
         graph_comp = {"ms_per_step": g0.elapsed_time(g1) / args.steps, "launches_per_step": g_launch,
                       "timing": f"{args.steps} replays of one captured step, CUDA events on the main stream"}
         del g
+    # The backward of the largest matrix's Linear layer for one microbatch, as one library call
+    # (dX = dY W on the library's tensor-core kernel, then the sketch) against the separate calls a
+    # caller would otherwise make (dX through torch.matmul, i.e. cuBLAS, then the sketch); one
+    # stream, CUDA events, median of 5 after 3 warm-ups.  Outside the timed step.
+    lb_comp = None
+    if dt == torch.bfloat16 and world == 1:
+        L.logra_set_concurrency(1)
+        mb_big = max(mats, key=lambda m: m["d"] * m["k"] + 0.5 * m["d"])
+        Xb, dYb, Wb = mb_big["X"][0], mb_big["dY"][0], mb_big["Wb"]
+        dXb = torch.empty((n, mb_big["k"]), dtype=torch.bfloat16, device=dev)
+        Sb = torch.zeros_like(mb_big["S"])
+
+        def med(fn):
+            for _ in range(3):
+                fn()
+            out = []
+            for _ in range(5):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                out.append(e0.elapsed_time(e1))
+            return statistics.median(out)
+
+        sd, st_ = mb_big["seed"], args.warmup + args.steps + 40
+        t_fused = med(lambda: L.logra_linear_backward(dYb, W=Wb, dX=dXb, X=Xb, S=Sb, seed=sd, step=st_))
+        t_sep = med(lambda: (torch.matmul(dYb, Wb, out=dXb), L.logra_sketch_accumulate(Xb, dYb, Sb, sd, st_)))
+        t_dx = med(lambda: L.logra_linear_backward(dYb, W=Wb, dX=dXb))
+        t_cublas = med(lambda: torch.matmul(dYb, Wb, out=dXb))
+        t_sk = med(lambda: L.logra_sketch_accumulate(Xb, dYb, Sb, sd, st_))
+        dx_flop = 2.0 * n * mb_big["d"] * mb_big["k"]
+        lb_comp = {"shape": {"n": n, "d": mb_big["d"], "k": mb_big["k"], "r": r},
+                   "fused_ms": t_fused, "separate_ms": t_sep, "fused_over_separate": t_fused / t_sep,
+                   "dx_ms": t_dx, "dx_tflops": dx_flop / (t_dx * 1e-3) / 1e12,
+                   "dx_cublas_ms": t_cublas, "dx_cublas_tflops": dx_flop / (t_cublas * 1e-3) / 1e12,
+                   "sketch_ms": t_sk,
+                   "timing": "fused: one logra_linear_backward call (dX + sketch); separate: torch.matmul "
+                             "(cuBLAS) for dX then logra_sketch_accumulate; one stream, CUDA events, "
+                             "median of 5 after 3 warm-ups"}
+        del dXb, Sb
+        L.logra_set_concurrency(len(streams))
+
     elapsed_ms = t_start.elapsed_time(t_end)
     if world > 1:
         t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
@@ -662,6 +706,7 @@ def run_ours(args):
         "roofline": roof,
         "cuda_graph_step": graph_comp,
         "one_stream_group_step": group_comp,
+        "linear_backward": lb_comp,
         "gpu_launches": launches,
         "clocks": clk,
         "device_status": status,

@@ -170,6 +170,37 @@ int logra_sketch_accumulate_group(const logra_sketch_item* items, int count,
                                   logra_stream_t stream);
 
 /*
+ * logra_linear_backward -- the backward pass of a Linear layer Y = X W^T as
+ * LoGRA runs it, for one microbatch (bf16 operands):
+ *   dX = dY W           the input gradient, handed to the layer below;
+ *   S += dY^T (X A^T)   the sketch, in place of the d x k weight gradient
+ *                       dY^T X, which is never formed (theclarity.today
+ *                       write-up, "Why it matters"; academy.dair.ai summary,
+ *                       "Gradient sketches": no full gradient buffer).
+ *   X   n x k bf16 activations of the microbatch
+ *   dY  n x d bf16 output gradients of the microbatch
+ *   W   d x k bf16 weight, the model's working copy (e.g. the W_bf16_out of
+ *       logra_rowadam_apply_ex); may be NULL when dX is NULL
+ *   dX  n x k bf16, overwritten: every element is the fp32 tensor-core sum
+ *       over d, rounded once to bf16 (nearest even).  NULL: the sketch only.
+ *       Must not overlap X, dY, W or S.
+ *   S   d x r fp32 sketch, accumulated in place by the same kernels (and
+ *       with the same result) as logra_sketch_accumulate.  NULL: dX only
+ *       (X, r, seed and step are then not used).
+ * dX and S must not both be NULL (LOGRA_ERR_INVALID_ARG); n must be below
+ * 2^31 (LOGRA_ERR_UNSUPPORTED).  Launches, in this order on `stream`: one
+ * persistent tensor-core kernel for dX (tcgen05 on CTA pairs, 256 x 256
+ * output tiles), then the sketch's launches.  dX comes first because the
+ * layer below waits for it, the sketch only for the end of the step.  The
+ * sketch uses the stream's workspace as logra_sketch_accumulate does; the dX
+ * kernel uses none.
+ */
+int logra_linear_backward(const void* X, const void* dY, const void* W,
+                          void* dX, int64_t n, int64_t d, int64_t k, int r,
+                          uint64_t seed, uint64_t step, float* S,
+                          logra_stream_t stream);
+
+/*
  * logra_rowadam_apply -- RowAdam update rebuilt from the sketch:
  *   Ghat = S A;  v_i <- beta2 v_i + (1-beta2) * mean_j Ghat_ij^2;
  *   W_ij <- W_ij - lr * c * Ghat_ij / sqrt(v_i + eps).

@@ -41,6 +41,7 @@ SIGNATURES = {
     "logra_set_concurrency": (_I, [_I]),
     "logra_sketch_accumulate_noalloc": (_I, [_VP, _VP, _I64, _I64, _I64, _I, _U64, _U64, _VP, _VP]),
     "logra_noalloc_scratch_bytes": (_SZ, []),
+    "logra_linear_backward": (_I, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _I, _U64, _U64, _VP, _VP]),
 }
 
 
@@ -143,6 +144,35 @@ def logra_sketch_accumulate(X, dY, S, seed: int, step: int, stream=None):
     _check(lib().logra_sketch_accumulate(px, py, _in_dtype(X), n, d, k, r, seed, step, ps, _stream(stream)),
            "logra_sketch_accumulate")
     return S
+
+
+def logra_linear_backward(dY, W=None, dX=None, X=None, S=None, seed: int = 0, step: int = 0, stream=None):
+    """Linear-layer backward for one microbatch: dX = dY W (bf16) and S += dY^T (X A^T).
+
+    dY: n x d bf16; W: d x k bf16 and dX: n x k bf16 (out), or both None for the sketch only;
+    X: n x k bf16 and S: d x r fp32, or both None for dX only."""
+    import torch
+    bf = (torch.bfloat16,)
+    n, d = dY.shape
+    if dX is not None:
+        k = dX.shape[1]
+    elif X is not None:
+        k = X.shape[1]
+    else:
+        raise ValueError("dX and S are both None: nothing to compute")
+    r = 32
+    py = _dev(dY, "dY", bf)
+    pw = _dev(W, "W", bf, (d, k)) if dX is not None else None
+    pdx = _dev(dX, "dX", bf, (n, k)) if dX is not None else None
+    px = _dev(X, "X", bf, (n, k)) if S is not None else None
+    if S is not None:
+        r = S.shape[1]
+        ps = _dev(S, "S", (torch.float32,), (d, r))
+    else:
+        ps = None
+    _check(lib().logra_linear_backward(px, py, pw, pdx, n, d, k, r, seed, step, ps, _stream(stream)),
+           "logra_linear_backward")
+    return dX
 
 
 def logra_sketch_accumulate_group(items, step: int, stream=None):

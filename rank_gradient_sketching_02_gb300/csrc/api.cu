@@ -1,6 +1,7 @@
 // C ABI of liblogra: argument checks, per-(device, stream) workspace, the
 // per-device control block, and the launches behind each logra_* entry point.
 #include <cmath>
+#include <cstdint>
 #include <cstdio>
 #include <atomic>
 #include <cstring>
@@ -380,6 +381,26 @@ int logra_sketch_accumulate_group(const logra_sketch_item* items, int count, int
     if (e != cudaSuccess && first_error == LOGRA_OK) first_error = cuda_fail(e);
   }
   return first_error;
+}
+
+int logra_linear_backward(const void* X, const void* dY, const void* W, void* dX, int64_t n, int64_t d, int64_t k,
+                          int r, uint64_t seed, uint64_t step, float* S, logra_stream_t stream) {
+  if (n < 0 || (!dX && !S)) return LOGRA_ERR_INVALID_ARG;
+  if (int st = check_mat(d, k)) return st;
+  if (S && check_rank(r)) return LOGRA_ERR_UNSUPPORTED;
+  if (n > int64_t(INT32_MAX)) return LOGRA_ERR_UNSUPPORTED;
+  if (n == 0) return LOGRA_OK;
+  if (!dY || (dX && !W) || (S && !X)) return LOGRA_ERR_INVALID_ARG;
+  if (!aligned16(dY) || (dX && (!aligned16(dX) || !aligned16(W))) || (S && (!aligned16(X) || !aligned16(S))))
+    return LOGRA_ERR_UNSUPPORTED;
+  int st;
+  if (dX) {
+    Control* ctl = control_block(&st);
+    if (!ctl) return st;
+    if ((st = launch_dgrad_tc(dY, W, dX, n, d, k, 0, ctl, stream))) return st;
+  }
+  if (S) return sketch_bf16_on(X, dY, n, d, k, r, seed, step, S, stream);
+  return LOGRA_OK;
 }
 
 // 1 / (1 - beta2^t): the factor of Adam's bias correction for the t-th

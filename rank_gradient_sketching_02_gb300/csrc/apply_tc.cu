@@ -71,10 +71,6 @@ struct ApplyShared {
 constexpr size_t kApplySmem = 1024 + kAbStages * (kABytes + kBBytes) + kWStages * kWBytes + 2 * kWBytes + 2 * kHBytes +
                               sizeof(ApplyShared) + 64;
 
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {

@@ -29,6 +29,10 @@ struct ZeroTrack;
 int launch_sketch_tc(const void* X, const void* dY, int64_t n, int64_t d, int64_t k, int r, uint64_t key,
                      float scale, float* S, void* ws, ZeroTrack* zt, Control* ctl, cudaStream_t s);
 
+// dX = dY W (bf16 in and out) on CTA pairs; max_pairs > 0 caps the grid.
+int launch_dgrad_tc(const void* dY, const void* W, void* dX, int64_t n, int64_t d, int64_t k, int max_pairs,
+                    Control* ctl, cudaStream_t s);
+
 size_t s_image_bytes(int64_t d, int r);
 
 // Matrices per grouped apply launch.

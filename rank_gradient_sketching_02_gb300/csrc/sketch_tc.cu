@@ -84,14 +84,6 @@ struct Shared {
   int abort;
 };
 
-struct Ring {
-  int stage = 0;
-  uint32_t phase = 0;
-  __device__ __forceinline__ void next(int n) {
-    if (++stage == n) { stage = 0; phase ^= 1u; }
-  }
-};
-
 // Stream-K work split: the flattened (tile, chunk) space of `total` chunks,
 // `per` chunks per tile, is cut into gridDim.x equal contiguous ranges, one per
 // CTA.  A CTA's range falls into segments at tile boundaries; every segment
@@ -120,10 +112,6 @@ struct SegIter {
     return true;
   }
 };
-
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
 
 // The MMA issuer is a single thread, so per-MMA work on it is latency it
 // cannot hide.  Descriptors are built once per ring and advanced by plain adds
@@ -181,23 +169,6 @@ __device__ __forceinline__ void accumulate_pair_mmas(uint32_t tmem, uint64_t ad,
         mma_bf16_pair(acc, am + 4, bk, idesc, 1u);     // lo term: bytes 64..127 of each row
       }
     }
-}
-
-// warp_wait for a barrier completed from the other CTA of a pair.
-template <class SH>
-__device__ __forceinline__ bool warp_wait_cluster(SH* sh, uint64_t* bar, uint32_t parity, unsigned long long limit,
-                                                  Control* ctl) {
-  int ok = 0;
-  if ((threadIdx.x & 31) == 0) ok = wait_or_abort_cluster(sh, bar, parity, limit, ctl) ? 1 : 0;
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (ok) (void)mbar_try_wait_cluster(bar, parity);
-  return ok != 0;
-}
-
-// Copies still in flight land before the CTA exits: wait (bounded) for the
-// last phase issued on every stage of a ring; phases already consumed pass.
-__device__ __forceinline__ void drain_ring(uint64_t* full, const Ring& rg, int n, unsigned long long limit) {
-  for (int s = 0; s < n; ++s) mbar_wait(&full[s], (s < rg.stage) ? rg.phase : (rg.phase ^ 1u), limit);
 }
 
 }  // namespace

@@ -145,6 +145,36 @@ __device__ __forceinline__ bool wait_or_abort_cluster(SH* sh, uint64_t* bar, uin
   return true;
 }
 
+// warp_wait for a barrier completed from the other CTA of a pair.
+template <class SH>
+__device__ __forceinline__ bool warp_wait_cluster(SH* sh, uint64_t* bar, uint32_t parity, unsigned long long limit,
+                                                  Control* ctl) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = wait_or_abort_cluster(sh, bar, parity, limit, ctl) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) (void)mbar_try_wait_cluster(bar, parity);
+  return ok != 0;
+}
+
+// ----------------------------------------------------------------- rings of shared-memory stages
+struct Ring {
+  int stage = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++stage == n) { stage = 0; phase ^= 1u; }
+  }
+};
+
+// Copies still in flight land before the CTA exits: wait (bounded) for the
+// last phase issued on every stage of a ring; phases already consumed pass.
+__device__ __forceinline__ void drain_ring(uint64_t* full, const Ring& rg, int n, unsigned long long limit) {
+  for (int s = 0; s < n; ++s) mbar_wait(&full[s], (s < rg.stage) ? rg.phase : (rg.phase ^ 1u), limit);
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
 // ----------------------------------------------------------------- clusters (CTA pairs)
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

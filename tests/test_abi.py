@@ -63,6 +63,13 @@ def test_bad_arguments_rejected_before_any_cuda_call(lib):
     assert lib.logra_sign_matrix(0, 0, 544, 8, 16, None) == LOGRA_ERR_UNSUPPORTED
     assert lib.logra_reconstruct(16, 8, 8, 32, 0, 0, 16, 5, 0, None) == LOGRA_ERR_INVALID_ARG
     assert lib.logra_rowadam_predict(16, 16, 8, 8, 32, 0, 0, 0.9, 1e-8, 1e-3, None, None) == LOGRA_ERR_INVALID_ARG
+    # linear backward: neither output, a misaligned dX, a bad rank with S, n too large, n == 0 (no-op)
+    assert lib.logra_linear_backward(16, 16, 16, None, 64, 64, 64, 32, 0, 0, None, None) == LOGRA_ERR_INVALID_ARG
+    assert lib.logra_linear_backward(None, 16, 16, 18, 64, 64, 64, 32, 0, 0, None, None) == LOGRA_ERR_UNSUPPORTED
+    assert lib.logra_linear_backward(16, 16, None, None, 64, 64, 64, 48, 0, 0, 16, None) == LOGRA_ERR_UNSUPPORTED
+    assert lib.logra_linear_backward(16, 16, 16, 16, 2**31, 64, 64, 32, 0, 0, 16, None) == LOGRA_ERR_UNSUPPORTED
+    assert lib.logra_linear_backward(16, 16, None, 16, 64, 64, 64, 32, 0, 0, None, None) == LOGRA_ERR_INVALID_ARG
+    assert lib.logra_linear_backward(16, 16, 16, 16, 0, 64, 64, 32, 0, 0, 16, None) == 0
 
 
 def _items(binding, shapes, W=16, S=16, v=16):

@@ -78,3 +78,27 @@ def test_apply_timeout_is_reported_and_context_survives(L):
     _, _, _, dW = O.rowadam_apply(np.zeros((d, k)), S64, np.zeros(d), 1, 1, b2, eps, lr, 1.0)
     got = W.double().cpu().numpy()
     assert np.linalg.norm(got - dW) / np.linalg.norm(dW) <= 1e-5
+
+
+def test_dgrad_timeout_is_reported_and_context_survives(L):
+    import torch
+    n, d, k = 512, 512, 768
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    dY = torch.randn((n, d), generator=g, device="cuda").to(torch.bfloat16)
+    W = torch.randn((d, k), generator=g, device="cuda").to(torch.bfloat16)
+    dX = torch.zeros((n, k), dtype=torch.bfloat16, device="cuda")
+    assert L.logra_get_status() == 0
+    L.logra_debug_inject(1, SHORT_WAIT)
+    try:
+        L.logra_linear_backward(dY, W=W, dX=dX)
+        assert L.logra_get_status() == L.binding.LOGRA_ERR_TIMEOUT
+    finally:
+        L.logra_debug_inject(0, DEFAULT_WAIT)
+    assert L.logra_get_status() == 0
+    L.logra_linear_backward(dY, W=W, dX=dX)
+    torch.cuda.synchronize()
+    assert L.logra_get_status() == 0
+    want = O.input_gradient(dY.double().cpu().numpy(), W.double().cpu().numpy())
+    got = dX.double().cpu().numpy()
+    assert np.linalg.norm(got - want) / np.linalg.norm(want) <= 2.0 ** -8
