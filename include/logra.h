@@ -190,10 +190,13 @@ int logra_sketch_accumulate_group(const logra_sketch_item* items, int count,
  * dX and S must not both be NULL (LOGRA_ERR_INVALID_ARG); n must be below
  * 2^31 (LOGRA_ERR_UNSUPPORTED).  Launches, in this order on `stream`: one
  * persistent tensor-core kernel for dX (tcgen05 on CTA pairs, 256 x 256
- * output tiles), then the sketch's launches.  dX comes first because the
- * layer below waits for it, the sketch only for the end of the step.  The
- * sketch uses the stream's workspace as logra_sketch_accumulate does; the dX
- * kernel uses none.
+ * output tiles taken from a per-stream tile counter), then the sketch's
+ * launches.  dX comes first because the layer below waits for it, the sketch
+ * only for the end of the step.  The sketch uses the stream's workspace as
+ * logra_sketch_accumulate does; the dX kernel uses two words of the stream's
+ * zero-kept counters (16 KB, allocated by the first such call or apply on
+ * the stream: make one before capturing calls into a CUDA graph), which it
+ * leaves at zero.
  */
 int logra_linear_backward(const void* X, const void* dY, const void* W,
                           void* dX, int64_t n, int64_t d, int64_t k, int r,

@@ -393,14 +393,12 @@ int logra_linear_backward(const void* X, const void* dY, const void* W, void* dX
   if (!dY || (dX && !W) || (S && !X)) return LOGRA_ERR_INVALID_ARG;
   if (!aligned16(dY) || (dX && (!aligned16(dX) || !aligned16(W))) || (S && (!aligned16(X) || !aligned16(S))))
     return LOGRA_ERR_UNSUPPORTED;
+  if (!dX) return sketch_bf16_on(X, dY, n, d, k, r, seed, step, S, stream);
   int st;
-  if (dX) {
-    Control* ctl = control_block(&st);
-    if (!ctl) return st;
-    if ((st = launch_dgrad_tc(dY, W, dX, n, d, k, 0, ctl, stream))) return st;
-  }
-  if (S) return sketch_bf16_on(X, dY, n, d, k, r, seed, step, S, stream);
-  return LOGRA_OK;
+  Control* ctl = control_block(&st);
+  if (!ctl) return st;
+  if ((st = launch_dgrad_tc(dY, W, dX, n, d, k, 0, ctl, stream))) return st;
+  return S ? sketch_bf16_on(X, dY, n, d, k, r, seed, step, S, stream) : LOGRA_OK;
 }
 
 // 1 / (1 - beta2^t): the factor of Adam's bias correction for the t-th

@@ -76,6 +76,9 @@ void forget_zero_workspaces();
 // pass; from kArrivalBase, kArrivalWords per matrix of a grouped apply: the
 // Gram tiles' arrivals (at most 16 x 16 tiles of 32 x 32 for r <= 512).
 constexpr int kArrivalBase = 64;
+// Words 8 and 9: the dX kernel's tile counter and finished-pair counter.
+constexpr int kDgradNextWord = 8;
+constexpr int kDgradDoneWord = 9;
 constexpr int kArrivalWords = 256;
 constexpr int kCounterWords = 4096;
 // Gram counts per (device, stream): r x r ints (r <= 512) for each of up to

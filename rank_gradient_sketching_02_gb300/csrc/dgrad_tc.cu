@@ -16,9 +16,11 @@
 // Each CTA's TMEM holds two 128 x 256 fp32 accumulators (512 columns): the
 // epilogue drains one tile while the MMAs fill the next.  Epilogue: TMEM ->
 // registers -> bf16 (round to nearest even) -> shared memory (swizzled) -> TMA
-// store; the store clips rows past n and columns past k.  Tiles go to pairs
-// round robin, k-column tile fastest, so the pairs at work at one time share
-// their dY token rows and the W rows of the current d stage through L2.
+// store; the store clips rows past n and columns past k.  Tiles are taken in
+// raster order from a per-stream counter by whichever pair is free; the
+// grouped raster lets the pairs at work at one time share dY rows and W
+// columns through L2, and pairs that start late, behind other kernels, just
+// take fewer tiles.
 //
 // Roles per CTA (192 threads): warp 0 = TMA producer, warp 1 = TMEM owner and
 // (in the even CTA) the MMA issuer, warps 2..5 = epilogue (TMEM lane quadrant
@@ -61,19 +63,26 @@ struct DgradShape {
 // tiles, so the dY rows and W columns they read are shared through L2: a wave
 // of 74 tiles reads ~8 token tiles' dY and ~9 column tiles' W per d stage
 // instead of one token tile's and all 74 column tiles' (k = 18944).
-__device__ __forceinline__ void dgrad_tile(const DgradShape& P, int64_t t, int& mt, int& nt) {
-  const int64_t per_group = int64_t(kDgGroupM) * P.ntiles;
+__device__ __forceinline__ void dgrad_tile(const DgradShape& P, unsigned t, int& mt, int& nt) {
+  const unsigned per_group = unsigned(kDgGroupM) * unsigned(P.ntiles);
   const int g = int(t / per_group);
   const int first = g * kDgGroupM;
   const int gsz = P.mtiles - first < kDgGroupM ? P.mtiles - first : kDgGroupM;
-  const int local = int(t - int64_t(g) * per_group);
+  const int local = int(t - unsigned(g) * per_group);
   mt = first + local % gsz;
   nt = local / gsz;
 }
 
+// Tile slots between the pair's scheduler and the tile index's readers: the
+// leader's MMA thread, the peer's producer, the 4 epilogue warps of each CTA.
+constexpr int kDgTileSlots = 4;
+constexpr int kDgTileReaders = 1 + 1 + 4 + 4;
+
 struct DgShared {
   uint64_t full[kDgMaxStages], empty[kDgMaxStages];
   uint64_t tmem_full[2], tmem_empty[2], drain;
+  uint64_t tile_full[kDgTileSlots], tile_empty[kDgTileSlots];
+  int tile_id[kDgTileSlots];
   uint32_t tmem_base;
   int abort;
 };
@@ -87,7 +96,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(uint32_t a, uint32_t b) {
 
 __global__ void __launch_bounds__(192, 1)
     dgrad_pair_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_w,
-                      const __grid_constant__ CUtensorMap tmap_dx, DgradShape P, Control* ctl) {
+                      const __grid_constant__ CUtensorMap tmap_dx, DgradShape P, unsigned* sched, Control* ctl) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   const int NS = P.stages;
@@ -98,8 +107,8 @@ __global__ void __launch_bounds__(192, 1)
   const unsigned long long limit = ctl->wait_limit;
   const uint32_t cta = cluster_ctarank();
   const bool leader = cta == 0;
-  const int pair = int(cluster_id_x()), npairs = int(cluster_count_x());
-  const int64_t tiles = int64_t(P.mtiles) * P.ntiles;
+  const int npairs = int(cluster_count_x());
+  const unsigned tiles = unsigned(P.mtiles) * unsigned(P.ntiles);
   constexpr uint32_t kTmemCols = 512;
 
   if (threadIdx.x == 0) {
@@ -110,6 +119,10 @@ __global__ void __launch_bounds__(192, 1)
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sh->tmem_full[a], 1);
       mbar_init(&sh->tmem_empty[a], 8);    // the 4 epilogue warps of each CTA of the pair
+    }
+    for (int q = 0; q < kDgTileSlots; ++q) {
+      mbar_init(&sh->tile_full[q], 1);
+      mbar_init(&sh->tile_empty[q], kDgTileReaders);
     }
     mbar_init(&sh->drain, 1);
     sh->abort = 0;
@@ -129,11 +142,31 @@ __global__ void __launch_bounds__(192, 1)
   grid_dependency_wait();      // dY and W come from earlier work on the stream
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer (both CTAs)
+    // ---------------------------------------------------------------- tile scheduler + TMA producer
+    // The leader's thread takes the pair's next tile from the stream's tile
+    // counter and posts its index into both CTAs' tile slots; the peer's
+    // producer reads it there.  Pairs that start late (SMs busy with other
+    // kernels) simply take fewer tiles.
     if (lane == 0) {
       Ring rg;
       int inject = ctl->inject_fault && blockIdx.x == 0;
-      for (int64_t t = pair; t < tiles; t += npairs) {
+      for (int j = 0;; ++j) {
+        const int q = j & (kDgTileSlots - 1);
+        const uint32_t ph = uint32_t(j / kDgTileSlots) & 1u;
+        unsigned t;
+        if (leader) {
+          if (!wait_or_abort_cluster(sh, &sh->tile_empty[q], ph ^ 1u, limit, ctl)) break;
+          t = atomicAdd(&sched[kDgradNextWord], 1u);
+          sh->tile_id[q] = int(t < tiles ? t : tiles);
+          st_shared_cluster_u32(mapa_shared(smem_addr(&sh->tile_id[q]), 1), t < tiles ? t : tiles);
+          mbar_arrive(&sh->tile_full[q]);
+          mbar_arrive_cluster(mapa_shared(smem_addr(&sh->tile_full[q]), 1));
+        } else {
+          if (!wait_or_abort_cluster(sh, &sh->tile_full[q], ph, limit, ctl)) break;
+          t = unsigned(*reinterpret_cast<volatile int*>(&sh->tile_id[q]));
+          mbar_arrive_cluster(mapa_shared(smem_addr(&sh->tile_empty[q]), 0));
+        }
+        if (t >= tiles) break;
         int mt, nt;
         dgrad_tile(P, t, mt, nt);
         const int tok0 = mt * (2 * kDgTok) + int(cta) * kDgTok;
@@ -154,7 +187,17 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
     p_done:
-      if (leader) drain_ring(sh->full, rg, NS, limit);
+      if (leader) {
+        drain_ring(sh->full, rg, NS, limit);
+        // Every pair has taken its last index from the tile counter before it
+        // counts itself finished; the last pair to finish sets both counters
+        // back to zero for the next launch on the stream.
+        __threadfence();
+        if (atomicInc(&sched[kDgradDoneWord], unsigned(npairs - 1)) == unsigned(npairs - 1)) {
+          __threadfence();
+          atomicExch(&sched[kDgradNextWord], 0u);
+        }
+      }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer (leader only)
@@ -163,11 +206,15 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t idesc = idesc_bf16(256, kDgCols, 0, 1);
       const uint64_t adesc0 = smem_desc(smem_addr(stages), 16, 1024, kSw128);
       const uint64_t bdesc0 = smem_desc(smem_addr(stages + kDgABytes), kDgK * 128, 1024, kSw128);
-      int i = 0;
-      for (int64_t t = pair; t < tiles && !sh->abort; t += npairs, ++i) {
-        const int acc = i & 1;
+      for (int j = 0; !sh->abort; ++j) {
+        const int q = j & (kDgTileSlots - 1);
+        if (!wait_or_abort(sh, &sh->tile_full[q], uint32_t(j / kDgTileSlots) & 1u, limit, ctl)) goto mma_done;
+        const unsigned t = unsigned(*reinterpret_cast<volatile int*>(&sh->tile_id[q]));
+        mbar_arrive(&sh->tile_empty[q]);
+        if (t >= tiles) break;
+        const int acc = j & 1;
         // both CTAs have drained this accumulator's previous tile
-        if (!wait_or_abort_cluster(sh, &sh->tmem_empty[acc], (uint32_t(i >> 1) & 1u) ^ 1u, limit, ctl))
+        if (!wait_or_abort_cluster(sh, &sh->tmem_empty[acc], (uint32_t(j >> 1) & 1u) ^ 1u, limit, ctl))
           goto mma_done;
         tc_fence_after();
         const uint32_t d_tmem = tmem + uint32_t(acc * kDgCols);
@@ -193,10 +240,18 @@ __global__ void __launch_bounds__(192, 1)
     // ---------------------------------------------------------------- epilogue: TMEM -> bf16 -> smem -> TMA store
     const int quad = warp & 3;
     uint8_t* tile0 = staging + (warp - 2) * 4 * kDgOutTile;
-    int i = 0;
-    for (int64_t t = pair; t < tiles; t += npairs, ++i) {
-      const int acc = i & 1;
-      if (!warp_wait_cluster(sh, &sh->tmem_full[acc], uint32_t(i >> 1) & 1u, limit, ctl)) break;
+    for (int j = 0;; ++j) {
+      const int q = j & (kDgTileSlots - 1);
+      if (!warp_wait_cluster(sh, &sh->tile_full[q], uint32_t(j / kDgTileSlots) & 1u, limit, ctl)) break;
+      const unsigned t = unsigned(*reinterpret_cast<volatile int*>(&sh->tile_id[q]));
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(&sh->tile_empty[q]);
+        else mbar_arrive_cluster(mapa_shared(smem_addr(&sh->tile_empty[q]), 0));
+      }
+      if (t >= tiles) break;
+      const int acc = j & 1;
+      if (!warp_wait_cluster(sh, &sh->tmem_full[acc], uint32_t(j >> 1) & 1u, limit, ctl)) break;
       tc_fence_after();
       int mt, nt;
       dgrad_tile(P, t, mt, nt);
@@ -210,15 +265,15 @@ __global__ void __launch_bounds__(192, 1)
         tmem_ld32(taddr, v0);
         tmem_ld32(taddr + 32, v1);
         tmem_ld_wait();
-        // this lane's token row: 64 columns = 128 bytes, 16-byte chunk q at q ^ (lane & 7)
+        // this lane's token row: 64 columns = 128 bytes, 16-byte chunk c at c ^ (lane & 7)
         uint8_t* row = tile0 + cb * kDgOutTile + lane * 128;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint32_t* v = q < 4 ? v0 : v1;
-          const int j = (q & 3) * 8;
-          *reinterpret_cast<uint4*>(row + ((q ^ (lane & 7)) << 4)) =
-              make_uint4(pack_bf16x2_rn(v[j], v[j + 1]), pack_bf16x2_rn(v[j + 2], v[j + 3]),
-                         pack_bf16x2_rn(v[j + 4], v[j + 5]), pack_bf16x2_rn(v[j + 6], v[j + 7]));
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t* v = c < 4 ? v0 : v1;
+          const int e = (c & 3) * 8;
+          *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) << 4)) =
+              make_uint4(pack_bf16x2_rn(v[e], v[e + 1]), pack_bf16x2_rn(v[e + 2], v[e + 3]),
+                         pack_bf16x2_rn(v[e + 4], v[e + 5]), pack_bf16x2_rn(v[e + 6], v[e + 7]));
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -261,6 +316,13 @@ static DgradShape dgrad_plan(int64_t n, int64_t d, int64_t k) {
   return P;
 }
 
+static int dgrad_pairs(int64_t tiles, int max_pairs) {
+  int pairs = sm_count() / 2;
+  if (max_pairs > 0 && pairs > max_pairs) pairs = max_pairs;
+  if (int64_t(pairs) > tiles) pairs = int(tiles);
+  return pairs < 1 ? 1 : pairs;
+}
+
 int launch_dgrad_tc(const void* dY, const void* W, void* dX, int64_t n, int64_t d, int64_t k, int max_pairs,
                     Control* ctl, cudaStream_t s) {
   const DgradShape P = dgrad_plan(n, d, k);
@@ -275,14 +337,15 @@ int launch_dgrad_tc(const void* dY, const void* W, void* dX, int64_t n, int64_t 
                             64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
     return st;
   const int64_t tiles = int64_t(P.mtiles) * P.ntiles;
-  int pairs = sm_count() / 2;
-  if (max_pairs > 0 && pairs > max_pairs) pairs = max_pairs;
-  if (int64_t(pairs) > tiles) pairs = int(tiles);
-  if (pairs < 1) pairs = 1;
+  if (tiles >= (int64_t(1) << 31)) return LOGRA_ERR_UNSUPPORTED;    // 32-bit tile counter
+  int st = LOGRA_OK;
+  unsigned* sched = stream_counter(s, &st);
+  if (!sched) return st;
+  const int pairs = dgrad_pairs(tiles, max_pairs);
   const int smem = 1024 + P.stages * kDgStageBytes + kDgStaging + int(sizeof(DgShared));
   LOGRA_CUDA_TRY(ensure_smem(reinterpret_cast<const void*>(dgrad_pair_kernel), smem));
   LOGRA_CUDA_TRY(launch_overlapped_cluster(dgrad_pair_kernel, dim3(2 * pairs), dim3(192), size_t(smem), s, 2u, tdy,
-                                           tw, tdx, P, ctl));
+                                           tw, tdx, P, sched, ctl));
   LOGRA_LAUNCHED();
   return LOGRA_OK;
 }
