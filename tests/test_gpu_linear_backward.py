@@ -154,3 +154,62 @@ def test_dgrad_full_size_gate_sampled_rows(L):
     rows_t = torch.from_numpy(rows).cuda()
     check_dx(host64(gX.t[rows_t]), host64(dY[rows_t]), host64(W))
     assert not torch.isnan(gX.t.float()).any()
+
+
+# ------------------------------------------------------------------ scheduling: graphs, streams, late pairs
+def test_linear_backward_replayed_as_cuda_graph(L):
+    """Captured once (the first eager call allocates the stream's counters and workspace), replayed:
+    every replay gives the oracle's dX and sketch, and the tile counter is left at zero each time."""
+    import torch
+    n, d, k, r = 1024, 1032, 776, 128
+    X, dY, _ = synth.host_microbatch(n, d, k, dy_kind="gauss", key=(31,))
+    W = synth.host_weight(d, k, key=(32,))
+    Xd, dYd, Wd = synth.to_bf16_bits(X).cuda(), synth.to_bf16_bits(dY).cuda(), synth.to_bf16_bits(W).cuda()
+    s = torch.cuda.Stream()
+    dX = torch.empty((n, k), dtype=torch.bfloat16, device="cuda")
+    S = torch.zeros((d, r), dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(s):
+        L.logra_linear_backward(dYd, W=Wd, dX=dX, X=Xd, S=S, seed=5, step=6)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        S.zero_()
+        dX.zero_()
+        L.logra_linear_backward(dYd, W=Wd, dX=dX, X=Xd, S=S, seed=5, step=6)
+    want_S = O.sketch_accumulate(np.zeros((d, r)), host64(Xd), host64(dYd), 5, 6, r)
+    for _ in range(3):
+        g.replay()
+        torch.cuda.synchronize()
+        check_dx(host64(dX), host64(dYd), host64(Wd))
+        assert rel(host64(S), want_S) <= TOL_S_BF16
+    assert L.logra_get_status() == 0
+
+
+def test_dgrad_on_concurrent_streams_with_late_pairs(L):
+    """Two dX calls on two streams at once (each stream has its own tile counter) while a third
+    stream keeps SMs busy with sketches, so that some CTA pairs start late and take fewer tiles."""
+    import torch
+    shapes = [(2048, 3584, 1032), (1536, 2056, 3584)]
+    ins, outs = [], []
+    for i, (n, d, k) in enumerate(shapes):
+        _, dY, _ = synth.host_microbatch(n, d, 8, dy_kind="gauss", key=(40 + i,))
+        W = synth.host_weight(d, k, key=(50 + i,))
+        ins.append((synth.to_bf16_bits(dY).cuda(), synth.to_bf16_bits(W).cuda()))
+        outs.append(torch.empty((n, k), dtype=torch.bfloat16, device="cuda"))
+    Xb = torch.randn((8192, 3584), device="cuda").to(torch.bfloat16)
+    dYb = torch.randn((8192, 4096), device="cuda").to(torch.bfloat16)
+    Sb = torch.zeros((4096, 256), device="cuda")
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    torch.cuda.synchronize()
+    for rep in range(3):
+        with torch.cuda.stream(streams[2]):
+            for _ in range(4):
+                L.logra_sketch_accumulate(Xb, dYb, Sb, 1, rep)
+        for i in range(2):
+            with torch.cuda.stream(streams[i]):
+                outs[i].fill_(float("nan"))
+                L.logra_linear_backward(ins[i][0], W=ins[i][1], dX=outs[i])
+        torch.cuda.synchronize()
+        for i in range(2):
+            check_dx(host64(outs[i]), host64(ins[i][0]), host64(ins[i][1]))
+    assert L.logra_get_status() == 0
