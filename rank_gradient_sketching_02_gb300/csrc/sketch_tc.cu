@@ -1020,6 +1020,14 @@ static SketchShape plan(int64_t n, int64_t d, int64_t k, int r, int sms) {
     P.pdb = 2 / P.prb;
     P.pdtiles = ceil_div(d, P.pdb * 256);
     P.pairs = stream_k_ctas_hinted(int64_t(P.pdtiles) * tchunks, sms / 2, 12, 12 * hint, hint);
+    // Prefer a pair count that cuts every tile into s equal parts (s dividing the
+    // tile's chunks): each pair's range is then one segment, with one drain of
+    // its accumulators instead of two.  On one stream only when it keeps 90% of
+    // the pairs; under the concurrency hint (SM-time counts) when it keeps half.
+    int best = 0;
+    for (int sp = 1; sp <= tchunks && int64_t(P.pdtiles) * sp <= P.pairs; sp <<= 1)
+      if (tchunks % sp == 0) best = P.pdtiles * sp;
+    if (best > 0 && (hint > 1 ? 2 * best >= P.pairs : 10 * best >= 9 * P.pairs)) P.pairs = best;
   }
   // With sketch calls running on several streams at once, each accumulate takes
   // fewer, longer CTA ranges: SMs stay free for the other streams' kernels and
