@@ -973,6 +973,17 @@ static int stream_k_ctas_hinted(int64_t total, int sms, int min_chunks, int hint
   return wide > floor_ctas ? wide : floor_ctas;
 }
 
+// A stream-K grid of `base` CTAs over `tiles` tiles of `per` chunks each,
+// replaced by tiles * s CTAs (s dividing `per`, as many as fit in `base`) when
+// that keeps at least num/den of them: every CTA's range is then 1/s of one
+// tile, a single segment with a single drain, instead of straddling two.
+static int tile_aligned_ctas(int64_t tiles, int per, int base, int num, int den) {
+  int64_t best = 0;
+  for (int64_t s = 1; tiles * s <= base && s <= per; ++s)
+    if (per % s == 0) best = tiles * s;
+  return (best > 0 && best * den >= int64_t(base) * num) ? int(best) : base;
+}
+
 // True when some CTA's range starts or ends inside a tile, i.e. some segment
 // covers only part of that tile's chunks.
 static bool has_partial_segment(int64_t total, int per, int ctas) {
@@ -1007,7 +1018,9 @@ static SketchShape plan(int64_t n, int64_t d, int64_t k, int r, int sms) {
     if (int64_t(c) > ptotal) c = int(ptotal);
     P.proj_ctas = c < sms ? c : sms;
   } else {
-    P.proj_ctas = stream_k_ctas(ptotal, sms, 8);
+    // (ranges of whole fractions of a group's k range when that keeps 80% of the
+    // CTAs: one partial-sum drain per CTA)
+    P.proj_ctas = tile_aligned_ctas(P.groups, P.nchunks, stream_k_ctas(ptotal, sms, 8), 4, 5);
   }
   P.proj_partial = has_partial_segment(ptotal, P.nchunks, P.proj_ctas) ? 1 : 0;
   P.direct = P.proj_partial ? 0 : 1;
@@ -1020,20 +1033,23 @@ static SketchShape plan(int64_t n, int64_t d, int64_t k, int r, int sms) {
     P.pdb = 2 / P.prb;
     P.pdtiles = ceil_div(d, P.pdb * 256);
     P.pairs = stream_k_ctas_hinted(int64_t(P.pdtiles) * tchunks, sms / 2, 12, 12 * hint, hint);
-    // Prefer a pair count that cuts every tile into s equal parts (s dividing the
-    // tile's chunks): each pair's range is then one segment, with one drain of
-    // its accumulators instead of two.  On one stream only when it keeps 90% of
-    // the pairs; under the concurrency hint (SM-time counts) when it keeps half.
-    int best = 0;
-    for (int sp = 1; sp <= tchunks && int64_t(P.pdtiles) * sp <= P.pairs; sp <<= 1)
-      if (tchunks % sp == 0) best = P.pdtiles * sp;
-    if (best > 0 && (hint > 1 ? 2 * best >= P.pairs : 10 * best >= 9 * P.pairs)) P.pairs = best;
+    // Prefer a pair count that cuts every tile into equal parts: each pair's
+    // range is then one segment, with one drain of its accumulators instead of
+    // two.  On one stream only when it keeps 90% of the pairs; under the
+    // concurrency hint (SM-time counts) when it keeps half.
+    P.pairs = hint > 1 ? tile_aligned_ctas(P.pdtiles, tchunks, P.pairs, 1, 2)
+                       : tile_aligned_ctas(P.pdtiles, tchunks, P.pairs, 9, 10);
   }
   // With sketch calls running on several streams at once, each accumulate takes
   // fewer, longer CTA ranges: SMs stay free for the other streams' kernels and
   // fewer partial S tiles are reduced in L2 (4 streams, 27B layers: +1.6% on
   // the step; one stream keeps every SM busy)
-  P.acc_ctas = P.pair ? 2 * P.pairs : stream_k_ctas_hinted(int64_t(P.dtiles) * tchunks, sms, 12, 12 * hint, hint);
+  if (P.pair) {
+    P.acc_ctas = 2 * P.pairs;
+  } else {
+    const int base = stream_k_ctas_hinted(int64_t(P.dtiles) * tchunks, sms, 12, 12 * hint, hint);
+    P.acc_ctas = hint > 1 ? tile_aligned_ctas(P.dtiles, tchunks, base, 1, 2) : tile_aligned_ctas(P.dtiles, tchunks, base, 9, 10);
+  }
   // project: three sign-tile stages when three X stages still fit beside
   // them (the generators then have a whole chunk of MMA time of slack), else
   // two; the rest of shared memory for X tiles
