@@ -305,35 +305,42 @@ def run_ours(args):
     # ---- resident state and inputs (the input generation is timed on its own, outside the step)
     # Inputs of `pool` distinct layers stay resident; layer l reads slot l mod pool (every layer
     # keeps its own W, S, v and seeds, so the work per layer is the same as with its own inputs).
+    # The projections that read one activation share it (q/k/v, gate/up: synth.input_group), and
+    # every tensor of a microbatch has the same padding rows.
     pool = layers if args.input_layers <= 0 else min(layers, args.input_layers)
     mats = []
-    inputs = {}
+    x_inputs, dy_inputs = {}, {}
     gen_ms = 0.0
     for layer in range(layers):
         for mi, (name, d, k) in enumerate(w.matrices):
             gen = torch.Generator(device=dev)
             gen.manual_seed(1000 + 16 * layer + mi)
             W = torch.empty((d, k), dtype=torch.float32, device=dev).normal_(0.0, 0.02, generator=gen)
-            slot = (layer % pool, mi)
-            if slot not in inputs:
+            ls, grp = layer % pool, synth.input_group(name)
+            g0 = torch.cuda.Event(enable_timing=True)
+            g1 = torch.cuda.Event(enable_timing=True)
+            g0.record()
+            if (ls, grp) not in x_inputs:
                 Xs = torch.empty((nmb, n, k), dtype=dt, device=dev)
-                Ys = torch.empty((nmb, n, d), dtype=dt, device=dev)
-                g0 = torch.cuda.Event(enable_timing=True)
-                g1 = torch.cuda.Event(enable_timing=True)
-                g0.record()
                 for mb in range(nmb):
-                    synth.device_microbatch(n, d, k, dy_kind=w.dy_kind, dy_std=w.dy_std, mask_frac=w.mask_frac,
-                                            key=(2026, rank, slot[0], mi, mb), dtype=dt, device=dev,
-                                            out_X=Xs[mb], out_dY=Ys[mb])
-                g1.record()
-                g1.synchronize()
-                gen_ms += g0.elapsed_time(g1)
-                inputs[slot] = (Xs, Ys)
+                    synth.device_activations(n, k, mask_frac=w.mask_frac, key=(2026, rank, ls, grp, mb),
+                                             mb_key=(2026, rank, ls, mb), dtype=dt, device=dev, out=Xs[mb])
+                x_inputs[(ls, grp)] = Xs
+            if (ls, mi) not in dy_inputs:
+                Ys = torch.empty((nmb, n, d), dtype=dt, device=dev)
+                for mb in range(nmb):
+                    synth.device_output_grads(n, d, dy_kind=w.dy_kind, dy_std=w.dy_std, mask_frac=w.mask_frac,
+                                              key=(2027, rank, ls, mi, mb), mb_key=(2026, rank, ls, mb), dtype=dt,
+                                              device=dev, out=Ys[mb])
+                dy_inputs[(ls, mi)] = Ys
+            g1.record()
+            g1.synchronize()
+            gen_ms += g0.elapsed_time(g1)
             m = {"name": name, "layer": layer, "d": d, "k": k, "seed": synth.matrix_seed(2026, layer, mi), "W": W,
                  "Wb": W.to(torch.bfloat16), "v": torch.zeros(d, dtype=torch.float32, device=dev),
                  "S": torch.zeros((d, r), dtype=torch.float32, device=dev),
                  "norms": torch.zeros(2, dtype=torch.float64, device=dev),
-                 "X": inputs[slot][0], "dY": inputs[slot][1]}
+                 "group": grp, "X": x_inputs[(ls, grp)], "dY": dy_inputs[(ls, mi)]}
             mats.append(m)
     torch.cuda.synchronize()
     layer_mats = [[m for m in mats if m["layer"] == li] for li in range(layers)]
@@ -341,9 +348,16 @@ def run_ours(args):
     def group_items(ms):
         return [{"W": m["W"], "S": m["S"], "v": m["v"], "seed": m["seed"], "lr": lr, "c": c,
                  "norms_out": m["norms"], "W_bf16_out": m["Wb"]} for m in ms]
-    input_bytes = sum(X.numel() * X.element_size() + Y.numel() * Y.element_size() for X, Y in inputs.values())
-    step_input_bytes = sum(m["X"].numel() * m["X"].element_size() + m["dY"].numel() * m["dY"].element_size()
-                           for m in mats)
+    input_bytes = sum(t.numel() * t.element_size() for t in list(x_inputs.values()) + list(dy_inputs.values()))
+    # one X per (layer, input group) and one dY per matrix, every microbatch
+    step_input_bytes = 0
+    for lm in layer_mats:
+        seen = set()
+        for mm in lm:
+            step_input_bytes += mm["dY"].numel() * mm["dY"].element_size()
+            if mm["group"] not in seen:
+                seen.add(mm["group"])
+                step_input_bytes += mm["X"].numel() * mm["X"].element_size()
 
     # a side stream as the step's main stream (a CUDA graph cannot be captured on the legacy
     # default stream, and the library's per-stream workspaces must be the ones warmed up)
@@ -681,6 +695,7 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; torch Philox on device)",
         "config": workload_config(w, layers, nmb, r, world, pool),
         "run": {"input_bytes_resident": input_bytes, "input_bytes_per_step": step_input_bytes,
+                "shared_activations": "q/k/v read one X, gate/up one X (per layer and microbatch)",
                 "input_pool": (f"layer l reads the inputs of resident slot l mod {pool}; W, S, v and the "
                                "sign matrices are per layer") if pool < layers else "every layer its own inputs",
                 "input_generation_ms": gen_ms,
@@ -731,21 +746,22 @@ def run_ours(args):
 
 
 def run_e2e(args, L, dp, mats, w, r, dt, dev, stream, sk_f, world, layer_mats, group_items):
-    """Same step, but every microbatch's X and dY come from pinned host memory
-    (copied on a side stream, double-buffered) and the norms go back to the host."""
+    """Same step, but every microbatch's inputs come from pinned host memory and the norms go
+    back to the host.  Per layer and microbatch the step's inputs are one X per input group
+    (q/k/v share one, gate/up one) and one dY per matrix; they are copied on two side streams
+    into one of two device slots (double-buffered: the next microbatch's copies overlap this
+    one's sketches)."""
     import torch
     from rank_gradient_sketching_02_gb300 import synth
     beta2, eps, lr, c = synth.BETA2, synth.EPS, synth.LR, synth.C
     n, nmb = w.tokens, args.microbatches or w.microbatches
-    host = {}
-    for m in mats:
-        key = (m["d"], m["k"])
-        if key not in host:
-            host[key] = (m["X"][0].cpu().pin_memory(), m["dY"][0].cpu().pin_memory())
-    maxk = max(m["k"] for m in mats)
-    maxd = max(m["d"] for m in mats)
-    bufX = [torch.empty(n * maxk, dtype=dt, device=dev) for _ in range(2)]
-    bufY = [torch.empty(n * maxd, dtype=dt, device=dev) for _ in range(2)]
+    lm0 = layer_mats[0]
+    groups = list(dict.fromkeys(m["group"] for m in lm0))
+    # pinned host copies of one microbatch's inputs (re-sent for every layer and microbatch)
+    host_x = {g: next(m for m in lm0 if m["group"] == g)["X"][0].cpu().pin_memory() for g in groups}
+    host_dy = [m["dY"][0].cpu().pin_memory() for m in lm0]
+    slots = [({g: torch.empty_like(host_x[g], device=dev) for g in groups},
+              [torch.empty_like(t, device=dev) for t in host_dy]) for _ in range(2)]
     # two copy streams, each moving half of every tensor, so two copy engines work at once
     copies = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
     norms_h = torch.empty((len(mats), 2), dtype=torch.float64).pin_memory()
@@ -755,43 +771,45 @@ def run_e2e(args, L, dp, mats, w, r, dt, dev, stream, sk_f, world, layer_mats, g
         nonlocal h2d, d2h
         done = [None, None]
         i = 0
-        for mi, m in enumerate(mats):
-            lm = layer_mats[m["layer"]]
-            Xh, Yh = host[(m["d"], m["k"])]
-            m["S"].zero_()
+        for lm in layer_mats:
+            for m in lm:
+                m["S"].zero_()
             for mb in range(nmb):
                 slot = i % 2
-                Xd = bufX[slot][: n * m["k"]].view(n, m["k"])
-                Yd = bufY[slot][: n * m["d"]].view(n, m["d"])
+                xs, dys = slots[slot]
                 readies = []
                 for half, cs in enumerate(copies):
                     with torch.cuda.stream(cs):
                         if done[slot] is not None:
                             cs.wait_event(done[slot])
                         lo, hi = (0, n // 2) if half == 0 else (n // 2, n)
-                        Xd[lo:hi].copy_(Xh[lo:hi], non_blocking=True)
-                        Yd[lo:hi].copy_(Yh[lo:hi], non_blocking=True)
+                        for g in groups:
+                            xs[g][lo:hi].copy_(host_x[g][lo:hi], non_blocking=True)
+                        for j in range(len(lm)):
+                            dys[j][lo:hi].copy_(host_dy[j][lo:hi], non_blocking=True)
                         ev_r = torch.cuda.Event()
                         ev_r.record(cs)
                         readies.append(ev_r)
-                h2d += Xh.numel() * Xh.element_size() + Yh.numel() * Yh.element_size()
+                h2d += sum(t.numel() * t.element_size() for t in list(host_x.values()) + host_dy)
                 for ev_r in readies:
                     stream.wait_event(ev_r)
-                L.logra_sketch_accumulate(Xd, Yd, m["S"], m["seed"], step_idx)
+                for j, m in enumerate(lm):
+                    L.logra_sketch_accumulate(xs[m["group"]], dys[j], m["S"], m["seed"], step_idx)
                 ev = torch.cuda.Event()
                 ev.record(stream)
                 done[slot] = ev
                 i += 1
-            dp.allreduce_sketch(m["S"])
+            for m in lm:
+                dp.allreduce_sketch(m["S"])
             if args.apply_mode == "single":
-                L.logra_rowadam_apply_ex(m["W"], m["S"], m["v"], m["seed"], step_idx, beta2, eps, lr, c,
-                                         m["norms"], m["Wb"], None)
-            elif m is lm[-1]:
+                for m in lm:
+                    L.logra_rowadam_apply_ex(m["W"], m["S"], m["v"], m["seed"], step_idx, beta2, eps, lr, c,
+                                             m["norms"], m["Wb"], None)
+            else:
                 L.logra_rowadam_apply_group(group_items(lm), step_idx, beta2, eps)
-            if args.apply_mode == "single" or m is lm[-1]:
-                for mm in ([m] if args.apply_mode == "single" else lm):
-                    norms_h[mats.index(mm)].copy_(mm["norms"], non_blocking=True)
-                    d2h += 16
+            for m in lm:
+                norms_h[mats.index(m)].copy_(m["norms"], non_blocking=True)
+                d2h += 16
         return norms_h
 
     e2e_step(10_000)
@@ -809,7 +827,8 @@ def run_e2e(args, L, dp, mats, w, r, dt, dev, stream, sk_f, world, layer_mats, g
     return {"value": world * sk_f / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d // steps, "d2h_bytes_per_step": d2h // steps,
             "h2d_gbs": (h2d / steps) / (ms * 1e-3) / 1e9,
-            "host_inputs": "pinned host copy of one microbatch per matrix shape, re-sent for every microbatch"}
+            "host_inputs": "pinned host copy of one microbatch's inputs of a layer (one X per input group, one "
+                           "dY per matrix), re-sent for every layer and microbatch"}
 
 
 def main(argv=None):

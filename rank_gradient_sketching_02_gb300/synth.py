@@ -22,6 +22,11 @@ only these matrices):
 From ``proj1536`` on, dY rows are z * s_t with z ~ N(0,1) and a per-token
 lognormal scale s_t = exp(-7 + 1.5 zeta_t), standing in for advantage-weighted
 RL gradients; padding rows are zero in both X and dY.
+
+Within a decoder layer the projections that read the same activation share it:
+q, k and v read the attention block's input, gate and up the MLP block's input
+(``input_group``); o and down read their own.  The benchmark keeps one X per
+(layer, input group) and microbatch, and one padding pattern per microbatch.
 """
 from __future__ import annotations
 
@@ -30,6 +35,14 @@ from dataclasses import dataclass, field
 import numpy as np
 
 MATRIX_NAMES = ("q", "k", "v", "o", "gate", "up", "down")
+
+_INPUT_GROUPS = {"q": "attn_in", "k": "attn_in", "v": "attn_in", "o": "attn_out",
+                 "gate": "mlp_in", "up": "mlp_in", "down": "mlp_act"}
+
+
+def input_group(matrix: str) -> str:
+    """The activation a projection reads: q/k/v share the attention input, gate/up the MLP input."""
+    return _INPUT_GROUPS.get(matrix, matrix)
 
 
 @dataclass(frozen=True)
@@ -122,6 +135,60 @@ def to_bf16_bits(a: np.ndarray):
     """Round float32 to bfloat16 (round to nearest even) and return it as a torch tensor."""
     import torch
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
+
+
+def _key_int(x) -> int:
+    """Integer key element; names (input groups) enter through their CRC-32."""
+    import zlib
+    return zlib.crc32(x.encode()) if isinstance(x, str) else int(x)
+
+
+def _device_generator(key, device):
+    import torch
+    seed = int(np.random.SeedSequence([_key_int(x) for x in key]).generate_state(1, np.uint64)[0] >> 1)
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def _device_padding_rows(n: int, mask_frac: float, mb_key, device):
+    """The padding rows of one microbatch (shared by every tensor of that microbatch)."""
+    import torch
+    nm = n_masked(n, mask_frac)
+    if not nm:
+        return None
+    return torch.randperm(n, generator=_device_generator(("pad",) + tuple(mb_key), device), device=device)[:nm]
+
+
+def device_activations(n: int, k: int, *, mask_frac: float, key, mb_key, dtype=None, device="cuda", out=None):
+    """One microbatch's activations X (n x k, N(0,1)) on the device, zero on the microbatch's padding rows."""
+    import torch
+    X = out if out is not None else torch.empty((n, k), dtype=dtype or torch.bfloat16, device=device)
+    X.normal_(0.0, 1.0, generator=_device_generator(key, device))
+    drop = _device_padding_rows(n, mask_frac, mb_key, device)
+    if drop is not None:
+        X.index_fill_(0, drop, 0.0)
+    return X
+
+
+def device_output_grads(n: int, d: int, *, dy_kind: str, dy_std: float = 1.0, mask_frac: float, key, mb_key,
+                        dtype=None, device="cuda", out=None):
+    """One microbatch's output gradients dY (n x d) on the device, distributed as in ``host_microbatch``,
+    zero on the microbatch's padding rows."""
+    import torch
+    dtype = dtype or torch.bfloat16
+    g = _device_generator(key, device)
+    dY = out if out is not None else torch.empty((n, d), dtype=dtype, device=device)
+    dY.normal_(0.0, 1.0, generator=g)
+    if dy_kind == "gauss":
+        dY.mul_(dy_std)
+    else:
+        s = torch.exp(-7.0 + 1.5 * torch.randn(n, generator=g, device=device, dtype=torch.float32))
+        dY.mul_(s.to(dtype)[:, None])
+    drop = _device_padding_rows(n, mask_frac, mb_key, device)
+    if drop is not None:
+        dY.index_fill_(0, drop, 0.0)
+    return dY
 
 
 def device_microbatch(n: int, d: int, k: int, *, dy_kind: str, dy_std: float = 1.0,
