@@ -61,8 +61,8 @@ struct DgradShape {
 // of kDgGroupM, column tiles outer, token tiles inner within a group.  The
 // pairs at work at one time (consecutive t) then cover about a square of
 // tiles, so the dY rows and W columns they read are shared through L2: a wave
-// of 74 tiles reads ~8 token tiles' dY and ~9 column tiles' W per d stage
-// instead of one token tile's and all 74 column tiles' (k = 18944).
+// of 76 tiles (one per pair) reads ~8 token tiles' dY and ~10 column tiles' W
+// per d stage instead of one token tile's and all 74 column tiles' (k = 18944).
 __device__ __forceinline__ void dgrad_tile(const DgradShape& P, unsigned t, int& mt, int& nt) {
   const unsigned per_group = unsigned(kDgGroupM) * unsigned(P.ntiles);
   const int g = int(t / per_group);
