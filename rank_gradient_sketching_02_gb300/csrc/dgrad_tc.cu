@@ -187,6 +187,7 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
     p_done:
+      drain_empties(sh, sh->empty, rg, NS, limit);
       if (leader) {
         drain_ring(sh->full, rg, NS, limit);
         // Every pair has taken its last index from the tile counter before it

@@ -830,6 +830,7 @@ __global__ void __launch_bounds__(352, 1)
     a_done:
       // the peer's copies complete on the leader's barriers: the leader waits for both halves
       if (leader) drain_ring(sh->o_full, ar, AS, limit);
+      drain_empties(sh, sh->o_empty, ar, AS, limit);
     }
   } else if (warp == 6) {
     // ---------------------------------------------------------------- dY tile producer (HBM)
@@ -851,6 +852,7 @@ __global__ void __launch_bounds__(352, 1)
       }
     b_done:
       if (leader) drain_ring(sh->s_full, br, BS, limit);
+      drain_empties(sh, sh->s_empty, br, BS, limit);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer (leader only)

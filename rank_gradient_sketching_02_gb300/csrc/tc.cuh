@@ -208,6 +208,21 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, const Ring& rg, int n
   for (int s = 0; s < n; ++s) mbar_wait(&full[s], (s < rg.stage) ? rg.phase : (rg.phase ^ 1u), limit);
 }
 
+// In a CTA pair the leader's MMA commits arrive on the other CTA's empty
+// barriers from another SM, asynchronously: before a CTA releases its shared
+// memory, its producer waits (bounded) until every stage it filled has been
+// released, so that no such arrival is still on its way.  After an abort the
+// consumer may never release a stage: each wait then gives up after a
+// sixty-fourth of the limit.
+template <class SH>
+__device__ __forceinline__ void drain_empties(SH* sh, uint64_t* empty, const Ring& rg, int n,
+                                              unsigned long long limit) {
+  for (int s = 0; s < n; ++s) {
+    const bool aborted = *reinterpret_cast<volatile int*>(&sh->abort) != 0;
+    mbar_wait(&empty[s], (s < rg.stage) ? rg.phase : (rg.phase ^ 1u), aborted ? limit / 64 + 1 : limit);
+  }
+}
+
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
