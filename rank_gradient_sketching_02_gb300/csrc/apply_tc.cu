@@ -219,6 +219,11 @@ __global__ void __launch_bounds__(480, 1)
       }
     a_done:
       for (int s = 0; s < AS; ++s) mbar_wait(&sh->ab_full[s], (s < stage) ? phase : (phase ^ 1u), limit);
+      // and the MMA commits' last arrivals on the ring land before the CTA can leave
+      for (int s = 0; s < AS; ++s) {
+        const bool aborted = *reinterpret_cast<volatile int*>(&sh->abort) != 0;
+        mbar_wait(&sh->ab_empty[s], (s < stage) ? phase : (phase ^ 1u), aborted ? limit / 64 + 1 : limit);
+      }
     }
   } else if (warp == 10) {
     // ------------------------------------------------------------------ W tile producer

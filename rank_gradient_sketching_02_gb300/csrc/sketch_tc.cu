@@ -337,6 +337,7 @@ __global__ void __launch_bounds__(512, 1)
       }
     producer_done:
       drain_ring(sh->s_full, xr, XS, limit);
+      drain_empties(sh, sh->s_empty, xr, XS, limit);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
@@ -357,8 +358,8 @@ __global__ void __launch_bounds__(512, 1)
           if (!wait_or_abort(sh, &sh->tmem_empty[ab * T + t], uphase ^ 1u, limit, ctl)) goto mma_done;
         tc_fence_after();
         for (int c = c0; c < c1; ++c) {
-          if (!spin_or_abort<false>(sh, &sh->s_full[xr.stage], xr.phase, limit, ctl)) goto mma_done;
-          if (!spin_or_abort<false>(sh, &sh->o_full[gr.stage], gr.phase, limit, ctl)) goto mma_done;
+          if (!wait_or_abort(sh, &sh->s_full[xr.stage], xr.phase, limit, ctl)) goto mma_done;
+          if (!wait_or_abort(sh, &sh->o_full[gr.stage], gr.phase, limit, ctl)) goto mma_done;
           tc_fence_after();
           const uint64_t ad = xdesc0 + uint64_t(uint32_t(xr.stage) * (x_bytes >> 4));
           const uint64_t bd = gdesc0 + uint64_t(uint32_t(gr.stage) * (g_bytes >> 4));
@@ -462,7 +463,9 @@ __global__ void __launch_bounds__(512, 1)
           gr.next(GS);
         }
       }
-    gen_done:;
+    gen_done:
+      // the MMA commits' last arrivals on the sign ring land before the CTA can leave
+      if (gtid == 0) drain_empties(sh, sh->o_empty, gr, GS, limit);
     }
     if (extra_drain && warp < 14 && !*reinterpret_cast<volatile int*>(&sh->abort)) {
       // -------------------------------------------------------------- share the final segment's image drain
@@ -612,6 +615,7 @@ __global__ void __launch_bounds__(352, 1)
       }
     a_done:
       drain_ring(sh->o_full, ar, AS, limit);
+      drain_empties(sh, sh->o_empty, ar, AS, limit);
     }
   } else if (warp == 6) {
     // ---------------------------------------------------------------- dY tile producer (HBM)
@@ -630,6 +634,7 @@ __global__ void __launch_bounds__(352, 1)
       }
     b_done:
       drain_ring(sh->s_full, br, BS, limit);
+      drain_empties(sh, sh->s_empty, br, BS, limit);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
@@ -648,8 +653,8 @@ __global__ void __launch_bounds__(352, 1)
           if (!wait_or_abort(sh, &sh->tmem_empty[ab * mblocks + m], uphase ^ 1u, limit, ctl)) goto mma_done;
         tc_fence_after();
         for (int c = c0; c < c1; ++c) {
-          if (!spin_or_abort<false>(sh, &sh->o_full[ar.stage], ar.phase, limit, ctl)) goto mma_done;
-          if (!spin_or_abort<false>(sh, &sh->s_full[br.stage], br.phase, limit, ctl)) goto mma_done;
+          if (!wait_or_abort(sh, &sh->o_full[ar.stage], ar.phase, limit, ctl)) goto mma_done;
+          if (!wait_or_abort(sh, &sh->s_full[br.stage], br.phase, limit, ctl)) goto mma_done;
           tc_fence_after();
           const uint64_t ad = adesc0 + uint64_t(uint32_t(ar.stage) * (a_bytes >> 4));
           const uint64_t bd = bdesc0 + uint64_t(uint32_t(br.stage) * (b_bytes >> 4));
@@ -867,8 +872,8 @@ __global__ void __launch_bounds__(352, 1)
         if (!wait_or_abort_cluster(sh, &sh->tmem_empty[0], (uint32_t(seg) & 1u) ^ 1u, limit, ctl)) goto mma_done;
         tc_fence_after();
         for (int c = c0; c < c1; ++c) {
-          if (!spin_or_abort<true>(sh, &sh->o_full[ar.stage], ar.phase, limit, ctl)) goto mma_done;
-          if (!spin_or_abort<true>(sh, &sh->s_full[br.stage], br.phase, limit, ctl)) goto mma_done;
+          if (!wait_or_abort_cluster(sh, &sh->o_full[ar.stage], ar.phase, limit, ctl)) goto mma_done;
+          if (!wait_or_abort_cluster(sh, &sh->s_full[br.stage], br.phase, limit, ctl)) goto mma_done;
           tc_fence_after();
           const uint64_t ad = adesc0 + uint64_t(uint32_t(ar.stage) * (a_bytes >> 4));
           const uint64_t bd = bdesc0 + uint64_t(uint32_t(br.stage) * (b_bytes >> 4));
