@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem + uint32_t(acc * kDgCols);
         for (int c = 0; c < P.kchunks; ++c) {
-          if (!wait_or_abort_cluster(sh, &sh->full[rg.stage], rg.phase, limit, ctl)) goto mma_done;
+          if (!spin_or_abort<true>(sh, &sh->full[rg.stage], rg.phase, limit, ctl)) goto mma_done;
           tc_fence_after();
           const uint64_t ad = adesc0 + uint64_t(uint32_t(rg.stage) * (kDgStageBytes >> 4));
           const uint64_t bd = bdesc0 + uint64_t(uint32_t(rg.stage) * (kDgStageBytes >> 4));

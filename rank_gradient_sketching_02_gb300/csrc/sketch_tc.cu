@@ -358,8 +358,8 @@ __global__ void __launch_bounds__(512, 1)
           if (!wait_or_abort(sh, &sh->tmem_empty[ab * T + t], uphase ^ 1u, limit, ctl)) goto mma_done;
         tc_fence_after();
         for (int c = c0; c < c1; ++c) {
-          if (!wait_or_abort(sh, &sh->s_full[xr.stage], xr.phase, limit, ctl)) goto mma_done;
-          if (!wait_or_abort(sh, &sh->o_full[gr.stage], gr.phase, limit, ctl)) goto mma_done;
+          if (!spin_or_abort<false>(sh, &sh->s_full[xr.stage], xr.phase, limit, ctl)) goto mma_done;
+          if (!spin_or_abort<false>(sh, &sh->o_full[gr.stage], gr.phase, limit, ctl)) goto mma_done;
           tc_fence_after();
           const uint64_t ad = xdesc0 + uint64_t(uint32_t(xr.stage) * (x_bytes >> 4));
           const uint64_t bd = gdesc0 + uint64_t(uint32_t(gr.stage) * (g_bytes >> 4));
@@ -653,8 +653,8 @@ __global__ void __launch_bounds__(352, 1)
           if (!wait_or_abort(sh, &sh->tmem_empty[ab * mblocks + m], uphase ^ 1u, limit, ctl)) goto mma_done;
         tc_fence_after();
         for (int c = c0; c < c1; ++c) {
-          if (!wait_or_abort(sh, &sh->o_full[ar.stage], ar.phase, limit, ctl)) goto mma_done;
-          if (!wait_or_abort(sh, &sh->s_full[br.stage], br.phase, limit, ctl)) goto mma_done;
+          if (!spin_or_abort<false>(sh, &sh->o_full[ar.stage], ar.phase, limit, ctl)) goto mma_done;
+          if (!spin_or_abort<false>(sh, &sh->s_full[br.stage], br.phase, limit, ctl)) goto mma_done;
           tc_fence_after();
           const uint64_t ad = adesc0 + uint64_t(uint32_t(ar.stage) * (a_bytes >> 4));
           const uint64_t bd = bdesc0 + uint64_t(uint32_t(br.stage) * (b_bytes >> 4));
@@ -872,8 +872,8 @@ __global__ void __launch_bounds__(352, 1)
         if (!wait_or_abort_cluster(sh, &sh->tmem_empty[0], (uint32_t(seg) & 1u) ^ 1u, limit, ctl)) goto mma_done;
         tc_fence_after();
         for (int c = c0; c < c1; ++c) {
-          if (!wait_or_abort_cluster(sh, &sh->o_full[ar.stage], ar.phase, limit, ctl)) goto mma_done;
-          if (!wait_or_abort_cluster(sh, &sh->s_full[br.stage], br.phase, limit, ctl)) goto mma_done;
+          if (!spin_or_abort<true>(sh, &sh->o_full[ar.stage], ar.phase, limit, ctl)) goto mma_done;
+          if (!spin_or_abort<true>(sh, &sh->s_full[br.stage], br.phase, limit, ctl)) goto mma_done;
           tc_fence_after();
           const uint64_t ad = adesc0 + uint64_t(uint32_t(ar.stage) * (a_bytes >> 4));
           const uint64_t bd = bdesc0 + uint64_t(uint32_t(br.stage) * (b_bytes >> 4));

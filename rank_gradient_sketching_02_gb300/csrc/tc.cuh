@@ -145,6 +145,43 @@ __device__ __forceinline__ bool wait_or_abort_cluster(SH* sh, uint64_t* bar, uin
   return true;
 }
 
+// try_wait with cluster-scope acquire and no suspend-time hint.
+__device__ __forceinline__ bool mbar_try_wait_cluster_nohint(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// wait_or_abort / wait_or_abort_cluster for the single MMA-issuing thread:
+// no suspend-time hint, so the thread resumes the moment its operands land
+// (a suspended issuer wakes late and leaves the tensor pipe idle).  Bounded
+// like the others: past `limit` it records LOGRA_ERR_TIMEOUT and raises the
+// CTA's abort flag; it also gives up once another role has raised it.
+template <bool kCluster, class SH>
+__device__ __forceinline__ bool spin_or_abort(SH* sh, uint64_t* bar, uint32_t parity, unsigned long long limit,
+                                              Control* ctl) {
+  auto ready = [&]() { return kCluster ? mbar_try_wait_cluster_nohint(bar, parity) : mbar_try_wait(bar, parity); };
+  if (ready()) return true;
+  const long long t0 = clock64();
+  for (unsigned n = 1;; ++n) {
+    if (ready()) return true;
+    if ((n & 63u) == 0) {
+      if (*reinterpret_cast<volatile int*>(&sh->abort)) return false;
+      if (static_cast<unsigned long long>(clock64() - t0) > limit) {
+        record_status(ctl, LOGRA_ERR_TIMEOUT);
+        *reinterpret_cast<volatile int*>(&sh->abort) = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // warp_wait for a barrier completed from the other CTA of a pair.
 template <class SH>
 __device__ __forceinline__ bool warp_wait_cluster(SH* sh, uint64_t* bar, uint32_t parity, unsigned long long limit,
