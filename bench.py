@@ -57,9 +57,9 @@ METRIC = "sketch TFLOP/s + fused RowAdam-apply GB/s per GB300; % of roofline"
 # (n, d, k, r) -> (bytes, what was captured).  Shapes without an entry report
 # null traffic.
 SKETCH_TRAFFIC_PER_CALL = {
-    # one stream: project 67.18 + 0.00 MB, split 8.40 + 0 MB, accumulate (CTA pairs) 338.2 + 8.5 MB
-    # (incl. re-zeroing P^T); under the concurrency hint the call moves 397.2 MB (no split, X read once)
-    (8192, 18944, 3584, 256): (422.3e6, "ncu dram__bytes_read.sum + dram__bytes_write.sum of the three launches "
+    # one stream: project 67.18 + 0.00 MB, split 8.40 + 0 MB, accumulate (CTA pairs) 338.2 + 8.6 MB
+    # (incl. re-zeroing P^T); under the concurrency hint the call moves 397.1 MB (no split, X read once)
+    (8192, 18944, 3584, 256): (422.4e6, "ncu dram__bytes_read.sum + dram__bytes_write.sum of the three launches "
                                         "of one 18944x3584 gate call on one stream, kernels as they stand"),
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
