@@ -71,7 +71,11 @@ struct ApplyShared {
 constexpr size_t kApplySmem = 1024 + kAbStages * (kABytes + kBBytes) + kWStages * kWBytes + 2 * kWBytes + 2 * kHBytes +
                               sizeof(ApplyShared) + 64;
 
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// Named barrier of the eight epilogue warps (warp-aligned, so reconverged first).
+__device__ __forceinline__ void epi_sync() {
+  __syncwarp();
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
@@ -184,7 +188,7 @@ __global__ void __launch_bounds__(480, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   tc_fence_after();
   const uint32_t tmem = sh->tmem_base;
   grid_dependency_wait();      // the S image, Gram image and row factors come from the launches before
@@ -578,7 +582,7 @@ __global__ void __launch_bounds__(480, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -664,7 +668,7 @@ __device__ __forceinline__ void gram_block(uint64_t key, int r, int nw, int64_t 
       }
       (side ? wb : wa)[rr][w] = v;
     }
-    __syncthreads();
+    cta_sync();
     int diff[4] = {0, 0, 0, 0};
     for (int w = 0; w < nwr; ++w) {
       const uint64_t x = wb[tx][w];
@@ -681,9 +685,9 @@ __device__ __forceinline__ void gram_block(uint64_t key, int r, int nw, int64_t 
         if (a < r && b < r && diff[q]) atomicAdd(&counts[a * r + b], diff[q]);
       }
       __threadfence();
-      __syncthreads();
+      cta_sync();
       if (threadIdx.x == 0) last = (atomicInc(&arrivals[by * gx + bx], gz - 1) == gz - 1) ? 1u : 0u;
-      __syncthreads();
+      cta_sync();
       if (!last) return;
       __threadfence();
       // the tile's counts, read back and left at zero
@@ -697,7 +701,7 @@ __device__ __forceinline__ void gram_block(uint64_t key, int r, int nw, int64_t 
         cnt[e / 32][e % 32] = v;
       }
     }
-    __syncthreads();
+    cta_sync();
   } else if (bz != 0) {
     return;                                                   // padding tiles: block z = 0 writes the zeros
   }

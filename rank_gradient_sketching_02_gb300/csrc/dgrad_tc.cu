@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(192, 1)
     tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = sh->tmem_base;
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(192, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   cluster_sync();              // the leader's MMAs are done with this CTA's memory; no more signals
   if (warp == 1) {
     tc_fence_after();

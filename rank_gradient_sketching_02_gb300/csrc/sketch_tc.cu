@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(512, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   tc_fence_after();
   const uint32_t tmem = sh->tmem_base;
   grid_dependency_wait();      // the previous call's kernels still use P^T until they complete
@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(512, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, tmem_cols);
@@ -588,7 +588,7 @@ __global__ void __launch_bounds__(352, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   tc_fence_after();
   const uint32_t tmem = sh->tmem_base;
   grid_dependency_wait();      // the image comes from the split just before, S from earlier calls
@@ -730,7 +730,7 @@ __global__ void __launch_bounds__(352, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, tmem_cols);
@@ -804,7 +804,7 @@ __global__ void __launch_bounds__(352, 1)
     tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = sh->tmem_base;
@@ -948,7 +948,7 @@ __global__ void __launch_bounds__(352, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   cluster_sync();              // the leader's MMAs are done with this CTA's memory; no more signals
   if (warp == 1) {
     tc_fence_after();
