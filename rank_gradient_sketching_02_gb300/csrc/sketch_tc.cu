@@ -192,21 +192,25 @@ __device__ __forceinline__ void gen_sigma_kmajor(uint8_t* tile, const uint2* nib
 }
 
 // Direct image drain of one segment's accumulators (whole k range): this
-// warp's 32 tokens of token tile t are one 32-token image chunk; per 32-rank
-// block a 4 KB tile of 32 rows (hi bf16 of the 32 tokens at bytes 0..63, lo at
-// 64..127, 16-byte chunk q at q ^ (row & 7)) goes out by one bulk copy.  Rows
-// from r up to r_pad are zero.  Lanes pair up: the even lane stores the hi
-// word of tokens (t, t + 1), the odd lane the lo word.  Only the blocks
-// b = t * (r_pad / 32) + j0 / 32 with b % nslots == slot are drained, so that
-// several warps of one TMEM lane quadrant can share the work.  `stg` holds two
-// 4 KB staging tiles; `sb` alternates between them.
+// warp's 32 tokens of token tile t are one 32-token image chunk, whose rows
+// (one per rank: hi bf16 of the 32 tokens at bytes 0..63, lo at 64..127,
+// 16-byte chunk q at q ^ (row & 7)) go straight from registers to global
+// memory.  Lane = token; two ranks at a time, lanes exchange with their
+// neighbour so that the even lane stores the hi and lo words of tokens
+// (t, t + 1) for the first rank and the odd lane those for the second: each
+// warp store fills half of two 128-byte rows, whole sectors.  Rows from r up to
+// r_pad are zero.  Only the blocks b = t * (r_pad / 32) + j0 / 32 with
+// b % nslots == slot are drained, so that several warps of one TMEM lane
+// quadrant can share the work.  The image is read by the accumulate's bulk
+// copies in a later kernel.
 __device__ __forceinline__ void drain_image_blocks(uint32_t acc_tile0, uint32_t acc_cols, int T, int quad, int grp,
-                                                   const SketchShape& P, uint8_t* __restrict__ image, uint8_t* stg,
-                                                   int& sb, int slot, int nslots, int lane) {
+                                                   const SketchShape& P, uint8_t* __restrict__ image, int slot,
+                                                   int nslots, int lane) {
   const int nchunk32 = P.n_pad / kChunk;
   const int t2 = lane & ~1;
-  const bool odd = lane & 1;
+  const int odd = lane & 1;
   const int nb = P.r_pad / 32;
+  const uint32_t hi_q = uint32_t(t2 >> 3), lo_q = 4u + uint32_t(t2 >> 3), in_q = uint32_t(t2 & 7) << 1;
   for (int t = 0; t < T; ++t) {
     const uint32_t acc = acc_tile0 + uint32_t(t) * acc_cols + (uint32_t(quad * 32) << 16);
     const int ci = ((grp * T + t) * kTok + quad * 32) / kChunk;
@@ -222,27 +226,24 @@ __device__ __forceinline__ void drain_image_blocks(uint32_t acc_tile0, uint32_t 
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = 0u;
       }
-      uint8_t* tile = stg + sb * kStageTile;
+      uint8_t* rows = image + (size_t(ci) * P.r_pad + j0) * 128;
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const float p = __uint_as_float(v[jj]);
-        const __nv_bfloat16 h = __float2bfloat16_rn(p);
-        const __nv_bfloat16 l = __float2bfloat16_rn(p - __bfloat162float(h));
-        const uint32_t hu = __bfloat16_as_ushort(h), lu = __bfloat16_as_ushort(l);
-        const uint32_t other = __shfl_xor_sync(0xffffffffu, odd ? hu : lu, 1);
-        const uint32_t word = odd ? (other | (lu << 16)) : (hu | (other << 16));
-        const int q = (odd ? 4 : 0) + (t2 >> 3);
-        *reinterpret_cast<uint32_t*>(tile + jj * 128 + ((q ^ (jj & 7)) << 4) + ((t2 & 7) << 1)) = word;
+      for (int jj = 0; jj < 32; jj += 2) {
+        const float p0 = __uint_as_float(v[jj]), p1 = __uint_as_float(v[jj + 1]);
+        const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);             // .x = rank jj, .y = rank jj + 1
+        const uint32_t hu = *reinterpret_cast<const uint32_t*>(&h);
+        const __nv_bfloat162 l = __floats2bfloat162_rn(p0 - __uint_as_float(hu << 16),
+                                                       p1 - __uint_as_float(hu & 0xFFFF0000u));
+        const uint32_t lu = *reinterpret_cast<const uint32_t*>(&l);
+        const uint32_t oh = __shfl_xor_sync(0xffffffffu, hu, 1), ol = __shfl_xor_sync(0xffffffffu, lu, 1);
+        // even lane: rank jj of tokens (t2, t2 + 1); odd lane: rank jj + 1 of the same tokens
+        const uint32_t wh = odd ? __byte_perm(oh, hu, 0x7632) : __byte_perm(hu, oh, 0x5410);
+        const uint32_t wl = odd ? __byte_perm(ol, lu, 0x7632) : __byte_perm(lu, ol, 0x5410);
+        const uint32_t row = uint32_t(jj + odd);
+        uint8_t* rp = rows + row * 128u + in_q;
+        *reinterpret_cast<uint32_t*>(rp + ((hi_q ^ (row & 7u)) << 4)) = wh;
+        *reinterpret_cast<uint32_t*>(rp + ((lo_q ^ (row & 7u)) << 4)) = wl;
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        bulk_store(image + (size_t(ci) * P.r_pad + j0) * 128, tile, kStageTile);
-        bulk_commit();
-        bulk_wait_read_1();      // the other staging tile is free again
-      }
-      __syncwarp();
-      sb ^= 1;
     }
   }
 }
@@ -279,9 +280,8 @@ __global__ void __launch_bounds__(512, 1)
   while (tmem_cols < acc_cols * uint32_t(T * nacc)) tmem_cols <<= 1;
   const int64_t total = int64_t(P.groups) * P.nchunks;
   // The image drain of a CTA's only segment is shared by 12 warps (3 per TMEM
-  // lane quadrant: the epilogue warp and two of warps 6..13, free by then) when
-  // the X ring, idle after the last MMA, can hold their 8 KB of staging each.
-  const bool extra_drain = P.direct && uint32_t(XS) * x_bytes >= 8u * 2u * kStageTile;
+  // lane quadrant: the epilogue warp and two of warps 6..13, free by then).
+  const bool extra_drain = P.direct;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < XS; ++s) {
@@ -401,13 +401,8 @@ __global__ void __launch_bounds__(512, 1)
         SegIter peek = it;
         int g2, d0, d1;
         const bool only = seg == 0 && !peek.next(g2, d0, d1);
-        uint8_t* stg8 = reinterpret_cast<uint8_t*>(stg);
-        if (only && extra_drain)
-          drain_image_blocks(tmem + uint32_t(ab * T) * acc_cols, acc_cols, T, quad, grp, P, image, stg8, sb, 0, 3,
-                             lane);
-        else
-          drain_image_blocks(tmem + uint32_t(ab * T) * acc_cols, acc_cols, T, quad, grp, P, image, stg8, sb, 0, 1,
-                             lane);
+        drain_image_blocks(tmem + uint32_t(ab * T) * acc_cols, acc_cols, T, quad, grp, P, image, 0,
+                           (only && extra_drain) ? 3 : 1, lane);
         tc_fence_before();
         __syncwarp();
         if (lane == 0)
@@ -480,14 +475,10 @@ __global__ void __launch_bounds__(512, 1)
         const uint32_t uphase = 0u;
         if (warp_wait(sh, &sh->tmem_full[ab], uphase, limit, ctl)) {
           tc_fence_after();
-          uint8_t* stg8 = x_tiles + size_t(warp - 6) * 2 * kStageTile;
-          int sb = 0;
-          drain_image_blocks(tmem + uint32_t(ab * T) * acc_cols, acc_cols, T, warp & 3, fg, P, image, stg8, sb,
+          drain_image_blocks(tmem + uint32_t(ab * T) * acc_cols, acc_cols, T, warp & 3, fg, P, image,
                              warp < 10 ? 1 : 2, 3, lane);
           tc_fence_before();
         }
-        if (lane == 0) bulk_wait_all();
-        __syncwarp();
       }
     }
   }
