@@ -5,7 +5,9 @@
 //             generated sign tile; A = X tile by TMA, B = Sigma tile generated
 //             in shared memory from the sign hash); segments covering a whole
 //             k range store, the others reduce-add into the P^T buffer (kept
-//             at zero between calls)
+//             at zero between calls); when every segment covers a whole k
+//             range the epilogue writes the split's image itself and the
+//             split is not launched
 //   split     P^T stored as a two-term bf16 expansion P^T = hi + lo, written
 //             pre-swizzled in 32-token chunks so the next kernel loads one
 //             chunk with a single bulk copy
@@ -253,7 +255,9 @@ __device__ __forceinline__ void drain_image_blocks(uint32_t acc_tile0, uint32_t 
 // generation cost per MMA falls with the group size.  The epilogue stages
 // 32 x 32 fp32 tiles in shared memory and hands them to TMA: a plain tensor
 // store when the segment covers the whole k range, else a tensor reduce-add
-// (performed by the TMA unit and L2) into the zeroed P^T buffer.  When two
+// (performed by the TMA unit and L2) into the zeroed P^T buffer; when every
+// segment covers a whole k range (P.direct) it stores the accumulate's hi/lo
+// image rows from registers instead (drain_image_blocks).  When two
 // groups' accumulators fit TMEM together, consecutive segments alternate
 // between them, so the drain of one overlaps the MMAs of the next.
 __global__ void __launch_bounds__(512, 1)
@@ -382,7 +386,7 @@ __global__ void __launch_bounds__(512, 1)
       mbar_wait(&sh->drain, 0, limit);
     }
   } else if (warp < 6) {
-    // ---------------------------------------------------------------- epilogue: TMEM -> smem -> TMA into P^T
+    // ---------------------------------------------------------------- epilogue: TMEM -> P^T (smem + TMA) or image
     const int quad = warp & 3;
     float* stg = reinterpret_cast<float*>(staging + (warp - 2) * 2 * kStageTile);
     int sb = 0;
