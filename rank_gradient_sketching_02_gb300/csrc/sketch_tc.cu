@@ -121,15 +121,18 @@ struct SegIter {
 // 256 KB, so the field never carries), inside fully unrolled bodies.
 
 // Projection, one k chunk: T token tiles x NP parts of r, kKc / 16 k steps.
+// Each accumulator takes its k steps back to back: a single-CTA MMA stream
+// into one accumulator runs at ~7550 FLOP/clk (M128 N256 K16), one that
+// alternates between two accumulators at ~6540.
 template <int T, int NP>
 __device__ __forceinline__ void project_chunk_mmas(uint32_t acc0, uint32_t acc_cols, uint32_t npart, uint64_t ad,
                                                    uint64_t bd, uint32_t idesc, uint32_t first) {
 #pragma unroll
-  for (int ks = 0; ks < kKc / 16; ++ks)
+  for (int t = 0; t < T; ++t)
 #pragma unroll
-    for (int t = 0; t < T; ++t)
+    for (int p = 0; p < NP; ++p)
 #pragma unroll
-      for (int p = 0; p < NP; ++p)
+      for (int ks = 0; ks < kKc / 16; ++ks)
         mma_bf16(acc0 + uint32_t(t) * acc_cols + uint32_t(p) * npart,
                  ad + uint64_t(t * ((kTok * 128) >> 4) + 2 * ks), bd + uint64_t(p * (npart * 8) + 2 * ks), idesc,
                  ks ? 1u : first);
@@ -140,15 +143,14 @@ template <int MB>
 __device__ __forceinline__ void accumulate_chunk_mmas(uint32_t acc0, uint32_t N, uint64_t ad, uint64_t bd,
                                                       uint32_t idesc, uint32_t first) {
 #pragma unroll
-  for (int ks = 0; ks < kChunk / 16; ++ks) {
-    const uint64_t bk = bd + uint64_t(ks * (2048 >> 4));
+  for (int m = 0; m < MB; ++m)
 #pragma unroll
-    for (int m = 0; m < MB; ++m) {
+    for (int ks = 0; ks < kChunk / 16; ++ks) {
+      const uint64_t bk = bd + uint64_t(ks * (2048 >> 4));
       const uint64_t am = ad + uint64_t(m * ((128 * 128) >> 4) + 2 * ks);
       mma_bf16(acc0 + uint32_t(m) * N, am, bk, idesc, ks ? 1u : first);
       mma_bf16(acc0 + uint32_t(m) * N, am + 4, bk, idesc, 1u);   // lo term: bytes 64..127 of each row
     }
-  }
 }
 
 // Accumulate on a CTA pair, one token chunk: RB rank blocks x DB d blocks of
@@ -159,13 +161,13 @@ template <int RB, int DB>
 __device__ __forceinline__ void accumulate_pair_mmas(uint32_t tmem, uint64_t ad, uint64_t bd, uint32_t idesc,
                                                      uint32_t first) {
 #pragma unroll
-  for (int ks = 0; ks < kChunk / 16; ++ks)
+  for (int rb = 0; rb < RB; ++rb)
 #pragma unroll
-    for (int rb = 0; rb < RB; ++rb) {
-      const uint64_t am = ad + uint64_t(rb * (16384 >> 4) + 2 * ks);
+    for (int db = 0; db < DB; ++db) {
+      const uint32_t acc = tmem + uint32_t((rb * DB + db) * 256);
 #pragma unroll
-      for (int db = 0; db < DB; ++db) {
-        const uint32_t acc = tmem + uint32_t((rb * DB + db) * 256);
+      for (int ks = 0; ks < kChunk / 16; ++ks) {
+        const uint64_t am = ad + uint64_t(rb * (16384 >> 4) + 2 * ks);
         const uint64_t bk = bd + uint64_t(db * ((2 * kChunk * 128) >> 4) + ks * (2048 >> 4));
         mma_bf16_pair(acc, am, bk, idesc, ks ? 1u : first);
         mma_bf16_pair(acc, am + 4, bk, idesc, 1u);     // lo term: bytes 64..127 of each row
@@ -327,7 +329,7 @@ __global__ void __launch_bounds__(512, 1)
       SegIter it(total, P.nchunks);
       while (it.next(grp, c0, c1)) {
         for (int c = c0; c < c1; ++c) {
-          if (!wait_or_abort(sh, &sh->s_empty[xr.stage], xr.phase ^ 1u, limit, ctl)) goto producer_done;
+          if (!spin_or_abort<false>(sh, &sh->s_empty[xr.stage], xr.phase ^ 1u, limit, ctl)) goto producer_done;
           if (inject) {
             inject = 0;                      // test hook: this CTA's first stage never fills
           } else {
@@ -454,7 +456,9 @@ __global__ void __launch_bounds__(512, 1)
       SegIter it(total, P.nchunks);
       while (it.next(grp, c0, c1)) {
         for (int c = c0; c < c1; ++c) {
-          if (!warp_wait(sh, &sh->o_empty[gr.stage], gr.phase ^ 1u, limit, ctl)) goto gen_done;
+          // polling: a generator that sleeps through the stage's release delays the MMAs
+          // (the down projection under the hint 327 -> 309 us)
+          if (!warp_spin_wait(sh, &sh->o_empty[gr.stage], gr.phase ^ 1u, limit, ctl)) goto gen_done;
           gen_sigma_kmajor(g_tiles + size_t(gr.stage) * g_bytes, sh->nib, key, P.r, c, gtid, 256);
           fence_proxy_async_smem();
           __syncwarp();

@@ -183,6 +183,19 @@ __device__ __forceinline__ bool spin_or_abort(SH* sh, uint64_t* bar, uint32_t pa
 }
 
 // warp_wait for a barrier completed from the other CTA of a pair.
+// warp_wait with a polling lane 0 (spin_or_abort): for producers whose
+// stage must be refilled the moment the MMAs release it (a suspended thread
+// wakes late).  Every lane then observes the phase itself.
+template <class SH>
+__device__ __forceinline__ bool warp_spin_wait(SH* sh, uint64_t* bar, uint32_t parity, unsigned long long limit,
+                                               Control* ctl) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = spin_or_abort<false>(sh, bar, parity, limit, ctl) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) (void)mbar_try_wait(bar, parity);
+  return ok != 0;
+}
+
 template <class SH>
 __device__ __forceinline__ bool warp_wait_cluster(SH* sh, uint64_t* bar, uint32_t parity, unsigned long long limit,
                                                   Control* ctl) {
