@@ -72,7 +72,7 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--workload", default="model7b")
-    p.add_argument("--rank", type=int, default=256)
+    p.add_argument("--rank", type=int, default=None, help="sketch rank r (default: the workload's)")
     p.add_argument("--layers", type=int, default=None, help="override the workload's layer count")
     p.add_argument("--microbatches", type=int, default=None,
                    help="override the workload's microbatches per step (small profiling cases)")
@@ -251,7 +251,7 @@ def run_reference(args):
         return 0
     from rank_gradient_sketching_02_gb300 import synth
     w = synth.WORKLOADS[args.workload]
-    r = args.rank
+    r = args.rank or w.r
     layers = args.layers or w.layers
     pool = layers if args.input_layers <= 0 else min(layers, args.input_layers)
     per_step = max(2.0, args.cpu_seconds / 2)
@@ -295,7 +295,7 @@ def run_ours(args):
     from rank_gradient_sketching_02_gb300 import dp, synth
 
     w = synth.WORKLOADS[args.workload]
-    r = args.rank
+    r = args.rank or w.r
     layers = args.layers or w.layers
     n, nmb = w.tokens, args.microbatches or w.microbatches
     dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32

@@ -105,12 +105,20 @@ int logra_sign_matrix(uint64_t seed, uint64_t step, int r, int64_t k,
  *   S        d x r fp32, read and written in place (the caller zeroes it at
  *            the first microbatch of a step)
  *   seed     per-matrix seed; step  the optimiser step (A is redrawn per step)
- * Padding tokens are zero rows of X and dY.  bf16 inputs are multiplied
- * exactly and accumulated in fp32; the X A^T intermediate is kept as a
- * two-term bf16 expansion (relative error about 2^-16), fp32 inputs run in fp32.
+ * Padding tokens are zero rows of X and dY; n is at most 2^28
+ * (LOGRA_ERR_UNSUPPORTED above).  bf16 inputs are multiplied exactly and
+ * accumulated in fp32; the X A^T intermediate is kept as a two-term bf16
+ * expansion (relative error about 2^-16).  fp32 inputs run on the same
+ * tensor-core kernels: each element is split into two bf16 terms
+ * x = x1 + x2 (|x - x1 - x2| <= 2^-18 |x|, the two-term bf16 splitting of
+ * Henry, Tang & Heinecke, ARITH 2019), the planes are stacked along the
+ * tokens as X' = [X1; X2; X1; X2], dY' = [dY1; dY1; dY2; dY2], and the bf16
+ * sketch of those 4n tokens adds all four cross terms; fp32 inputs must be
+ * finite and below bf16's largest finite value (about 3.39e38).
  * Uses the internal workspace: for bf16 inputs about 8 * r * n bytes (an fp32
  * P^T buffer and the two-term bf16 image the accumulate reads;
- * logra_sketch_workspace_bytes gives the exact figure), r * n * 4 for fp32.
+ * logra_sketch_workspace_bytes gives the exact figure); for fp32 inputs the
+ * same for 4n tokens plus 8 * n * (k + d) bytes of stacked planes.
  * S is updated with atomic fp32 additions, so calls that add into the same S
  * (different microbatches of one step) may run concurrently on different
  * streams; the sum is then formed in an unspecified order.
@@ -163,7 +171,7 @@ typedef struct logra_sketch_item {
  * group call of the largest shapes before capturing groups into a CUDA graph,
  * which records the fork and join like any other).  Every item is checked
  * before anything is launched; a failing launch still joins what was issued.
- * count == 0 or n == 0 is a no-op.
+ * count == 0 or n == 0 is a no-op; n above 2^28 is LOGRA_ERR_UNSUPPORTED.
  */
 int logra_sketch_accumulate_group(const logra_sketch_item* items, int count,
                                   int64_t n, int r, uint64_t step,
@@ -188,7 +196,7 @@ int logra_sketch_accumulate_group(const logra_sketch_item* items, int count,
  *       with the same result) as logra_sketch_accumulate.  NULL: dX only
  *       (X, r, seed and step are then not used).
  * dX and S must not both be NULL (LOGRA_ERR_INVALID_ARG); n must be below
- * 2^31 (LOGRA_ERR_UNSUPPORTED).  Launches, in this order on `stream`: one
+ * 2^31, and at most 2^28 when S is given (LOGRA_ERR_UNSUPPORTED).  Launches, in this order on `stream`: one
  * persistent tensor-core kernel for dX (tcgen05 on CTA pairs, 256 x 256
  * output tiles taken from a per-stream tile counter), then the sketch's
  * launches.  dX comes first because the layer below waits for it, the sketch

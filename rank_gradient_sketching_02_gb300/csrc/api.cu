@@ -256,7 +256,7 @@ const char* logra_status_string(int status) {
 
 int logra_last_cuda_error(void) { return t_last_cuda_error; }
 
-int logra_version(void) { return (1 << 16) | 0; }
+int logra_version(void) { return (1 << 16) | 1; }
 
 uint64_t logra_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -266,10 +266,26 @@ int logra_sign_matrix(uint64_t seed, uint64_t step, int r, int64_t k, float* A_o
   return launch_sign_matrix(step_key(seed, step), r, k, inv_sqrt_r(r), A_out, stream);
 }
 
+// Largest token count of one sketch call (the fp32 path runs the bf16 kernels on 4n stacked tokens).
+constexpr int64_t kMaxSketchTokens = int64_t(1) << 28;
+
+// fp32 sketch workspace: the bf16 sketch's scratch for 4n tokens, then the
+// stacked bf16 planes of X (4n x k) and dY (4n x d).
+struct F32SketchLayout {
+  size_t x_off, y_off, bytes;
+};
+static F32SketchLayout f32_sketch_layout(int64_t n, int64_t d, int64_t k, int r) {
+  F32SketchLayout L;
+  L.x_off = (sketch_tc_workspace_bytes(4 * n, d, k, r, sm_count()) + 255) & ~size_t(255);
+  L.y_off = L.x_off + ((size_t(8) * size_t(n) * size_t(k) + 255) & ~size_t(255));
+  L.bytes = L.y_off + size_t(8) * size_t(n) * size_t(d);
+  return L;
+}
+
 size_t logra_sketch_workspace_bytes(int64_t n, int64_t d, int64_t k, int r, int in_dtype) {
-  if (n <= 0 || r <= 0 || d <= 0 || k <= 0) return 0;
+  if (n <= 0 || r <= 0 || d <= 0 || k <= 0 || n > kMaxSketchTokens) return 0;
   if (in_dtype == LOGRA_BF16) return sketch_tc_workspace_bytes(n, d, k, r, sm_count());
-  return size_t(n) * size_t(r) * 4;
+  return f32_sketch_layout(n, d, k, r).bytes;
 }
 
 size_t logra_apply_workspace_bytes(int64_t d, int64_t k, int r) {
@@ -302,20 +318,28 @@ int logra_sketch_accumulate(const void* X, const void* dY, int in_dtype, int64_t
   if (int st = check_mat(d, k)) return st;
   if (check_rank(r)) return LOGRA_ERR_UNSUPPORTED;
   if (n == 0) return LOGRA_OK;
+  if (n > kMaxSketchTokens) return LOGRA_ERR_UNSUPPORTED;
   if (!X || !dY) return LOGRA_ERR_INVALID_ARG;
   if (!aligned16(X) || !aligned16(dY) || !aligned16(S)) return LOGRA_ERR_UNSUPPORTED;
   int st;
   ZeroTrack* zero = nullptr;
   void* ws = workspace(stream, logra_sketch_workspace_bytes(n, d, k, r, in_dtype), &st, &zero);
   if (st) return st;
-  if (in_dtype == LOGRA_BF16) {
-    Control* ctl = control_block(&st);
-    if (!ctl) return st;
+  Control* ctl = control_block(&st);
+  if (!ctl) return st;
+  if (in_dtype == LOGRA_BF16)
     return launch_sketch_tc(X, dY, n, d, k, r, step_key(seed, step), inv_sqrt_r(r), S, ws, zero, ctl, stream);
-  }
-  zero->bytes.store(0);           // the fp32 path keeps its P in the workspace
-  return launch_sketch_simt(X, dY, in_dtype, n, d, k, r, step_key(seed, step), inv_sqrt_r(r), S,
-                            static_cast<float*>(ws), stream);
+  // fp32: the bf16 planes of X and dY stacked along the tokens, then the bf16
+  // sketch of the 4n stacked tokens.  The planes lie past that sketch's own
+  // scratch, so nothing from their offset on stays known to be zero.
+  const F32SketchLayout F = f32_sketch_layout(n, d, k, r);
+  char* base = static_cast<char*>(ws);
+  if (zero->bytes.load() > F.x_off) zero->bytes.store(F.x_off);
+  if (int e = launch_f32_planes(static_cast<const float*>(X), static_cast<const float*>(dY), n, d, k,
+                                base + F.x_off, base + F.y_off, stream))
+    return e;
+  return launch_sketch_tc(base + F.x_off, base + F.y_off, 4 * n, d, k, r, step_key(seed, step), inv_sqrt_r(r), S,
+                          ws, zero, ctl, stream);
 }
 
 // Side streams of the grouped sketch, per device: created on first use and kept.
@@ -351,7 +375,7 @@ int side_streams(SideStreams** out) {
 int logra_sketch_accumulate_group(const logra_sketch_item* items, int count, int64_t n, int r, uint64_t step,
                                   logra_stream_t stream) {
   if (count < 0 || (count > 0 && !items) || n < 0) return LOGRA_ERR_INVALID_ARG;
-  if (check_rank(r)) return LOGRA_ERR_UNSUPPORTED;
+  if (check_rank(r) || n > kMaxSketchTokens) return LOGRA_ERR_UNSUPPORTED;
   for (int i = 0; i < count; ++i) {
     const logra_sketch_item& it = items[i];
     if (!it.S) return LOGRA_ERR_INVALID_ARG;
@@ -388,7 +412,7 @@ int logra_linear_backward(const void* X, const void* dY, const void* W, void* dX
   if (n < 0 || (!dX && !S)) return LOGRA_ERR_INVALID_ARG;
   if (int st = check_mat(d, k)) return st;
   if (S && check_rank(r)) return LOGRA_ERR_UNSUPPORTED;
-  if (n > int64_t(INT32_MAX)) return LOGRA_ERR_UNSUPPORTED;
+  if (n > int64_t(INT32_MAX) || (S && n > kMaxSketchTokens)) return LOGRA_ERR_UNSUPPORTED;
   if (n == 0) return LOGRA_OK;
   if (!dY || (dX && !W) || (S && !X)) return LOGRA_ERR_INVALID_ARG;
   if (!aligned16(dY) || (dX && (!aligned16(dX) || !aligned16(W))) || (S && (!aligned16(X) || !aligned16(S))))

@@ -20,8 +20,10 @@ int launch_sign_matrix(uint64_t key, int r, int64_t k, float scale, float* A, cu
 size_t gram_image_bytes(int r);
 
 
-int launch_sketch_simt(const void* X, const void* dY, int dtype, int64_t n, int64_t d, int64_t k, int r,
-                       uint64_t key, float scale, float* S, float* P, cudaStream_t s);
+// fp32 X (n x k) and dY (n x d) -> bf16 planes Xp = [X1; X2; X1; X2] (4n x k) and
+// dYp = [dY1; dY1; dY2; dY2] (4n x d), x = x1 + x2 the two-term bf16 split.
+int launch_f32_planes(const float* X, const float* dY, int64_t n, int64_t d, int64_t k, void* Xp, void* dYp,
+                      cudaStream_t s);
 
 size_t sketch_tc_workspace_bytes(int64_t n, int64_t d, int64_t k, int r, int sms);
 struct ZeroTrack;

@@ -46,7 +46,10 @@ def test_host_only_calls(lib):
         assert lib.logra_status_string(st)
     assert lib.logra_status_string(99) == b"unknown status"
     assert lib.logra_sketch_workspace_bytes(8192, 1536, 1536, 256, 1) >= 8192 * 256 * 4
-    assert lib.logra_sketch_workspace_bytes(8192, 1536, 1536, 256, 0) == 8192 * 256 * 4
+    # fp32: the bf16 scratch of the 4n stacked tokens, then the stacked bf16 planes of X and dY
+    assert (lib.logra_sketch_workspace_bytes(8192, 1536, 1536, 256, 0)
+            >= lib.logra_sketch_workspace_bytes(4 * 8192, 1536, 1536, 256, 1) + 8 * 8192 * (1536 + 1536))
+    assert lib.logra_sketch_workspace_bytes((1 << 28) + 1, 8, 8, 32, 1) == 0
     assert lib.logra_sketch_workspace_bytes(0, 8, 8, 32, 1) == 0
     assert lib.logra_apply_workspace_bytes(1536, 1536, 256) > 0
 

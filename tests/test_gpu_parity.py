@@ -125,6 +125,18 @@ def test_sketch_fp32_ragged(L, n, d, k, r):
     assert rel(S, S_or) <= TOL_S_F32
 
 
+@pytest.mark.parametrize("n,d,k,r", [(777, 1032, 520, 256), (300, 264, 1032, 512), (129, 4104, 136, 128),
+                                     (1000, 1536, 1536, 384)])
+def test_sketch_fp32_tensor_core_shapes(L, n, d, k, r):
+    """fp32 inputs through the stacked bf16 planes on both accumulate kernels (CTA pairs at
+    r = 256 and 512, one CTA otherwise), with the lognormal gradient scales: dropping the
+    second plane of X or dY would leave an error near 1e-3, a hundred times the bound."""
+    mbs = [synth.host_microbatch(n, d, k, dy_kind="lognormal", mask_frac=0.25, key=(8, n, d, k, r, mb))[:2]
+           for mb in range(2)]
+    S, S_or = run_sketch(L, mbs, d, r, "f32", 11, 4)
+    assert rel(S, S_or) <= TOL_S_F32
+
+
 def test_sketch_n0_is_noop_and_padding_rows(L):
     import torch
     d, k, r = 64, 128, 32
