@@ -23,7 +23,7 @@ workloads remain available.  The metric is sketch TFLOP/s over the whole step (a
 sketch FLOPs 2 n r (k + d) per matrix-microbatch, divided by the step time
 including the apply), with the apply's GB/s and both kernels' roofline
 fractions alongside.  The matrices are independent, so the step issues them
-round robin on --streams CUDA streams (default 8); per-call durations (the
+round robin on --streams CUDA streams (default 16); per-call durations (the
 components and the dominant call's roofline) come from one extra step on a
 single stream right after the timed region; the apply component also reports all of a
 step's apply calls issued at once on up to --apply-streams streams (default 7), and
@@ -79,7 +79,7 @@ def parse_args(argv=None):
     p.add_argument("--input-layers", type=int, default=4,
                    help="distinct layers of resident inputs; layer l reads the inputs of slot l mod this "
                         "(0: every layer its own inputs)")
-    p.add_argument("--streams", type=int, default=8,
+    p.add_argument("--streams", type=int, default=16,
                    help="CUDA streams the matrices are issued on, round robin (each keeps its own workspace)")
     p.add_argument("--apply-streams", type=int, default=7,
                    help="streams for the all-applies-at-once measurement (each with its own workspace)")
@@ -311,6 +311,10 @@ def run_ours(args):
     mats = []
     x_inputs, dy_inputs = {}, {}
     gen_ms = 0.0
+    # each layer's sketches are views of one buffer (dp.SketchArena): zeroed and, under torchrun,
+    # summed over the ranks as one collective per layer
+    arenas = [dp.SketchArena([d for _, d, _ in w.matrices], r, device=dev, bucket_bytes=1 << 62)
+              for _ in range(layers)]
     for layer in range(layers):
         for mi, (name, d, k) in enumerate(w.matrices):
             gen = torch.Generator(device=dev)
@@ -338,7 +342,7 @@ def run_ours(args):
             gen_ms += g0.elapsed_time(g1)
             m = {"name": name, "layer": layer, "d": d, "k": k, "seed": synth.matrix_seed(2026, layer, mi), "W": W,
                  "Wb": W.to(torch.bfloat16), "v": torch.zeros(d, dtype=torch.float32, device=dev),
-                 "S": torch.zeros((d, r), dtype=torch.float32, device=dev),
+                 "S": arenas[layer][mi], "arena": arenas[layer],
                  "norms": torch.zeros(2, dtype=torch.float64, device=dev),
                  "group": grp, "X": x_inputs[(ls, grp)], "dY": dy_inputs[(ls, mi)]}
             mats.append(m)
@@ -420,8 +424,8 @@ def run_ours(args):
                             st.wait_stream(smb)
                     i += 1
                     with torch.cuda.stream(st):
-                        dp.allreduce_sketch(m["S"])
                         if args.apply_mode == "single":
+                            dp.allreduce_sketch(m["S"])
                             L.logra_rowadam_apply_ex(m["W"], m["S"], m["v"], m["seed"], step_idx, beta2, eps, lr,
                                                      c, m["norms"], m["Wb"], None)
                     continue
@@ -431,8 +435,8 @@ def run_ours(args):
                     for mb in range(nmb):
                         timed(ev, "sketch", st, lambda: L.logra_sketch_accumulate(
                             m["X"][mb], m["dY"][mb], m["S"], m["seed"], step_idx), m["d"], m["k"])
-                    dp.allreduce_sketch(m["S"])
                     if args.apply_mode == "single":
+                        dp.allreduce_sketch(m["S"])
                         timed(ev, "apply", st, lambda: L.logra_rowadam_apply_ex(
                             m["W"], m["S"], m["v"], m["seed"], step_idx, beta2, eps, lr, c, m["norms"], m["Wb"],
                             None), m["d"], m["k"])
@@ -444,6 +448,7 @@ def run_ours(args):
                     if st is not ast:
                         ast.wait_stream(st)
                 with torch.cuda.stream(ast):
+                    arenas[li].allreduce()
                     timed(ev, "apply", ast, lambda: L.logra_rowadam_apply_group(
                         group_items(lm), step_idx, beta2, eps), li, len(lm))
         for st in sts[1:]:
@@ -557,8 +562,7 @@ def run_ours(args):
                     m["S"].zero_()
                 L.logra_sketch_accumulate_group([{"X": m["X"][mb], "dY": m["dY"][mb], "S": m["S"],
                                                   "seed": m["seed"]} for m in lm for mb in range(nmb)], step_idx)
-                for m in lm:
-                    dp.allreduce_sketch(m["S"])
+                lm[0]["arena"].allreduce()
                 L.logra_rowadam_apply_group(group_items(lm), step_idx, beta2, eps)
 
         group_step(args.warmup + args.steps + 20)
@@ -799,8 +803,7 @@ def run_e2e(args, L, dp, mats, w, r, dt, dev, stream, sk_f, world, layer_mats, g
                 ev.record(stream)
                 done[slot] = ev
                 i += 1
-            for m in lm:
-                dp.allreduce_sketch(m["S"])
+            lm[0]["arena"].allreduce()
             if args.apply_mode == "single":
                 for m in lm:
                     L.logra_rowadam_apply_ex(m["W"], m["S"], m["v"], m["seed"], step_idx, beta2, eps, lr, c,

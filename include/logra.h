@@ -161,7 +161,7 @@ typedef struct logra_sketch_item {
  *   items   HOST array of `count` items, read during the call only.  Items may
  *           share an S (microbatches of one matrix): S is updated with atomic
  *           additions, so their sum is formed in an unspecified order.
- * The library forks the sketches round robin onto up to 8 side streams of its
+ * The library forks the sketches round robin onto up to 16 side streams of its
  * own (created on the device's first group call and kept), shapes their
  * launches as for logra_set_concurrency(number of side streams used), and
  * joins the side streams back into `stream` before returning: work issued on

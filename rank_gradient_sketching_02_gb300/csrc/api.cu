@@ -344,7 +344,7 @@ int logra_sketch_accumulate(const void* X, const void* dY, int in_dtype, int64_t
 
 // Side streams of the grouped sketch, per device: created on first use and kept.
 namespace {
-constexpr int kSideStreams = 8;
+constexpr int kSideStreams = 16;
 struct SideStreams {
   cudaStream_t s[kSideStreams] = {};
   cudaEvent_t fork = nullptr;

@@ -25,7 +25,9 @@ def test_defaults_match_the_contract():
     import bench
     a = bench.parse_args([])
     assert (a.gpus, a.impl, a.warmup >= 3, a.steps >= 1) == (1, "ours", True, True)
-    assert a.workload == "model7b" and a.rank == 256
+    assert a.workload == "model7b" and a.rank is None and a.streams == 16
+    from rank_gradient_sketching_02_gb300 import synth
+    assert synth.WORKLOADS[a.workload].r == 256          # the rank of the 7B-class configuration
 
 
 def test_reference_arm_prints_one_complete_line():
@@ -44,7 +46,7 @@ def test_reference_arm_prints_one_complete_line():
     from rank_gradient_sketching_02_gb300 import synth
     w = synth.WORKLOADS["tiny"]
     # the same config object as the GPU arm builds for this workload
-    assert d["config"] == bench.workload_config(w, w.layers, w.microbatches, 256, 1, 1)
+    assert d["config"] == bench.workload_config(w, w.layers, w.microbatches, w.r, 1, 1)
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     e = d["e2e"]

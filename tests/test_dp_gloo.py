@@ -99,3 +99,63 @@ def test_shard_microbatches_partition():
     for world in (1, 2, 3, 8):
         got = sorted(i for r in range(world) for i in dp.shard_microbatches(16, r, world))
         assert got == list(range(16))
+
+
+ARENA_D = (24, 8, 64, 8, 8, 96)    # several matrices of one rank r, packed into one buffer
+
+
+def _worker_arena(rank, world, port, out):
+    from rank_gradient_sketching_02_gb300 import dp
+    _init(rank, world, port)
+    # buckets of at most two 24 x 32 sketches' worth of bytes: 24 + 8 rows share one, the 64-row
+    # sketch is one of its own, 8 + 8 rows share one and the 96-row sketch (larger than a bucket)
+    # is one of its own: four collectives
+    arena = dp.SketchArena(ARENA_D, R, bucket_bytes=2 * 24 * R * 4)
+    arena.flat.fill_(7.0)
+    arena.zero_()                  # the first microbatch of a step adds into zeros
+    for m, d in enumerate(ARENA_D):
+        S = np.zeros((d, R))
+        for i in dp.shard_microbatches(MBS, rank, world):
+            X, dY = _microbatches()[i]
+            S = O.sketch_accumulate(S, X, dY[:, :1].repeat(d, axis=1) * (m + 1), 20 + m, 3, R)
+        arena[m].copy_(torch.from_numpy(S).float())
+    arena.allreduce()
+    np.save(os.path.join(out, f"A{rank}.npy"), arena.flat.numpy())
+    np.save(os.path.join(out, f"buckets{rank}.npy"), np.array(arena.buckets))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_arena_exchange_in_buckets_equals_single_rank_sketches(tmp_path):
+    port = _free_port()
+    mp.start_processes(_worker_arena, args=(2, port, str(tmp_path)), nprocs=2, start_method="spawn")
+    want = []
+    for m, d in enumerate(ARENA_D):
+        S = np.zeros((d, R))
+        for X, dY in _microbatches():
+            S = O.sketch_accumulate(S, X, dY[:, :1].repeat(d, axis=1) * (m + 1), 20 + m, 3, R)
+        want.append(S.astype(np.float32).astype(np.float64).ravel())
+    want = np.concatenate(want)
+    buckets = np.load(tmp_path / "buckets0.npy")
+    assert [tuple(b[2:]) for b in buckets] == [(0, 2), (2, 3), (3, 5), (5, 6)] and buckets[-1][1] == want.size
+    for rank in range(2):
+        got = np.load(tmp_path / f"A{rank}.npy").astype(np.float64)
+        # each rank's shard was rounded to fp32 before the sum: fp32-sized differences only
+        np.testing.assert_allclose(got, want, rtol=1e-5, atol=1e-6 * np.abs(want).max())
+
+
+def test_arena_views_layout():
+    from rank_gradient_sketching_02_gb300 import dp
+    a = dp.SketchArena((3584, 512, 18944), 256, bucket_bytes=16 << 20)
+    assert [tuple(s.shape) for s in a.S] == [(3584, 256), (512, 256), (18944, 256)]
+    assert all(s.data_ptr() % 16 == 0 and s.is_contiguous() for s in a.S)
+    assert a.S[1].data_ptr() == a.S[0].data_ptr() + 3584 * 256 * 4          # views of one buffer
+    a.S[2].fill_(1.0)
+    assert float(a.flat.sum()) == 18944 * 256
+    a.zero_()
+    assert float(a.flat.abs().sum()) == 0.0
+    # 3.7 MB + 0.5 MB share a bucket; the 19.4 MB sketch is a bucket of its own
+    assert [b[2:] for b in a.buckets] == [(0, 2), (2, 3)]
+    assert [a.bucket_of(i) for i in range(3)] == [0, 0, 1]
+    with pytest.raises(ValueError):
+        dp.SketchArena((8,), 48)
