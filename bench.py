@@ -23,7 +23,8 @@ workloads remain available.  The metric is sketch TFLOP/s over the whole step (a
 sketch FLOPs 2 n r (k + d) per matrix-microbatch, divided by the step time
 including the apply), with the apply's GB/s and both kernels' roofline
 fractions alongside.  The matrices are independent, so the step issues them
-round robin on --streams CUDA streams (default 16); per-call durations (the
+round robin on --streams CUDA streams (default 16, 8 for workloads of fewer than 16
+matrices); per-call durations (the
 components and the dominant call's roofline) come from one extra step on a
 single stream right after the timed region; the apply component also reports all of a
 step's apply calls issued at once on up to --apply-streams streams (default 7), and
@@ -79,8 +80,11 @@ def parse_args(argv=None):
     p.add_argument("--input-layers", type=int, default=4,
                    help="distinct layers of resident inputs; layer l reads the inputs of slot l mod this "
                         "(0: every layer its own inputs)")
-    p.add_argument("--streams", type=int, default=16,
-                   help="CUDA streams the matrices are issued on, round robin (each keeps its own workspace)")
+    p.add_argument("--streams", type=int, default=None,
+                   help="CUDA streams the matrices are issued on, round robin (each keeps its own workspace); "
+                        "default 16 for workloads of at least 16 matrices per step, else 8")
+    p.add_argument("--hint", type=int, default=None,
+                   help="concurrency hint given to the library (default: the stream count)")
     p.add_argument("--apply-streams", type=int, default=7,
                    help="streams for the all-applies-at-once measurement (each with its own workspace)")
     p.add_argument("--spread", choices=("auto", "on", "off"), default="auto",
@@ -374,7 +378,9 @@ def run_ours(args):
     # The matrices are independent, so they are issued round robin on `--streams` CUDA streams (each
     # with its own library workspace): one matrix's launches fill the SMs that another's leave idle
     # in its tails and launch gaps.  Each matrix's own calls stay in order on one stream.
-    streams = [stream] + [torch.cuda.Stream(device=dev) for _ in range(max(1, args.streams) - 1)]
+    nstreams = args.streams or (16 if len(mats) >= 16 else 8)
+    streams = [stream] + [torch.cuda.Stream(device=dev) for _ in range(max(1, nstreams) - 1)]
+    hint = args.hint or len(streams)
     for st in streams:
         with torch.cuda.stream(st):
             L.logra_reserve_workspace(ws)
@@ -460,7 +466,7 @@ def run_ours(args):
 
     # the step issues sketch calls on len(streams) streams at once: tell the library, so that
     # each call's accumulate leaves SMs to the other streams (the launch shape only)
-    L.logra_set_concurrency(len(streams))
+    L.logra_set_concurrency(hint)
     for s in range(args.warmup):
         one_step(s)
     torch.cuda.synchronize()
@@ -583,7 +589,7 @@ def run_ours(args):
     # costs on top of the GPU work.
     graph_comp = None
     if not args.graph and not args.no_graph and world == 1:
-        L.logra_set_concurrency(len(streams))
+        L.logra_set_concurrency(hint)
         g, g_launch = capture_step(args.warmup + args.steps + 8)
         g0 = torch.cuda.Event(enable_timing=True)
         g1 = torch.cuda.Event(enable_timing=True)
@@ -637,7 +643,7 @@ def run_ours(args):
                              "(cuBLAS) for dX then logra_sketch_accumulate; one stream, CUDA events, "
                              "median of 5 after 3 warm-ups"}
         del dXb, Sb
-        L.logra_set_concurrency(len(streams))
+        L.logra_set_concurrency(hint)
 
     elapsed_ms = t_start.elapsed_time(t_end)
     if world > 1:
@@ -704,7 +710,7 @@ def run_ours(args):
                                "sign matrices are per layer") if pool < layers else "every layer its own inputs",
                 "input_generation_ms": gen_ms,
                 "streams": len(streams), "apply_mode": args.apply_mode,
-                "microbatches_spread_over_streams": bool(spread), "concurrency_hint": len(streams),
+                "microbatches_spread_over_streams": bool(spread), "concurrency_hint": hint,
                 "cuda_graph": bool(args.graph),
                 "component_timing": "components and roofline: CUDA events around each call in one "
                 "extra step issued on a single stream right after the timed region"},

@@ -21,7 +21,7 @@
 // exact row norms before the update pass uses it.
 //
 // Operands: A = the row block of S, pre-split into bf16 hi/lo and pre-swizzled
-// (one bulk copy per 64-wide rank chunk); B = Sigma rows of that chunk for the
+// (one bulk copy per 32-wide rank chunk); B = Sigma rows of that chunk for the
 // super-tile's 256 columns, MN-major, generated in shared memory from the sign
 // hash (mode 4: the M image by bulk copy).  W moves in by TMA in 128 x 32
 // sub-tiles through a 3-stage ring whose stages are released as soon as the
@@ -48,13 +48,18 @@ namespace {
 
 constexpr int kRows = 128;        // MMA M: rows of W per block
 constexpr int kCols = 256;        // MMA N: columns per super-tile
-constexpr int kRc = 64;           // ranks per K chunk
+// Ranks per K chunk.  A chunk of 32 ranks (16 KB of S image, 16 KB of sign
+// tile) lets four stages fit where two 64-rank stages did: the producers then
+// have three chunks of MMA time, not one, to refill a stage (bulk copy from L2
+// plus sign generation), which at r = 512 held the MMAs back.
+constexpr int kRc = 32;
+constexpr int kARow = kRc * 2;    // bytes per row of an A chunk (64: SWIZZLE_64B, K-major)
 constexpr int kSub = 32;          // epilogue sub-tile width (columns)
-constexpr int kAbStages = 2;      // A/B stages of the update and rebuild passes
-constexpr int kAbStagesNorm = 2;  // row norms: two 96 KB stages (S chunk + M hi + M lo) in the A/B, W ring and staging space
+constexpr int kAbStages = 4;      // A/B stages of the update and rebuild passes
+constexpr int kAbStagesNorm = 4;  // row norms: four 48 KB stages (S chunk + M hi + M lo) in the A/B, W ring and staging space
 constexpr int kWStages = 3;
-constexpr uint32_t kABytes = 2 * kRows * 128;   // hi + lo: 32 KB
-constexpr uint32_t kBBytes = kRc * kCols * 2;   // 64 ranks x 256 columns bf16: 32 KB
+constexpr uint32_t kABytes = 2 * kRows * kARow; // hi + lo: 16 KB
+constexpr uint32_t kBBytes = kRc * kCols * 2;   // 32 ranks x 256 columns bf16: 16 KB
 constexpr uint32_t kWBytes = kRows * kSub * 4;  // fp32 sub-tile: 16 KB
 constexpr uint32_t kHBytes = kRows * kSub * 2;  // bf16 sub-tile: 8 KB
 
@@ -118,7 +123,7 @@ struct ApplyArgs {
   int nm;
   int r;
   int inner;                  // super-tiles per unit: 1, or nsuper in mode 4
-  int nck;                    // 64-rank chunks
+  int nck;                    // rank chunks of kRc
   float scale;                // 1 / sqrt(r)       (rebuild)
   float beta2, eps;
   int accumulate;             // rebuild: add into the output
@@ -147,7 +152,7 @@ __global__ void __launch_bounds__(480, 1)
   const unsigned long long limit = ctl->wait_limit;
   constexpr bool kNorm = (MODE == 4);
   constexpr int AS = kNorm ? kAbStagesNorm : kAbStages;   // mode 4 uses no W ring or staging
-  // a stage holds one 64-rank chunk of the S image and its B operand: the sign
+  // a stage holds one rank chunk of the S image and its B operand: the sign
   // tile, or (mode 4) both terms of the Gram image, so each S chunk loads once
   constexpr uint32_t kStageB = kNorm ? kABytes + 2 * kBBytes : kABytes + kBBytes;
   const int nchunks = A.nck;
@@ -260,7 +265,7 @@ __global__ void __launch_bounds__(480, 1)
       int buf = 0;
       const uint32_t idesc = idesc_bf16(kRows, kCols, 0, 1);
       // stage-0 descriptors, advanced by adds of the 16-byte-unit address field
-      const uint64_t adesc0 = smem_desc(smem_addr(ab), 16, 1024, kSw128);
+      const uint64_t adesc0 = smem_desc(smem_addr(ab), 16, 8 * kARow, kSw64);
       const uint64_t bdesc0 = smem_desc(smem_addr(ab + kABytes), kRc * 128, 1024, kSw128);
       for (int u = blockIdx.x; u < units && !sh->abort; u += gridDim.x) {
         for (int t = 0; t < A.inner; ++t) {
@@ -275,7 +280,7 @@ __global__ void __launch_bounds__(480, 1)
             const uint64_t bd = bdesc0 + uint64_t(uint32_t(stage) * (kStageB >> 4));
             const int ksteps = min(kRc, A.r - c * kRc) / 16;
             for (int ks = 0; ks < ksteps; ++ks) {
-              const uint64_t a_hi = ad + uint64_t(2 * ks), a_lo = a_hi + uint64_t((kRows * 128) >> 4);
+              const uint64_t a_hi = ad + uint64_t(2 * ks), a_lo = a_hi + uint64_t((kRows * kARow) >> 4);
               const uint64_t b = bd + uint64_t(ks * (2048 >> 4));
               mma_bf16(dt, a_hi, b, idesc, (c | ks) ? 1u : 0u);
               mma_bf16(dt, a_lo, b, idesc, 1u);
@@ -561,7 +566,7 @@ __global__ void __launch_bounds__(480, 1)
         for (int c = 0; c < nchunks; ++c) {
           if (!warp_wait(sh, &sh->ab_empty[stage], phase ^ 1u, limit, ctl)) goto gen_done;
           uint8_t* bt = ab + stage * kStageB + kABytes;
-          // 4 groups of 64 columns x 64 rank rows; row = one sign word (64 columns)
+          // 4 groups of 64 columns x kRc rank rows; row = one sign word (64 columns)
           for (int e = gtid; e < 4 * kRc; e += 128) {
             const int grp = e / kRc, a_l = e % kRc;
             const int a = c * kRc + a_l;
@@ -589,14 +594,14 @@ __global__ void __launch_bounds__(480, 1)
   }
 }
 
-// S image for the A operand: rows split into bf16 hi + lo, 64-rank chunks of
-// 128-byte rows, 16-byte chunk q of row i stored at q ^ (i & 7).  Element e
-// is one (row, chunk, 8-rank group).
+// S image for the A operand: rows split into bf16 hi + lo, 32-rank chunks of
+// 64-byte rows (the SWIZZLE_64B K-major layout), 16-byte unit q of row i
+// stored at q ^ ((i >> 1) & 3).  Element e is one (row, chunk, 8-rank group).
 __device__ __forceinline__ void s_image_elem(const float* __restrict__ S, int64_t d, int r, int nchunks,
                                              uint8_t* __restrict__ img, int64_t e) {
-  const int q = int(e & 7);
-  const int c = int((e >> 3) % nchunks);
-  const int64_t row = (e >> 3) / nchunks;
+  const int q = int(e & 3);
+  const int c = int((e >> 2) % nchunks);
+  const int64_t row = (e >> 2) / nchunks;
   // r is a multiple of 32: the 8 ranks of an element are all inside or all outside
   float v[8];
   if (row < d && c * kRc + q * 8 < r) {
@@ -620,9 +625,9 @@ __device__ __forceinline__ void s_image_elem(const float* __restrict__ S, int64_
   const int64_t rb = row / kRows;
   const int rl = int(row % kRows);
   uint8_t* chunk = img + (size_t(rb) * nchunks + c) * kABytes;
-  const int off = rl * 128 + ((q ^ (rl & 7)) << 4);
+  const int off = rl * kARow + ((q ^ ((rl >> 1) & 3)) << 4);
   *reinterpret_cast<uint4*>(chunk + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-  *reinterpret_cast<uint4*>(chunk + kRows * 128 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  *reinterpret_cast<uint4*>(chunk + kRows * kARow + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
 }
 
 // One block of the Gram pass: M = Sigma Sigma^T, the B operand of the
@@ -639,8 +644,8 @@ __device__ __forceinline__ void s_image_elem(const float* __restrict__ S, int64_
 // 2^17 (hi keeps 8 significant bits, so the integer M - hi is at most 2^8 in
 // magnitude and fits lo's 8 bits); for larger k, lo rounds, an error below
 // 2^-16 of the entry.  Image layout per
-// (256-column super-tile st, 64-rank chunk c, term): a 32 KB MN-major tile of
-// 4 groups of 64 columns x 64 rows of 128 bytes, 16-byte chunk q of row a
+// (256-column super-tile st, 32-rank chunk c, term): a 16 KB MN-major tile of
+// 4 groups of 64 columns x 32 rows of 128 bytes, 16-byte chunk q of row a
 // stored at q ^ (a & 7).  Entries outside r x r are zero.
 constexpr int kGramWords = 64;
 
@@ -708,7 +713,7 @@ __device__ __forceinline__ void gram_block(uint64_t key, int r, int nw, int64_t 
   // the tile's image (and, above the diagonal, the mirrored tile's): 32 rows
   // x 4 sixteen-byte chunks x 2 terms, one whole chunk (8 consecutive
   // columns of one row, one term) per thread
-  const int nck = (r + 63) / 64;
+  const int nck = (r + kRc - 1) / kRc;
   for (int mirror = 0; mirror < ((live && bx > by) ? 2 : 1); ++mirror) {
     const int ra = mirror ? b0 : a0, cb = mirror ? a0 : b0;  // image rows / columns of this tile
     const int term = threadIdx.x >> 7, a = ra + ((threadIdx.x >> 2) & 31), bq = cb + (threadIdx.x & 3) * 8;
@@ -728,9 +733,9 @@ __device__ __forceinline__ void gram_block(uint64_t key, int r, int nw, int64_t 
       packed[i] = two;
     }
     const int st = bq >> 8, grp = (bq >> 6) & 3, q = (bq >> 3) & 7;
-    const int c = a >> 6, a_l = a & 63;
-    uint8_t* tile = mimg + ((size_t(st) * nck + c) * 2 + term) * 32768;
-    *reinterpret_cast<uint4*>(tile + grp * 8192 + a_l * 128 + ((q ^ (a_l & 7)) << 4)) =
+    const int c = a / kRc, a_l = a % kRc;
+    uint8_t* tile = mimg + ((size_t(st) * nck + c) * 2 + term) * kBBytes;
+    *reinterpret_cast<uint4*>(tile + grp * (kRc * 128) + a_l * 128 + ((q ^ (a_l & 7)) << 4)) =
         make_uint4(packed[0], packed[1], packed[2], packed[3]);
   }
 }
@@ -769,11 +774,13 @@ __global__ void __launch_bounds__(256) apply_prep_kernel(const __grid_constant__
   const int64_t nb = int64_t(gridDim.x) - P.ngram;
   for (int mi = 0; mi < P.nm; ++mi) {
     const PrepMat& M = P.m[mi];
-    const int64_t total = ((M.d + kRows - 1) / kRows) * kRows * P.nck * 8;
+    const int64_t total = ((M.d + kRows - 1) / kRows) * kRows * P.nck * (kRc / 8);
     for (int64_t e = (int64_t(b) - P.ngram) * blockDim.x + threadIdx.x; e < total; e += nb * blockDim.x)
       s_image_elem(M.S, M.d, P.r, P.nck, M.img, e);
   }
 }
+
+size_t gram_image_bytes(int r) { return size_t((r + kCols - 1) / kCols) * ((r + kRc - 1) / kRc) * 2 * kBBytes; }
 
 size_t s_image_bytes(int64_t d, int r) {
   const int64_t rb = (d + kRows - 1) / kRows;
@@ -788,7 +795,7 @@ int launch_apply_prep(const PrepMatLaunch* mats, int nm, int r, bool gram, cudaS
   P.r = r;
   P.nck = (r + kRc - 1) / kRc;
   P.gx = gram ? ((r + 255) / 256) * 8 : 0;
-  P.gy = gram ? ((r + 63) / 64) * 2 : 0;
+  P.gy = gram ? ((r + kRc - 1) / kRc) * (kRc / 32) : 0;
   int64_t total = 0, ngram = 0;
   for (int i = 0; i < nm; ++i) {
     PrepMat& M = P.m[i];
@@ -804,7 +811,7 @@ int launch_apply_prep(const PrepMatLaunch* mats, int nm, int r, bool gram, cudaS
     M.S = mats[i].S;
     M.img = mats[i].img;
     ngram += int64_t(P.gx) * P.gy * M.gz;
-    total += ((M.d + kRows - 1) / kRows) * kRows * P.nck * 8;
+    total += ((M.d + kRows - 1) / kRows) * kRows * P.nck * (kRc / 8);
   }
   if (ngram > (int64_t(1) << 30)) return LOGRA_ERR_UNSUPPORTED;
   P.ngram = int(ngram);

@@ -1,5 +1,5 @@
-// Sign-matrix kernels: explicit A (for tests / callers); the size of the Gram
-// image (the Gram pass itself runs in the apply's prep launch, apply_tc.cu).
+// Sign-matrix kernel: explicit A (for tests / callers).  The in-kernel sign
+// tiles and the Gram pass live with the kernels that use them.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -19,8 +19,6 @@ __global__ void sign_matrix_kernel(uint64_t key, int r, int64_t k, float scale, 
     A[e] = __uint_as_float(__float_as_uint(scale) ^ (bit << 31));
   }
 }
-
-size_t gram_image_bytes(int r) { return size_t((r + 255) / 256) * ((r + 63) / 64) * 2 * 32768; }
 
 int launch_sign_matrix(uint64_t key, int r, int64_t k, float scale, float* A, cudaStream_t s) {
   const int64_t total = int64_t(r) * k;

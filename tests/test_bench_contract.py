@@ -25,7 +25,7 @@ def test_defaults_match_the_contract():
     import bench
     a = bench.parse_args([])
     assert (a.gpus, a.impl, a.warmup >= 3, a.steps >= 1) == (1, "ours", True, True)
-    assert a.workload == "model7b" and a.rank is None and a.streams == 16
+    assert a.workload == "model7b" and a.rank is None and a.streams is None
     from rank_gradient_sketching_02_gb300 import synth
     assert synth.WORKLOADS[a.workload].r == 256          # the rank of the 7B-class configuration
 

@@ -80,3 +80,41 @@ def test_two_ranks_allreduce_library_sketches(tmp_path):
     W0, W1 = np.load(tmp_path / "W0.npy"), np.load(tmp_path / "W1.npy")
     assert np.array_equal(W0.view(np.uint32), W1.view(np.uint32))
     assert np.any(W0)
+
+
+def test_arena_views_are_library_sketches():
+    """The sketches of several matrices as views of one dp.SketchArena buffer: each view is a
+    16-byte-aligned d x r tensor the library adds into like any other S, a fill zeroes them all,
+    and a grouped apply reads them in place.  Views must not bleed into their neighbours."""
+    import torch
+    from rank_gradient_sketching_02_gb300 import build as B
+    from rank_gradient_sketching_02_gb300 import dp
+    B.build()
+    import rank_gradient_sketching_02_gb300 as L
+    shapes = [(264, 520), (72, 1032), (1032, 264)]              # (d, k) of three matrices
+    arena = dp.SketchArena([d for d, _ in shapes], R, device="cuda")
+    arena.flat.fill_(3.0)
+    arena.zero_()
+    n, want = 300, []
+    for m, (d, k) in enumerate(shapes):
+        S_or = np.zeros((d, R))
+        for mb in range(2):
+            X, dY, _ = synth.host_microbatch(n, d, k, dy_kind="lognormal", mask_frac=0.25, key=(32, m, mb))
+            Xd, dYd = synth.to_bf16_bits(X).cuda(), synth.to_bf16_bits(dY).cuda()
+            L.logra_sketch_accumulate(Xd, dYd, arena[m], 70 + m, STEP)
+            S_or = O.sketch_accumulate(S_or, Xd.double().cpu().numpy(), dYd.double().cpu().numpy(), 70 + m, STEP, R)
+        want.append(S_or)
+    Ws = [torch.zeros((d, k), device="cuda") for d, k in shapes]
+    vs = [torch.zeros(d, device="cuda") for d, _ in shapes]
+    items = [{"W": Ws[m], "S": arena[m], "v": vs[m], "seed": 70 + m, "lr": 1e-5, "c": 1.0}
+             for m in range(len(shapes))]
+    L.logra_rowadam_apply_group(items, STEP, 0.999, 1e-8)
+    torch.cuda.synchronize()
+    assert L.logra_get_status() == 0
+    b2, eps, lr = (float(np.float32(x)) for x in (0.999, 1e-8, 1e-5))
+    for m, (d, k) in enumerate(shapes):
+        S = arena[m].double().cpu().numpy()
+        assert np.linalg.norm(S - want[m]) / np.linalg.norm(want[m]) <= 1e-3, m
+        _, _, _, dW_or = O.rowadam_apply(np.zeros((d, k)), S, np.zeros(d), 70 + m, STEP, b2, eps, lr, 1.0)
+        W = Ws[m].double().cpu().numpy()
+        assert np.linalg.norm(W - dW_or) / np.linalg.norm(dW_or) <= 1e-5, m
