@@ -84,3 +84,41 @@ def test_fullsize_sampled_sketch_and_apply(L, label, d, k, r, mbs, mask):
     m = (vg - b2 * v0.astype(np.float64)) / (1.0 - b2)
     want_dw2 = (lr * c) ** 2 * float(np.sum(k * m / (vg + eps)))
     assert abs(nr[1] - want_dw2) <= 1e-4 * want_dw2
+
+
+HINT_CASES = [
+    # (label, d, k): the 7B-class shapes the default bench step issues on 16 streams
+    ("7b-gate", 18944, 3584),
+    ("7b-down", 3584, 18944),
+    ("7b-k", 512, 3584),
+]
+
+
+@pytest.mark.parametrize("label,d,k", HINT_CASES, ids=[c[0] for c in HINT_CASES])
+def test_fullsize_sampled_sketch_in_the_benchs_launch_shape(L, label, d, k):
+    """The step's launch shape: concurrency hint 16, so the projection runs one CTA per 256-token
+    group over the whole k range and writes the accumulate's image itself, and the accumulate
+    takes fewer, longer CTA-pair ranges.  Sampled columns of S against the oracle, 8192-token
+    microbatches, r = 256."""
+    import torch
+    n, r = 8192, 256
+    seed, step = synth.matrix_seed(2026, 11, 2), 4
+    S = torch.zeros((d, r), dtype=torch.float32, device="cuda")
+    cols = np.random.default_rng(d + 7 * k).choice(r, size=3, replace=False)
+    want_cols = np.zeros((d, len(cols)))
+    L.logra_set_concurrency(16)
+    try:
+        for mb in range(2):
+            X, dY, _ = synth.host_microbatch(n, d, k, dy_kind="lognormal", mask_frac=0.25, key=(10, d, k, mb))
+            Xb, dYb = synth.to_bf16_bits(X), synth.to_bf16_bits(dY)
+            del X, dY
+            L.logra_sketch_accumulate(Xb.cuda(), dYb.cuda(), S, seed, step)
+            want_cols += O.sketch_columns(Xb.double().numpy(), dYb.double().numpy(), seed, step, r, cols)
+            del Xb, dYb
+        torch.cuda.synchronize()
+    finally:
+        L.logra_set_concurrency(1)
+    assert L.logra_get_status() == 0
+    Sg = S.double().cpu().numpy()
+    assert np.all(np.isfinite(Sg))
+    assert rel(Sg[:, cols], want_cols) <= TOL_S
