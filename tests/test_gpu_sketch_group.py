@@ -107,3 +107,26 @@ def test_group_rejects_mixed_token_counts(L):
              dY=torch.zeros((32, 64), dtype=torch.bfloat16, device="cuda"))
     with pytest.raises(ValueError):
         L.logra_sketch_accumulate_group([a, b], 0)
+
+
+def test_group_wider_than_the_side_streams(L):
+    """More items than the library has side streams (16): items wrap around onto streams already in
+    use, and microbatches of one matrix land on different streams and add into one S at once."""
+    import torch
+    n, r, step = 512, 128, 2
+    shapes = [(72 + 8 * (mi % 5), 264 + 64 * (mi % 3), 2) for mi in range(11)]     # 11 matrices, 22 items
+    mats = _case(n, shapes, 91)
+    S = [Guarded((d, r), torch.float32, fill=0.0) for d, _, _ in mats]
+    items = [{"X": X.cuda(), "dY": dY.cuda(), "S": S[mi].t, "seed": 700 + mi}
+             for mi, (_, _, mbs) in enumerate(mats) for X, dY in mbs]
+    assert len(items) > 16
+    L.logra_sketch_accumulate_group(items, step)
+    copies = [g.t.clone() for g in S]            # ordinary work on the caller stream, after the join
+    torch.cuda.synchronize()
+    assert L.logra_get_status() == 0
+    for mi, (d, k, mbs) in enumerate(mats):
+        S[mi].check(f"S of matrix {mi}")
+        want = np.zeros((d, r))
+        for X, dY in mbs:
+            want = O.sketch_accumulate(want, X.double().numpy(), dY.double().numpy(), 700 + mi, step, r)
+        assert rel(copies[mi].cpu().numpy(), want) <= 1e-3, mi
