@@ -110,7 +110,7 @@ int logra_sign_matrix(uint64_t seed, uint64_t step, int r, int64_t k,
  * accumulated in fp32; the X A^T intermediate is kept as a two-term bf16
  * expansion (relative error about 2^-16).  fp32 inputs run on the same
  * tensor-core kernels: each element is split into two bf16 terms
- * x = x1 + x2 (|x - x1 - x2| <= 2^-18 |x|, the two-term bf16 splitting of
+ * x = x1 + x2 (|x - x1 - x2| <= 2^-16 |x|, the two-term bf16 splitting of
  * Henry, Tang & Heinecke, ARITH 2019), the planes are stacked along the
  * tokens as X' = [X1; X2; X1; X2], dY' = [dY1; dY1; dY2; dY2], and the bf16
  * sketch of those 4n tokens adds all four cross terms; fp32 inputs must be

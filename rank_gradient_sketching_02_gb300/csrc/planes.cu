@@ -3,18 +3,19 @@
 // The sketch is S += dY^T (X A^T) (theclarity.today write-up, "Why it
 // matters": S = G A^T with G = dY^T X).  For fp32 X and dY each element is
 // split into two bf16 terms, x = x1 + x2 + e with x1 = RN_bf16(x) and
-// x2 = RN_bf16(x - x1), where x - x1 is exact in fp32 and |e| <= 2^-18 |x|
-// (the two-term splitting of Henry, Tang & Heinecke, "Leveraging the
+// x2 = RN_bf16(x - x1), where x - x1 is exact in fp32 and |e| <= u^2 |x| =
+// 2^-16 |x| for bf16's unit roundoff u = 2^-8 (about 2.5e-6 |x| root-mean-
+// square): the two-term splitting of Henry, Tang & Heinecke, "Leveraging the
 // bfloat16 Artificial Intelligence Datatype For Higher-Precision
-// Computations", ARITH 2019).  Stacking the planes along the token axis,
+// Computations", ARITH 2019.  Stacking the planes along the token axis,
 //
 //   X' = [X1; X2; X1; X2],   dY' = [dY1; dY1; dY2; dY2]   (4n rows each),
 //
 // makes the bf16 sketch of the 4n stacked tokens equal to
 // (dY1 + dY2)^T ((X1 + X2) A^T): all four cross terms of the two expansions,
-// so the fp32 sketch runs on the same tcgen05 kernels as the bf16 one, with a
-// relative error of a few 2^-18 (the splits and the projection's two-term
-// image of P) on top of the fp32 accumulation.  Inputs must be finite with
+// so the fp32 sketch runs on the same tcgen05 kernels as the bf16 one; with
+// the projection's two-term image of P the sketch comes within about 4e-6 of
+// the exact one in practice, under the 1e-5 bound.  Inputs must be finite with
 // magnitude below bf16's largest finite value (about 3.39e38).
 #include <cuda_bf16.h>
 

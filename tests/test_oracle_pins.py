@@ -138,6 +138,40 @@ def test_sketch_linear_over_microbatches():
     np.testing.assert_allclose(S, S1, rtol=1e-12, atol=1e-12)
 
 
+def test_sketch_of_stacked_two_term_planes():
+    """The identity the fp32-input path rests on: with x = x1 + x2 + e (x1 = RN_bf16(x),
+    x2 = RN_bf16(x - x1), |e| <= u^2 |x| for bf16's unit roundoff u = 2^-8), the sketch of the
+    token-stacked planes [X1; X2; X1; X2] against [dY1; dY1; dY2; dY2] is the sketch of
+    (X1 + X2, dY1 + dY2), and that is well inside the fp32 bound (1e-5) of the sketch of the
+    fp32 inputs themselves."""
+    import torch
+    n, d, k, r = 48, 24, 136, 32
+    g = np.random.default_rng(12)
+    X = g.standard_normal((n, k)).astype(np.float32)
+    dY = (g.standard_normal((n, d)) * np.exp(-7 + 1.5 * g.standard_normal((n, 1)))).astype(np.float32)
+
+    def planes(a):
+        t = torch.from_numpy(a)
+        hi = t.to(torch.bfloat16).float()
+        lo = (t - hi).to(torch.bfloat16).float()      # t - hi is exact in fp32
+        return hi.double().numpy(), lo.double().numpy()
+
+    X1, X2 = planes(X)
+    dY1, dY2 = planes(dY)
+    stacked = O.sketch_accumulate(np.zeros((d, r)), np.concatenate([X1, X2, X1, X2]),
+                                  np.concatenate([dY1, dY1, dY2, dY2]), 9, 2, r)
+    summed = O.sketch_accumulate(np.zeros((d, r)), X1 + X2, dY1 + dY2, 9, 2, r)
+    exact = O.sketch_accumulate(np.zeros((d, r)), X.astype(np.float64), dY.astype(np.float64), 9, 2, r)
+    np.testing.assert_allclose(stacked, summed, rtol=1e-12, atol=1e-12 * np.abs(summed).max())
+    assert np.all(np.abs(X1 + X2 - X) <= 2.0 ** -16 * np.abs(X))
+    assert np.all(np.abs(dY1 + dY2 - dY) <= 2.0 ** -16 * np.abs(dY))
+    err = np.linalg.norm(summed - exact) / np.linalg.norm(exact)
+    assert 0 < err <= 1e-5, err
+    # one plane alone (bf16 inputs) is two orders worse: the second plane carries the fp32 accuracy
+    one = O.sketch_accumulate(np.zeros((d, r)), X1, dY1, 9, 2, r)
+    assert np.linalg.norm(one - exact) / np.linalg.norm(exact) > 100 * err
+
+
 def test_sketch_padding_rows_contribute_nothing():
     n, d, k, r = 40, 9, 128, 8
     X, dY = _tiny(n, d, k, seed=4)
