@@ -87,21 +87,23 @@ def test_fullsize_sampled_sketch_and_apply(L, label, d, k, r, mbs, mask):
 
 
 HINT_CASES = [
-    # (label, d, k): the 7B-class shapes the default bench step issues on 16 streams
-    ("7b-gate", 18944, 3584),
-    ("7b-down", 3584, 18944),
-    ("7b-k", 512, 3584),
+    # (label, d, k, r): shapes the bench's multi-matrix steps issue on 16 streams
+    ("7b-gate", 18944, 3584, 256),
+    ("7b-down", 3584, 18944, 256),
+    ("7b-k", 512, 3584, 256),
+    ("27b-gate", 27648, 5120, 256),
+    ("27b-kv-r512", 1024, 5120, 512),
 ]
 
 
-@pytest.mark.parametrize("label,d,k", HINT_CASES, ids=[c[0] for c in HINT_CASES])
-def test_fullsize_sampled_sketch_in_the_benchs_launch_shape(L, label, d, k):
+@pytest.mark.parametrize("label,d,k,r", HINT_CASES, ids=[c[0] for c in HINT_CASES])
+def test_fullsize_sampled_sketch_in_the_benchs_launch_shape(L, label, d, k, r):
     """The step's launch shape: concurrency hint 16, so the projection runs one CTA per 256-token
     group over the whole k range and writes the accumulate's image itself, and the accumulate
     takes fewer, longer CTA-pair ranges.  Sampled columns of S against the oracle, 8192-token
-    microbatches, r = 256."""
+    microbatches."""
     import torch
-    n, r = 8192, 256
+    n = 8192
     seed, step = synth.matrix_seed(2026, 11, 2), 4
     S = torch.zeros((d, r), dtype=torch.float32, device="cuda")
     cols = np.random.default_rng(d + 7 * k).choice(r, size=3, replace=False)
