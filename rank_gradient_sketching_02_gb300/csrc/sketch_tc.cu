@@ -71,7 +71,7 @@ struct SketchShape {
   int x_stages, g_stages;      // project rings: X tiles, sign tiles
   int a_stages, b_stages;      // accumulate rings: P^T chunks, dY tiles
   // accumulate on CTA pairs (r_pad 256 or 512): rank blocks of 256 and d blocks
-  // of 256 per pair tile (prb * pdb = 2), pair tiles along d, pairs (clusters)
+  // of 256 per pair tile (prb * pdb = 2, or 1 for narrow d on one stream), pair tiles along d, pairs (clusters)
   int pair, prb, pdb, pdtiles, pairs;
   int direct;                  // every projection segment covers the whole k range: the projection
                                // writes the accumulate's hi/lo image itself and the split is skipped
@@ -742,8 +742,9 @@ __global__ void __launch_bounds__(352, 1)
 // its own half of every operand (its 128 ranks of each 256-rank block of the
 // P^T chunk, its 128 d-columns of each 256-column block of the dY tile), and
 // the hardware hands the B halves across the pair.  A pair tile is
-// 256 prb ranks x 256 pdb d-columns with prb * pdb = 2, so each CTA's TMEM
-// holds two 128 x 256 fp32 accumulators (512 columns); per 32-token chunk a
+// 256 prb ranks x 256 pdb d-columns with prb * pdb = 2 (1 for narrow matrices on
+// one stream), so each CTA's TMEM holds two 128 x 256 fp32 accumulators (one
+// when prb * pdb = 1; 512 columns are allocated either way); per 32-token chunk a
 // CTA takes in 32 KB (prb 1) or 40 KB (prb 2) of operands for 1024 MMA cycles,
 // against 48 KB (r_pad 256) or 72 KB (r_pad 512) on a single CTA, which is
 // what limits the single-CTA kernel (operand ingest, not the tensor pipe).
@@ -877,10 +878,12 @@ __global__ void __launch_bounds__(352, 1)
           const uint64_t ad = adesc0 + uint64_t(uint32_t(ar.stage) * (a_bytes >> 4));
           const uint64_t bd = bdesc0 + uint64_t(uint32_t(br.stage) * (b_bytes >> 4));
           const uint32_t first = (c == c0) ? 0u : 1u;
-          if (RB == 1)
+          if (RB == 1 && DB == 2)
             accumulate_pair_mmas<1, 2>(tmem, ad, bd, idesc, first);
-          else
+          else if (RB == 2)
             accumulate_pair_mmas<2, 1>(tmem, ad, bd, idesc, first);
+          else
+            accumulate_pair_mmas<1, 1>(tmem, ad, bd, idesc, first);
           mma_commit_pair(&sh->o_empty[ar.stage], 3);
           mma_commit_pair(&sh->s_empty[br.stage], 3);
           ar.next(AS);
@@ -1036,7 +1039,12 @@ static SketchShape plan(int64_t n, int64_t d, int64_t k, int r, int sms) {
   P.pair = (P.r_pad == 256 || P.r_pad == 512) && sms >= 2 ? 1 : 0;
   if (P.pair) {
     P.prb = P.r_pad / 256;
-    P.pdb = 2 / P.prb;
+    // Pair tiles are 256 ranks x 512 d-columns (two accumulators per CTA) at
+    // r_pad 256, except for narrow matrices (d <= 4096) on one stream, where
+    // tiles one d block wide (one accumulator) give twice the tiles to spread
+    // over the SMs: one-stream sketch +1.4%.  Under the concurrency hint the
+    // wide tiles win (28-layer step 920 against 880 TFLOP/s with narrow ones).
+    P.pdb = (P.prb == 1 && hint <= 1 && d <= 4096) ? 1 : 2 / P.prb;
     P.pdtiles = ceil_div(d, P.pdb * 256);
     P.pairs = stream_k_ctas_hinted(int64_t(P.pdtiles) * tchunks, sms / 2, 12, 12 * hint, hint);
     // Prefer a pair count that cuts every tile into equal parts: each pair's
