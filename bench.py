@@ -62,6 +62,9 @@ SKETCH_TRAFFIC_PER_CALL = {
     # (incl. re-zeroing P^T); under the concurrency hint the call moves 397.1 MB (no split, X read once)
     (8192, 18944, 3584, 256): (422.4e6, "ncu dram__bytes_read.sum + dram__bytes_write.sum of the three launches "
                                         "of one 18944x3584 gate call on one stream, kernels as they stand"),
+    # one stream: project 92.35 + 0.10 MB, split 8.40 + 0 MB, accumulate (CTA pairs) 516.65 + 31.62 MB
+    (8192, 27648, 5120, 256): (649.1e6, "ncu dram__bytes_read.sum + dram__bytes_write.sum of the three launches "
+                                        "of one 27648x5120 gate call on one stream, kernels as they stand"),
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
