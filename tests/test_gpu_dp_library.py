@@ -118,3 +118,60 @@ def test_arena_views_are_library_sketches():
         _, _, _, dW_or = O.rowadam_apply(np.zeros((d, k)), S, np.zeros(d), 70 + m, STEP, b2, eps, lr, 1.0)
         W = Ws[m].double().cpu().numpy()
         assert np.linalg.norm(W - dW_or) / np.linalg.norm(dW_or) <= 1e-5, m
+
+
+ARENA_SHAPES = [(264, 520), (1032, 264), (72, 1032)]      # (d, k) of three matrices
+
+
+def _arena_mb(m, i):
+    d, k = ARENA_SHAPES[m]
+    X, dY, _ = synth.host_microbatch(300, d, k, dy_kind="lognormal", mask_frac=0.25, key=(33, m, i))
+    return synth.to_bf16_bits(X), synth.to_bf16_bits(dY)
+
+
+def _arena_worker(rank, world, port, out):
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(0)
+    import rank_gradient_sketching_02_gb300 as L
+    from rank_gradient_sketching_02_gb300 import dp
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=60))
+    # buckets of at most the first sketch's bytes: three collectives, one per sketch
+    arena = dp.SketchArena([d for d, _ in ARENA_SHAPES], R, device="cuda", bucket_bytes=264 * R * 4)
+    arena.zero_()
+    for m in range(len(ARENA_SHAPES)):
+        for i in dp.shard_microbatches(4, rank, world):
+            X, dY = _arena_mb(m, i)
+            L.logra_sketch_accumulate(X.cuda(), dY.cuda(), arena[m], SEED + m, STEP)
+    arena.allreduce()
+    torch.cuda.synchronize()
+    np.save(os.path.join(out, f"A{rank}.npy"), arena.flat.cpu().numpy())
+    with open(os.path.join(out, f"astatus{rank}.txt"), "w") as f:
+        f.write(f"{L.logra_get_status()} {len(arena.buckets)}")
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_ranks_exchange_a_sketch_arena_in_buckets(tmp_path):
+    """Both ranks run the library into views of one dp.SketchArena and exchange it bucket by
+    bucket over gloo: the same bits on both ranks, each sketch within 1e-3 of the oracle sketch of
+    all four microbatches."""
+    import torch.multiprocessing as mp
+    from rank_gradient_sketching_02_gb300 import build as B
+    B.build()
+    mp.start_processes(_arena_worker, args=(2, _free_port(), str(tmp_path)), nprocs=2, start_method="spawn")
+    for rank in range(2):
+        assert (tmp_path / f"astatus{rank}.txt").read_text() == "0 3"
+    A0, A1 = np.load(tmp_path / "A0.npy"), np.load(tmp_path / "A1.npy")
+    assert np.array_equal(A0.view(np.uint32), A1.view(np.uint32))
+    off = 0
+    for m, (d, k) in enumerate(ARENA_SHAPES):
+        want = np.zeros((d, R))
+        for i in range(4):
+            X, dY = _arena_mb(m, i)
+            want = O.sketch_accumulate(want, X.double().numpy(), dY.double().numpy(), SEED + m, STEP, R)
+        got = A0[off:off + d * R].reshape(d, R).astype(np.float64)
+        off += d * R
+        assert np.linalg.norm(got - want) / np.linalg.norm(want) <= 1e-3, m
